@@ -1,0 +1,463 @@
+"""fp64 oracle of the weight-only channel reader (prepare + per-token decode).
+
+TEST INFRASTRUCTURE ONLY -- see the package docstring for who may import it.
+
+Every step follows the two summaries of "Channel Selection for
+Mixture-of-Experts Decoding Needs No Calibration Data":
+[CN] the Chinese summary page (sections 前置知识 / 核心方法 / 方法步骤详情) and
+[KR] the Korean summary page (section 어떻게 쓰나).  Where the pages leave a
+step open, the reading taken is stated in the function's docstring.
+
+Inputs are the stored values: BF16 weights as uint16 bit patterns, fp32 x,
+int32 expert ids, fp32 routing weights and an int8 sign vector.  All method
+arithmetic runs in float64.  Numpy library primitives (matmul, eigh, sort) are
+used as single steps; nothing is blocked, fused or reordered beyond the
+definitions written here.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK = 128          # rotation block: [CN] §方法步骤详情, load-time (1)
+TWN_DELTA = 0.7      # Ternary Weight Networks threshold factor ([CN] §技术新颖性 credits TWN)
+
+
+# --------------------------------------------------------------------------
+# shapes
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Shape:
+    """Layer shape: hidden H, experts E, experts per token topk, expert width I,
+    screened coordinates per block c, recovery rank r."""
+    H: int
+    E: int
+    topk: int
+    I: int
+    c: int = 80
+    r: int = 32
+
+    @property
+    def Hp(self) -> int:
+        """Hidden size zero-padded to whole 128-coordinate blocks."""
+        return BLOCK * math.ceil(self.H / BLOCK)
+
+    @property
+    def nb(self) -> int:
+        return self.Hp // BLOCK
+
+    @property
+    def N(self) -> int:
+        """Routed channels per token: every channel of the token's topk experts
+        ([CN] §核心方法: 8 experts x 768 = 6144 channels for Qwen3-Thinking)."""
+        return self.topk * self.I
+
+
+# --------------------------------------------------------------------------
+# stored-value decoding (exact)
+# --------------------------------------------------------------------------
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact float64 value of BF16 bit patterns (upper half of an fp32)."""
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pad_hidden(a: np.ndarray, Hp: int) -> np.ndarray:
+    """Zero-pad the last axis to Hp (a block that runs past H holds zeros)."""
+    pad = Hp - a.shape[-1]
+    if pad == 0:
+        return a
+    width = [(0, 0)] * (a.ndim - 1) + [(0, pad)]
+    return np.pad(a, width)
+
+
+# --------------------------------------------------------------------------
+# randomized block Hadamard rotation
+# --------------------------------------------------------------------------
+def sylvester_hadamard(n: int = BLOCK) -> np.ndarray:
+    """Sylvester Hadamard matrix, entry (i, j) = (-1)^popcount(i & j)."""
+    i = np.arange(n)
+    anded = np.bitwise_and.outer(i, i)
+    parity = np.zeros_like(anded)
+    v = anded.copy()
+    while v.any():
+        parity ^= v & 1
+        v >>= 1
+    return np.where(parity == 0, 1.0, -1.0)
+
+
+def rotate(a: np.ndarray, sigma: np.ndarray) -> np.ndarray:
+    """R a, applied on the last axis (length Hp = 128 * nb).
+
+    R is block diagonal; block b is R_b = H_128 diag(sigma_b) / sqrt(128), an
+    orthogonal matrix, so g^T x = (R g)^T (R x)  ([CN] §前置知识 "Hadamard旋转与
+    三元Sketch"; [KR] §어떻게 쓰나).  Reading: the randomization is one
+    independent +-1 sign per coordinate (sigma), applied before the Sylvester
+    Hadamard of each block.
+    """
+    Hm = sylvester_hadamard()
+    a = np.asarray(a, dtype=np.float64)
+    nb = a.shape[-1] // BLOCK
+    s = np.asarray(sigma, dtype=np.float64)
+    u = (a * s).reshape(a.shape[:-1] + (nb, BLOCK))
+    out = (u @ Hm.T) / math.sqrt(BLOCK)
+    return out.reshape(a.shape)
+
+
+def butterfly_magnitudes_fp32(x_pad: np.ndarray, sigma: np.ndarray) -> np.ndarray:
+    """|H_128 (sigma * x)| per block, evaluated in fp32 by the Sylvester butterfly.
+
+    This is used ONLY to decide which coordinates the partial screen reads.
+    The decision is taken in the kernel's precision (fp32; the pages fix none)
+    so that both sides make the same integer choice: the transform is the
+    in-place butterfly over strides 1, 2, 4, ..., 64 where element i (bit h
+    clear) and i + h become (a + b, a - b), each rounded to fp32.  The positive
+    1/sqrt(128) factor does not change the order and is omitted.
+    Returns float32 magnitudes of shape [nb, 128].
+    """
+    u = (np.asarray(x_pad, dtype=np.float32) * np.asarray(sigma, dtype=np.float32))
+    u = u.reshape(-1, BLOCK).copy()
+    idx = np.arange(BLOCK)
+    h = 1
+    while h < BLOCK:
+        lo = idx[(idx & h) == 0]
+        hi = lo + h
+        a = u[:, lo].copy()
+        b = u[:, hi].copy()
+        u[:, lo] = a + b
+        u[:, hi] = a - b
+        h *= 2
+    return np.abs(u)
+
+
+def select_coordinates(mag: np.ndarray, c: int) -> np.ndarray:
+    """Partial-screen coordinate set T_b: the c coordinates with the largest
+    |Rx| in each 128-block ([CN] §方法步骤详情, decode (1); [KR] §어떻게 쓰나:
+    80 of 128).  Ties go to the lower coordinate index.  Returns bool [nb, 128].
+    """
+    nb = mag.shape[0]
+    mask = np.zeros((nb, BLOCK), dtype=bool)
+    for b in range(nb):
+        order = np.argsort(-mag[b].astype(np.float64), kind="stable")
+        mask[b, order[:c]] = True
+    return mask
+
+
+# --------------------------------------------------------------------------
+# ternary sketch (load time)
+# --------------------------------------------------------------------------
+def ternarize(wt: np.ndarray):
+    """Ternary code, FP16 scale and FP16 block mean-squared error of rotated blocks.
+
+    wt: float64 [..., 128], one rotated 128-block per leading index.
+    Ternary Weight Networks rule (reading of [CN] §前置知识 / load-time (1): codes
+    in {-1, 0, 1}, an FP16 scale and the block's quantisation MSE rho_b):
+        Delta = 0.7 * mean|w|,  t_i = sign(w_i) if |w_i| > Delta else 0,
+        alpha = mean of |w_i| over {t_i != 0}  (0 if empty), stored FP16,
+        rho   = mean_i (w_i - alpha_fp16 * t_i)^2, stored FP16.
+    Returns (t int8 [..., 128], alpha float16 [...], rho float16 [...]).
+    """
+    absw = np.abs(wt)
+    delta = TWN_DELTA * absw.mean(axis=-1, keepdims=True)
+    support = absw > delta
+    t = np.where(support, np.sign(wt), 0.0)
+    nnz = support.sum(axis=-1)
+    total = np.where(support, absw, 0.0).sum(axis=-1)
+    alpha = np.where(nnz > 0, total / np.maximum(nnz, 1), 0.0)
+    alpha16 = alpha.astype(np.float16)
+    resid = wt - alpha16.astype(np.float64)[..., None] * t
+    rho16 = (resid * resid).mean(axis=-1).astype(np.float16)
+    return t.astype(np.int8), alpha16, rho16
+
+
+def run_bytes(I: int) -> int:
+    """Bytes of one coordinate run of 2-bit codes (I channels, 4 per byte)."""
+    return (I + 3) // 4
+
+
+def run_stride(I: int) -> int:
+    """Run length padded to whole 32-byte sectors."""
+    return 32 * math.ceil(run_bytes(I) / 32)
+
+
+def pack_codes(t: np.ndarray) -> np.ndarray:
+    """2-bit packing of ternary codes along the last axis (channels).
+
+    Code values: 0 -> 0b00, +1 -> 0b01, -1 -> 0b11 (two's complement of the
+    trit).  Channel i sits in byte i // 4 at bits 2 * (i % 4).  The run is
+    zero-padded to a whole number of 32-byte sectors.
+    """
+    I = t.shape[-1]
+    q = np.where(t == 1, 1, np.where(t == -1, 3, 0)).astype(np.uint8)
+    padI = 4 * run_bytes(I)
+    if padI != I:
+        q = np.concatenate([q, np.zeros(q.shape[:-1] + (padI - I,), np.uint8)], axis=-1)
+    q = q.reshape(q.shape[:-1] + (padI // 4, 4))
+    packed = (q[..., 0] | (q[..., 1] << 2) | (q[..., 2] << 4) | (q[..., 3] << 6)).astype(np.uint8)
+    stride = run_stride(I)
+    if stride != packed.shape[-1]:
+        packed = np.concatenate(
+            [packed, np.zeros(packed.shape[:-1] + (stride - packed.shape[-1],), np.uint8)], axis=-1)
+    return packed
+
+
+def unpack_codes(packed: np.ndarray, I: int) -> np.ndarray:
+    """Inverse of pack_codes: int8 trits [..., I]."""
+    b = packed[..., : run_bytes(I)].astype(np.uint8)
+    fields = np.stack([(b >> (2 * k)) & 3 for k in range(4)], axis=-1)
+    fields = fields.reshape(b.shape[:-1] + (4 * b.shape[-1],))[..., :I]
+    out = np.zeros(fields.shape, np.int8)
+    out[fields == 1] = 1
+    out[fields == 3] = -1
+    if np.any(fields == 2):
+        raise ValueError("invalid 2-bit code 0b10")
+    return out
+
+
+@dataclass
+class ExpertSketch:
+    """Sketch of one expert: trits t[gv][I][nb][128] (gv 0 = gate, 1 = up),
+    alpha and rho float16 [nb][2][I]."""
+    t: np.ndarray
+    alpha: np.ndarray
+    rho: np.ndarray
+
+    def packed(self) -> np.ndarray:
+        """Documented layout of one expert: u8 [nb][128][2][run_stride(I)]."""
+        tt = np.transpose(self.t, (2, 3, 0, 1))  # [nb][128][2][I]
+        return pack_codes(tt)
+
+
+def sketch_expert(G_e: np.ndarray, V_e: np.ndarray, sigma: np.ndarray, Hp: int) -> ExpertSketch:
+    """Rotate every gate row g_j and up row v_j in 128-blocks, then ternarise
+    each block ([CN] §方法步骤详情, load-time (1); [KR] §어떻게 쓰나).
+    G_e, V_e: float64 [I][H] (exact BF16 values)."""
+    I = G_e.shape[0]
+    nb = Hp // BLOCK
+    ts, alphas, rhos = [], [], []
+    for W in (G_e, V_e):
+        Wr = rotate(pad_hidden(W, Hp), sigma).reshape(I, nb, BLOCK)
+        t, a, r = ternarize(Wr)
+        ts.append(t)
+        alphas.append(a.T)  # [nb][I]
+        rhos.append(r.T)
+    return ExpertSketch(
+        t=np.stack(ts),                                  # [2][I][nb][128]
+        alpha=np.stack(alphas, axis=1),                  # [nb][2][I]
+        rho=np.stack(rhos, axis=1),
+    )
+
+
+# --------------------------------------------------------------------------
+# down norms and per-layer recovery basis (load time)
+# --------------------------------------------------------------------------
+def down_norms(D_e: np.ndarray) -> np.ndarray:
+    """||d_j|| for every channel j of one expert; D_e float64 [H][I] (column j
+    is d_j).  Stored fp32 ([CN] §方法步骤详情, load-time (2))."""
+    return np.sqrt((D_e * D_e).sum(axis=0)).astype(np.float32)
+
+
+def canonical_signs(U: np.ndarray) -> np.ndarray:
+    """Flip each column so its largest-magnitude entry (first on ties) is positive.
+    The recovery term U U^T v does not depend on this choice."""
+    U = U.copy()
+    for j in range(U.shape[1]):
+        i = int(np.argmax(np.abs(U[:, j])))
+        if U[i, j] < 0:
+            U[:, j] = -U[:, j]
+    return U
+
+
+def recovery_basis(down_blocks, r: int):
+    """Top-r left singular vectors of the layer's stacked down columns.
+
+    [CN] §前置知识 "低秩恢复" and §方法步骤详情 load-time (3): stack the down
+    columns d_j of all experts of one layer and keep the top-32 left singular
+    vectors U.  Computed as the top-r eigenvectors of M = sum_j d_j d_j^T
+    (the same vectors), accumulated expert by expert.
+    down_blocks: iterable of float64 [H][I] arrays (one per expert).
+    Returns (U float16 [H][r], eigenvalues float64 [r] in descending order).
+    """
+    M = None
+    for D_e in down_blocks:
+        part = D_e @ D_e.T
+        M = part if M is None else M + part
+    evals, evecs = np.linalg.eigh(M)
+    order = np.argsort(-evals, kind="stable")[:r]
+    U = canonical_signs(evecs[:, order])
+    return U.astype(np.float16), evals[order]
+
+
+def recovery_coeffs(U16: np.ndarray, D_e: np.ndarray) -> np.ndarray:
+    """b_j = U^T d_j for every channel of one expert, with the stored FP16 U;
+    stored FP16, shape [I][r] ([CN] §前置知识 "低秩恢复")."""
+    return (U16.astype(np.float64).T @ D_e).T.astype(np.float16)
+
+
+# --------------------------------------------------------------------------
+# prepared layer
+# --------------------------------------------------------------------------
+@dataclass
+class Layer:
+    """One MoE layer's stored weights (BF16 bit patterns) and the oracle's
+    prepared arrays, computed lazily per expert."""
+    shape: Shape
+    G: np.ndarray        # uint16 [E][I][H]
+    V: np.ndarray        # uint16 [E][I][H]
+    D: np.ndarray        # uint16 [E][H][I]
+    sigma: np.ndarray    # int8 [Hp]
+    _sketch: dict = field(default_factory=dict)
+    _dnorm: dict = field(default_factory=dict)
+    _b: dict = field(default_factory=dict)
+    _U: np.ndarray | None = None
+    eigenvalues: np.ndarray | None = None
+
+    def g(self, e):
+        return bf16_bits_to_f64(self.G[e])
+
+    def v(self, e):
+        return bf16_bits_to_f64(self.V[e])
+
+    def d(self, e):
+        return bf16_bits_to_f64(self.D[e])
+
+    def sketch(self, e) -> ExpertSketch:
+        if e not in self._sketch:
+            self._sketch[e] = sketch_expert(self.g(e), self.v(e), self.sigma, self.shape.Hp)
+        return self._sketch[e]
+
+    def dnorm(self, e) -> np.ndarray:
+        if e not in self._dnorm:
+            self._dnorm[e] = down_norms(self.d(e))
+        return self._dnorm[e]
+
+    @property
+    def U(self) -> np.ndarray:
+        if self._U is None:
+            self._U, self.eigenvalues = recovery_basis(
+                (self.d(e) for e in range(self.shape.E)), self.shape.r)
+        return self._U
+
+    def b(self, e) -> np.ndarray:
+        if e not in self._b:
+            self._b[e] = recovery_coeffs(self.U, self.d(e))
+        return self._b[e]
+
+
+# --------------------------------------------------------------------------
+# decode (per token)
+# --------------------------------------------------------------------------
+def silu(z):
+    """phi(z) = z / (1 + e^{-z}), the experts' gate activation (SiLU)."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+@dataclass
+class TokenResult:
+    y: np.ndarray            # float64 [H]: y_exact + y_recovery
+    y_exact: np.ndarray      # sum over kept channels
+    y_recovery: np.ndarray   # U sum over skipped channels
+    kept: np.ndarray         # int64 sorted global channel ids e*I + i of K
+    kept_order: np.ndarray   # K in selection order (-s, id)
+    score: np.ndarray        # float64 [topk][I]
+    p: np.ndarray            # float64 [topk][I]: phi(ghat) vhat
+    ghat: np.ndarray
+    vhat: np.ndarray
+    mask: np.ndarray         # bool [nb][128] screened coordinates
+    kth_score: float         # score of the k-th kept channel (nan if k == 0)
+    next_score: float        # best skipped score (nan if k == N)
+
+
+def screen_estimates(layer: Layer, e: int, Rx: np.ndarray, mask: np.ndarray):
+    """Sketch activation estimates for every channel of expert e.
+
+    ghat_j = sum_b alpha^g_{j,b} sum_{c in T_b} t^g_{j,b,c} (Rx)_{b,c}; vhat
+    likewise with the up sketch ([CN] §核心方法 step 1; [KR] §어떻게 쓰나).  The
+    omitted coordinates are not rescaled (the pages are silent; plain reading).
+    Rx: float64 [nb][128]; mask: bool [nb][128].
+    """
+    sk = layer.sketch(e)
+    rx = np.where(mask, Rx, 0.0)                              # [nb][128]
+    partial = np.einsum("gibc,bc->gib", sk.t.astype(np.float64), rx)  # [2][I][nb]
+    alpha = np.transpose(sk.alpha.astype(np.float64), (1, 2, 0))     # [2][I][nb]
+    est = (alpha * partial).sum(axis=-1)
+    return est[0], est[1]
+
+
+def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int) -> TokenResult:
+    """One token through the reader ([CN] §方法步骤详情, decode (1)-(4)).
+
+    1. Rotate x once; partial screen of the c largest-|Rx| coordinates per block.
+    2. s_j = w_j ||d_j|| |phi(ghat_j) vhat_j| for every routed channel (the
+       placement of |.| follows [KR] §어떻게 쓰나; [CN] writes phi(ghat)|vhat|),
+       then the exact top-k over all routed experts' channels together; ties
+       go to the lower global channel id e*I + i.
+    3. Kept channels: native BF16 g_j, v_j with the original fp32 x,
+       a_j = phi(g_j^T x)(v_j^T x); y_exact = sum_K w_j a_j d_j.
+    4. Skipped channels: y_recovery = U sum_S w_j b_j p_j, p_j = phi(ghat_j) vhat_j.
+    """
+    sh = layer.shape
+    x64 = np.asarray(x, dtype=np.float64)
+    xpad = pad_hidden(x64, sh.Hp)
+    Rx = rotate(xpad, layer.sigma).reshape(sh.nb, BLOCK)
+    mask = select_coordinates(butterfly_magnitudes_fp32(pad_hidden(np.asarray(x, np.float32), sh.Hp),
+                                                        layer.sigma), sh.c)
+    ids = [int(e) for e in ids]
+    topk = len(ids)
+    ghat = np.zeros((topk, sh.I))
+    vhat = np.zeros((topk, sh.I))
+    dn = np.zeros((topk, sh.I))
+    for s, e in enumerate(ids):
+        ghat[s], vhat[s] = screen_estimates(layer, e, Rx, mask)
+        dn[s] = layer.dnorm(e).astype(np.float64)
+    p = silu(ghat) * vhat
+    wv = np.asarray(w, dtype=np.float64)
+    score = wv[:, None] * dn * np.abs(p)
+
+    gid = np.array([[e * sh.I + i for i in range(sh.I)] for e in ids], dtype=np.int64)
+    flat_s = score.reshape(-1)
+    flat_id = gid.reshape(-1)
+    order = np.lexsort((flat_id, -flat_s))       # primary -s, secondary id
+    kept_idx = order[:k]
+    skip_idx = order[k:]
+    kth = float(flat_s[order[k - 1]]) if k > 0 else float("nan")
+    nxt = float(flat_s[order[k]]) if k < flat_s.size else float("nan")
+
+    kept_slot, kept_i = np.divmod(kept_idx, sh.I)
+    skip_slot, skip_i = np.divmod(skip_idx, sh.I)
+
+    y_exact = np.zeros(sh.H)
+    for s, e in enumerate(ids):
+        rows = kept_i[kept_slot == s]
+        if rows.size == 0:
+            continue
+        g_rows = bf16_bits_to_f64(layer.G[e][rows])          # [n][H]
+        v_rows = bf16_bits_to_f64(layer.V[e][rows])
+        d_cols = bf16_bits_to_f64(layer.D[e][:, rows])        # [H][n]
+        a = silu(g_rows @ x64) * (v_rows @ x64)
+        y_exact += d_cols @ (wv[s] * a)
+
+    y_rec = np.zeros(sh.H)
+    if skip_idx.size:
+        coef = np.zeros(sh.r)
+        for s, e in enumerate(ids):
+            rows = skip_i[skip_slot == s]
+            if rows.size == 0:
+                continue
+            coef += (wv[s] * p[s, rows]) @ layer.b(e)[rows].astype(np.float64)
+        y_rec = layer.U.astype(np.float64) @ coef
+
+    return TokenResult(
+        y=y_exact + y_rec, y_exact=y_exact, y_recovery=y_rec,
+        kept=np.sort(flat_id[kept_idx]), kept_order=flat_id[kept_idx],
+        score=score, p=p, ghat=ghat, vhat=vhat, mask=mask,
+        kth_score=kth, next_score=nxt)
+
+
+def decode(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int):
+    """Batch decode: every token independently (selection is per token; the
+    batch-shared selection of [CN] §未来方向 is future work)."""
+    return [decode_token(layer, x[t], ids[t], w[t], k) for t in range(x.shape[0])]
