@@ -1,0 +1,125 @@
+// Internal declarations shared by the reader's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_reader.h"
+
+namespace mr {
+
+constexpr int kBlock = 128;          // rotation block (coordinates)
+constexpr int kSector = 32;          // DRAM sector bytes
+constexpr int kMaxTopk = 64;
+constexpr int kMaxRank = 64;
+constexpr int kMaxBatch = 1024;
+constexpr int kMaxInter = 8192;
+constexpr int kPhases = 5;           // rotate, screen, topk, exact, out
+constexpr int kProfSlots = 64;       // decode calls recorded between two reads
+
+// Device error word bits (mirror the public MOE_READER_ERR_* values).
+constexpr uint32_t kErrExpertRange = MOE_READER_ERR_EXPERT_RANGE;
+constexpr uint32_t kErrExpertDup = MOE_READER_ERR_EXPERT_DUP;
+constexpr uint32_t kErrWeight = MOE_READER_ERR_WEIGHT;
+constexpr uint32_t kErrXNonFinite = MOE_READER_ERR_X_NONFINITE;
+constexpr uint32_t kErrTimeout = MOE_READER_ERR_TIMEOUT;
+
+// Shapes derived from the public config.
+struct Dims {
+  int H, E, topk, I, c, r, Bmax;
+  int Hp, nb, N;
+  int S;            // bytes per coordinate run (multiple of 32)
+  int runW;         // 32-bit words of codes per run actually used: I / 16
+};
+
+// Decode workspace (device), sized for Bmax tokens.
+struct Workspace {
+  float* rx;            // [Bmax][Hp]     fp32 rotated x
+  uint32_t* mask;       // [Bmax][nb][4]  screened coordinates
+  int32_t* ids;         // [Bmax][topk]   sanitized expert ids
+  float* w;             // [Bmax][topk]   routing weights
+  float* partial;       // [Bmax][topk][nb][2][I]  alpha-scaled block partials
+  float* ghat;          // [Bmax][N]
+  float* vhat;          // [Bmax][N]
+  float* p;             // [Bmax][N]      phi(ghat) vhat
+  float* score;         // [Bmax][N]
+  uint32_t* keptbits;   // [Bmax][N/32]   1 = kept
+  int32_t* kept;        // [Bmax][N]      kept n = slot*I + i, ascending n (first k used)
+  float* wa;            // [Bmax][N]      w * a for kept list entries
+  float* cpart;         // [Bmax][N/64][r] recovery partials per 64-channel chunk
+  // host-ABI staging
+  float* x_stage;       // [Bmax][H]
+  float* y_stage;       // [Bmax][H]
+  int32_t* ids_stage;   // [Bmax][topk]
+  float* w_stage;       // [Bmax][topk]
+  // accounting scratch
+  uint32_t* bm_codes;   // [E][nb][4]   coordinate-run bitmap (union)
+  uint32_t* bm_kept;    // [E][I/32]
+  uint32_t* bm_skip;    // [E][I/32]
+  uint32_t* bm_expert;  // [E/32 + 1]
+  unsigned long long* counters;  // [16]
+  uint32_t* err;        // [1] device error word
+};
+
+struct Prepared {
+  uint8_t* codes;       // [E][nb][128][2][S]
+  __half* scales;       // [E][nb][2][I]
+  __half* rho;          // [E][nb][2][I]
+  float* dnorm;         // [E][I]
+  __nv_bfloat16* Dt;    // [E][I][H]
+  __half* U;            // [H][r]
+  __half* b;            // [E][I][r]
+  int8_t* sigma;        // [Hp]
+  double* eigvals;      // [r]
+};
+
+}  // namespace mr
+
+struct moe_reader {
+  moe_reader_config cfg;
+  mr::Dims d;
+  int device;
+  const __nv_bfloat16* G;   // caller-owned [E][I][H]
+  const __nv_bfloat16* V;   // caller-owned [E][I][H]
+  mr::Prepared p;
+  mr::Workspace ws;
+  uint64_t resident[9];
+  // per-phase profiling (events around each decode kernel)
+  int prof_on;
+  int prof_used;
+  int prof_created;
+  cudaEvent_t prof_ev[mr::kProfSlots][mr::kPhases + 1];
+  // last decode
+  int has_decode;
+  int last_B, last_k;
+  cudaStream_t last_stream;
+};
+
+namespace mr {
+
+// ---- prepare launchers (prepare_sketch.cu / prepare_svd.cu) ----
+cudaError_t launch_sketch(const Dims& d, const __nv_bfloat16* G, const __nv_bfloat16* V,
+                          const int8_t* sigma, uint8_t* codes, __half* scales, __half* rho,
+                          cudaStream_t s);
+cudaError_t launch_transpose_down(const Dims& d, const __nv_bfloat16* D, __nv_bfloat16* Dt,
+                                  cudaStream_t s);
+cudaError_t launch_dnorm(const Dims& d, const __nv_bfloat16* Dt, float* dnorm, cudaStream_t s);
+// Recovery basis: U (fp16 [H][r]) and eigenvalues from Dt; returns ETIMEOUT via *timeout.
+int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, double* eigvals,
+                         cudaStream_t s);
+cudaError_t launch_project_b(const Dims& d, const __nv_bfloat16* Dt, const __half* U, __half* b,
+                             cudaStream_t s);
+
+// ---- decode launchers (decode.cu) ----
+// `ev` (may be null): kPhases + 1 events recorded at the phase boundaries.
+cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
+                          const float* w, int k, float* y, cudaStream_t s,
+                          const cudaEvent_t* ev);
+cudaError_t configure_decode_kernels(const Dims& d);
+cudaError_t launch_stats(const moe_reader& h, int B, int k, cudaStream_t s);
+cudaError_t launch_gather_kept(const moe_reader& h, int B, int k, int32_t* out_dev,
+                               cudaStream_t s);
+
+}  // namespace mr

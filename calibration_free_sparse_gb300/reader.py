@@ -1,0 +1,261 @@
+"""Thin ctypes binding of ``libmoe_reader.so`` (the C ABI in include/moe_reader.h).
+
+Argument marshalling only: every step of prepare and decode runs in the CUDA
+library.  The binding raises ``ReaderError`` when the library is missing --
+there is no fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_reader.so")
+
+OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EDEVICE, ESTATE = 0, -1, -2, -3, -4, -5, -6
+ERR_EXPERT_RANGE, ERR_EXPERT_DUP, ERR_WEIGHT, ERR_X_NONFINITE, ERR_TIMEOUT = 1, 2, 4, 8, 16
+ARRAYS = ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")
+
+EXPORT = {
+    "codes": 0, "scales": 1, "rho": 2, "dnorm": 3, "Dt": 4, "U": 5, "b": 6, "sigma": 7,
+    "eigvals": 8, "mask": 9, "ghat": 10, "vhat": 11, "score": 12,
+}
+EXPORTED_SYMBOLS = (
+    "moe_reader_prepare", "moe_reader_decode", "moe_reader_decode_host", "moe_reader_status",
+    "moe_reader_get_stats", "moe_reader_get_kept", "moe_reader_export_size", "moe_reader_export",
+    "moe_reader_get_info", "moe_reader_destroy", "moe_reader_strerror", "moe_reader_abi_version",
+    "moe_reader_set_profiling", "moe_reader_read_profile",
+)
+PHASES = ("rotate", "screen", "topk", "exact", "out")
+
+
+class ReaderError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        msg = _lib().moe_reader_strerror(code).decode() if _LIB is not None else str(code)
+        super().__init__(f"{what}: {msg} ({code})" if what else f"{msg} ({code})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("experts_per_token", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("screen_coords", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("max_batch", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("sectors", ctypes.c_uint64 * 8), ("dense_sectors", ctypes.c_uint64),
+                ("activation_bytes", ctypes.c_uint64), ("batch", ctypes.c_int32),
+                ("k", ctypes.c_int32)]
+
+
+class Info(ctypes.Structure):
+    _fields_ = [("hidden_padded", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("routed_channels", ctypes.c_int32), ("run_stride", ctypes.c_int32),
+                ("resident_bytes", ctypes.c_uint64 * 9)]
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -m calibration_free_sparse_gb300.build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.moe_reader_prepare.argtypes = [ctypes.POINTER(Config), vp, vp, vp, vp, vp,
+                                           ctypes.POINTER(vp)]
+        lib.moe_reader_prepare.restype = ctypes.c_int
+        lib.moe_reader_decode.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp]
+        lib.moe_reader_decode.restype = ctypes.c_int
+        lib.moe_reader_decode_host.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp]
+        lib.moe_reader_decode_host.restype = ctypes.c_int
+        lib.moe_reader_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.moe_reader_status.restype = ctypes.c_int
+        lib.moe_reader_get_stats.argtypes = [vp, ctypes.POINTER(Stats)]
+        lib.moe_reader_get_stats.restype = ctypes.c_int
+        lib.moe_reader_get_kept.argtypes = [vp, vp, i64]
+        lib.moe_reader_get_kept.restype = ctypes.c_int
+        lib.moe_reader_export_size.argtypes = [vp, i32]
+        lib.moe_reader_export_size.restype = ctypes.c_int64
+        lib.moe_reader_export.argtypes = [vp, i32, vp, i64]
+        lib.moe_reader_export.restype = ctypes.c_int
+        lib.moe_reader_get_info.argtypes = [vp, ctypes.POINTER(Info)]
+        lib.moe_reader_get_info.restype = ctypes.c_int
+        lib.moe_reader_destroy.argtypes = [vp]
+        lib.moe_reader_destroy.restype = None
+        lib.moe_reader_strerror.argtypes = [ctypes.c_int]
+        lib.moe_reader_strerror.restype = ctypes.c_char_p
+        lib.moe_reader_set_profiling.argtypes = [vp, i32]
+        lib.moe_reader_set_profiling.restype = ctypes.c_int
+        lib.moe_reader_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
+                                                ctypes.POINTER(ctypes.c_int64)]
+        lib.moe_reader_read_profile.restype = ctypes.c_int
+        lib.moe_reader_abi_version.argtypes = []
+        lib.moe_reader_abi_version.restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def library():
+    """The loaded CDLL (raises if the library was not built)."""
+    return _lib()
+
+
+def _ptr(a):
+    """Device or host address of a torch tensor, a numpy array or an int."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("array must be C-contiguous")
+        return a.ctypes.data
+    if hasattr(a, "data_ptr"):
+        if not a.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return a.data_ptr()
+    raise TypeError(f"cannot take the address of {type(a)}")
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code, what):
+    if code != OK:
+        raise ReaderError(code, what)
+
+
+class MoeReader:
+    """One prepared MoE layer.  `gate`, `up`, `down` are device BF16 tensors
+    ([E][I][H], [E][I][H], [E][H][I]); gate and up must outlive the reader."""
+
+    def __init__(self, hidden, num_experts, experts_per_token, inter, gate, up, down, sigma,
+                 screen_coords=80, rank=32, max_batch=16, stream=None):
+        lib = _lib()
+        self.cfg = Config(hidden, num_experts, experts_per_token, inter, screen_coords, rank,
+                          max_batch, 0)
+        sig = np.ascontiguousarray(sigma, dtype=np.int8)
+        self._keep = (gate, up)
+        h = ctypes.c_void_p()
+        code = lib.moe_reader_prepare(ctypes.byref(self.cfg), _ptr(gate), _ptr(up), _ptr(down),
+                                      sig.ctypes.data, _stream(stream), ctypes.byref(h))
+        _check(code, "moe_reader_prepare")
+        self._h = h
+        self.H, self.E, self.topk, self.I = hidden, num_experts, experts_per_token, inter
+        self.r, self.c, self.max_batch = rank, screen_coords, max_batch
+        info = self.info()
+        self.Hp, self.nb, self.N, self.S = (info["hidden_padded"], info["num_blocks"],
+                                            info["routed_channels"], info["run_stride"])
+
+    # -- lifetime ---------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().moe_reader_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h.value
+
+    # -- decode -----------------------------------------------------------
+    def decode(self, x, ids, w, k, y, stream=None):
+        """Enqueue one decode of B = x.shape[0] tokens (device tensors)."""
+        B = int(x.shape[0])
+        code = _lib().moe_reader_decode(self._h, _ptr(x), B, _ptr(ids), _ptr(w), int(k), _ptr(y),
+                                        _stream(stream))
+        _check(code, "moe_reader_decode")
+
+    def decode_host(self, x, ids, w, k, y=None, stream=None):
+        """Decode with host numpy buffers; returns y (host, fp32 [B][H])."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        B = x.shape[0]
+        if y is None:
+            y = np.empty((B, self.H), np.float32)
+        code = _lib().moe_reader_decode_host(self._h, _ptr(x), B, _ptr(ids), _ptr(w), int(k),
+                                             _ptr(y), _stream(stream))
+        _check(code, "moe_reader_decode_host")
+        return y
+
+    def status(self):
+        bits = ctypes.c_uint32(0)
+        code = _lib().moe_reader_status(self._h, ctypes.byref(bits))
+        return code, bits.value
+
+    def stats(self):
+        st = Stats()
+        _check(_lib().moe_reader_get_stats(self._h, ctypes.byref(st)), "moe_reader_get_stats")
+        out = {name: int(st.sectors[i]) for i, name in enumerate(ARRAYS)}
+        out["dense"] = int(st.dense_sectors)
+        out["activation_bytes"] = int(st.activation_bytes)
+        out["batch"], out["k"] = int(st.batch), int(st.k)
+        return out
+
+    def kept(self, B, k):
+        out = np.zeros((B, k), np.int32)
+        _check(_lib().moe_reader_get_kept(self._h, _ptr(out), out.size), "moe_reader_get_kept")
+        return out
+
+    def export(self, name, B=None):
+        which = EXPORT[name]
+        n = _lib().moe_reader_export_size(self._h, which)
+        if n < 0:
+            raise ReaderError(int(n), f"export {name}")
+        buf = np.empty(int(n), np.uint8)
+        _check(_lib().moe_reader_export(self._h, which, _ptr(buf), int(n)), f"export {name}")
+        E, I, H, r, nb, S, Hp, N = self.E, self.I, self.H, self.r, self.nb, self.S, self.Hp, self.N
+        shapes = {
+            "codes": (np.uint8, (E, nb, 128, 2, S)), "scales": (np.float16, (E, nb, 2, I)),
+            "rho": (np.float16, (E, nb, 2, I)), "dnorm": (np.float32, (E, I)),
+            "Dt": (np.uint16, (E, I, H)), "U": (np.float16, (H, r)), "b": (np.float16, (E, I, r)),
+            "sigma": (np.int8, (Hp,)), "eigvals": (np.float64, (r,)),
+            "mask": (np.uint32, (-1, nb, 4)), "ghat": (np.float32, (-1, N)),
+            "vhat": (np.float32, (-1, N)), "score": (np.float32, (-1, N)),
+        }
+        dt, shape = shapes[name]
+        return buf.view(dt).reshape(shape)
+
+    def set_profiling(self, enable):
+        _check(_lib().moe_reader_set_profiling(self._h, 1 if enable else 0), "set_profiling")
+
+    def read_profile(self):
+        """(ms per phase dict, number of decode calls) since the last read."""
+        ms = (ctypes.c_double * len(PHASES))()
+        calls = ctypes.c_int64(0)
+        _check(_lib().moe_reader_read_profile(self._h, ms, ctypes.byref(calls)), "read_profile")
+        return dict(zip(PHASES, list(ms))), int(calls.value)
+
+    def info(self):
+        inf = Info()
+        _check(_lib().moe_reader_get_info(self._h, ctypes.byref(inf)), "moe_reader_get_info")
+        return {"hidden_padded": inf.hidden_padded, "num_blocks": inf.num_blocks,
+                "routed_channels": inf.routed_channels, "run_stride": inf.run_stride,
+                "resident_bytes": [int(v) for v in inf.resident_bytes]}

@@ -1,0 +1,238 @@
+/*
+ * moe_reader.h -- C ABI of the GB300 (sm_103a) calibration-free channel
+ * reader for Mixture-of-Experts decoding.
+ *
+ * The reader replaces the routed-expert gated-MLP step of a decode token
+ * ("Channel Selection for Mixture-of-Experts Decoding Needs No Calibration
+ * Data"; Chinese summary page, sections 核心方法 and 方法步骤详情; Korean
+ * summary page, section 어떻게 쓰나):
+ *
+ *   prepare (load time, weights only)
+ *     - rotate every gate/up row in 128-coordinate blocks with a randomized
+ *       Hadamard matrix R and store a ternary sketch per block: 2-bit codes,
+ *       an FP16 scale and the FP16 block mean-squared error rho_b;
+ *     - precompute the down-column norms ||d_j||;
+ *     - take the top-r left singular vectors U of the layer's stacked down
+ *       columns and store b_j = U^T d_j;
+ *     - transpose every down projection so a kept channel's down weights are
+ *       one contiguous row.
+ *   decode (per token)
+ *     - rotate x once; per block screen only the c largest-|Rx| coordinates;
+ *     - score s_j = w_j ||d_j|| |phi(ghat_j) vhat_j| for every routed channel
+ *       and keep the exact top-k over all routed experts together;
+ *     - y = sum_{j in K} w_j phi(g_j^T x)(v_j^T x) d_j      (native BF16 rows)
+ *         + U sum_{j in S} w_j b_j phi(ghat_j) vhat_j       (rank-r recovery).
+ *
+ * Conventions shared by every entry point
+ *   - Return value: MOE_READER_OK (0) or a negative MOE_READER_E* code.  No
+ *     call traps, asserts, exits or throws across the ABI.
+ *   - "dev" pointers are CUDA device pointers on the handle's device; "host"
+ *     pointers are ordinary host memory.  `stream` is a cudaStream_t (NULL =
+ *     the legacy default stream).
+ *   - A handle is not safe for concurrent use from several host threads or
+ *     streams: decode calls share one workspace.
+ */
+#ifndef MOE_READER_H
+#define MOE_READER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_READER_ABI_VERSION 1
+
+/* Status codes. */
+#define MOE_READER_OK        0
+#define MOE_READER_EINVAL   -1  /* bad config, shape, k, batch, pointer or alignment */
+#define MOE_READER_ENOMEM   -2  /* device allocation failed */
+#define MOE_READER_ECUDA    -3  /* a CUDA runtime call failed */
+#define MOE_READER_ETIMEOUT -4  /* a device-side wait exceeded its bound (never hangs) */
+#define MOE_READER_EDEVICE  -5  /* a device-side input check failed (see error bits) */
+#define MOE_READER_ESTATE   -6  /* call needs a completed decode that does not exist */
+
+/* Device error bits reported by moe_reader_status(). */
+#define MOE_READER_ERR_EXPERT_RANGE  0x1u  /* expert id outside [0, E) (clamped) */
+#define MOE_READER_ERR_EXPERT_DUP    0x2u  /* an expert id repeated within a token */
+#define MOE_READER_ERR_WEIGHT        0x4u  /* routing weight negative or non-finite */
+#define MOE_READER_ERR_X_NONFINITE   0x8u  /* x holds a NaN or an infinity */
+#define MOE_READER_ERR_TIMEOUT      0x10u  /* a bounded device wait gave up */
+
+typedef struct moe_reader moe_reader_t;   /* opaque handle */
+
+/* Layer shape and limits.  All fields are required. */
+typedef struct {
+  int32_t hidden;             /* H: a multiple of 8, 8..65536; zero-padded to Hp = 128*ceil(H/128) */
+  int32_t num_experts;        /* E >= 1 */
+  int32_t experts_per_token;  /* topk, 1 <= topk <= min(E, 64) */
+  int32_t inter;              /* I: channels per expert, a multiple of 64, <= 8192; topk*I <= 32768 */
+  int32_t screen_coords;      /* c: coordinates screened per block, 1..128 (80 = partial screen) */
+  int32_t rank;               /* r: recovery rank, 1 <= r <= min(H, 64) */
+  int32_t max_batch;          /* B_max: 1..1024 tokens per decode (workspace sizing) */
+  int32_t flags;              /* reserved, must be 0 */
+} moe_reader_config;
+
+/* Read accounting of the last decode, in 32-byte sectors.  Every parameter
+ * array starts on a 256-byte boundary; a count is the number of distinct
+ * sectors read, a union over the tokens of the batch ("Channel Selection
+ * for Mixture-of-Experts Decoding Needs No Calibration Data", Chinese summary
+ * page, section 前置知识: reads are billed per 32-byte sector).             */
+#define MOE_READER_ARR_CODES  0   /* ternary codes of the screened coordinates */
+#define MOE_READER_ARR_SCALES 1   /* FP16 block scales of the routed experts */
+#define MOE_READER_ARR_DNORM  2   /* ||d_j|| of the routed experts */
+#define MOE_READER_ARR_G      3   /* native gate rows of kept channels (caller's array) */
+#define MOE_READER_ARR_V      4   /* native up rows of kept channels (caller's array) */
+#define MOE_READER_ARR_DT     5   /* transposed down rows of kept channels */
+#define MOE_READER_ARR_B      6   /* b_j rows of skipped channels */
+#define MOE_READER_ARR_U      7   /* U, read whole when any token skips a channel */
+typedef struct {
+  uint64_t sectors[8];          /* indexed by MOE_READER_ARR_* */
+  uint64_t dense_sectors;       /* G, V and D of every routed expert (denominator) */
+  uint64_t activation_bytes;    /* x, ids, w read and y written (not in the fraction) */
+  int32_t batch;                /* B of the last decode */
+  int32_t k;                    /* k of the last decode */
+} moe_reader_stats;
+
+/* Derived sizes of a prepared handle. */
+typedef struct {
+  int32_t hidden_padded;        /* Hp */
+  int32_t num_blocks;           /* nb = Hp / 128 */
+  int32_t routed_channels;      /* N = topk * I */
+  int32_t run_stride;           /* S: bytes per coordinate run, ceil(ceil(I/4)/32)*32 */
+  uint64_t resident_bytes[9];   /* codes, scales, rho, dnorm, Dt, U, b, sigma, workspace */
+} moe_reader_info;
+
+/*
+ * moe_reader_prepare -- build the reader for one MoE layer from its weights
+ * alone (Chinese summary page, 方法步骤详情, load-time steps (1)-(4)).
+ *
+ *   cfg     host; the layer shape.
+ *   gate    dev, BF16 [E][I][H] row-major (row j of G_e is channel j's gate row).
+ *   up      dev, BF16 [E][I][H] row-major.
+ *   down    dev, BF16 [E][H][I] row-major (column j of D_e is d_j).
+ *   sigma   host, int8 [Hp], every entry +1 or -1: the sign vector of the
+ *           randomized rotation R_b = H_128 diag(sigma_b) / sqrt(128).
+ *   stream  work is enqueued on it; the call synchronizes it before returning.
+ *   out     host; receives the handle.
+ *
+ * gate, up and down must be 256-byte aligned.  The handle keeps NON-OWNING
+ * pointers to gate and up (the exact step reads their native rows), so those
+ * two arrays must outlive it; `down` may be freed after the call returns
+ * (the handle owns its transpose).  The handle owns everything else: codes
+ * u8 [E][nb][128][2][S] (per block and coordinate, the gate run then the up
+ * run of I 2-bit codes, 0b00 = 0, 0b01 = +1, 0b11 = -1, channel i in byte
+ * i/4 at bits 2*(i%4)), scales and rho FP16 [E][nb][2][I], dnorm fp32 [E][I],
+ * Dt BF16 [E][I][H], U FP16 [H][r], b FP16 [E][I][r] and the decode
+ * workspace.  Errors: EINVAL, ENOMEM, ECUDA, ETIMEOUT; *out is NULL then.
+ */
+int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const void* up,
+                       const void* down, const int8_t* sigma, void* stream,
+                       moe_reader_t** out);
+
+/*
+ * moe_reader_decode -- one decode step of B tokens through the layer
+ * (Chinese summary page, 方法步骤详情, decode steps (1)-(4); Korean summary
+ * page, 어떻게 쓰나).  Asynchronous on `stream`.
+ *
+ *   x           dev, fp32 [B][H]: the tokens' hidden states.
+ *   B           0 <= B <= max_batch (B = 0 enqueues nothing).
+ *   expert_ids  dev, int32 [B][topk]: routed experts, distinct within a token.
+ *   expert_w    dev, fp32 [B][topk]: routing weights (finite, >= 0).
+ *               Routing itself (softmax, expert choice) is the caller's job.
+ *   k           0 <= k <= N = topk*I exact channels per token; k = N gives
+ *               the dense gated-MoE output, k = 0 recovery only.
+ *   y           dev, fp32 [B][H]: overwritten with the routed-expert output.
+ *
+ * All four arrays must be 16-byte aligned and may not alias y.  Host-side
+ * argument errors return EINVAL without enqueuing work.  Device-side input
+ * errors (bad or repeated ids, bad weights, non-finite x) set error bits that
+ * moe_reader_status() reports; the kernels then stay in bounds and y is
+ * unspecified.
+ */
+int moe_reader_decode(moe_reader_t* h, const float* x, int32_t B, const int32_t* expert_ids,
+                      const float* expert_w, int32_t k, float* y, void* stream);
+
+/*
+ * moe_reader_decode_host -- the same decode with HOST buffers: copies x, ids
+ * and w to the handle's device staging area, decodes, copies y back and
+ * synchronizes `stream`.  Arguments as for moe_reader_decode but every array
+ * is host memory (pinned memory gives the fastest copies).  Returns EDEVICE
+ * if a device-side input check failed.
+ */
+int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
+                           const int32_t* ids_host, const float* w_host, int32_t k,
+                           float* y_host, void* stream);
+
+/* moe_reader_status -- synchronize the stream of the last decode, read and
+ * clear the device error word.  *bits (host, may be NULL) receives the
+ * MOE_READER_ERR_* bits.  Returns OK, EDEVICE (input check) or ETIMEOUT. */
+int moe_reader_status(moe_reader_t* h, uint32_t* bits);
+
+/* moe_reader_get_stats -- read accounting of the last decode (synchronizes
+ * its stream, computes the union counts on device).  ESTATE if no decode. */
+int moe_reader_get_stats(moe_reader_t* h, moe_reader_stats* out);
+
+/* moe_reader_get_kept -- kept global channel ids e*I + i of the last decode,
+ * ascending per token: host int32 [B][k], `capacity` >= B*k entries.
+ * Synchronizes the last decode's stream.  ESTATE if no decode. */
+int moe_reader_get_kept(moe_reader_t* h, int32_t* kept_host, int64_t capacity);
+
+/* Exportable arrays (moe_reader_export).  Prepared data: */
+#define MOE_READER_EXPORT_CODES    0   /* u8   [E][nb][128][2][S] */
+#define MOE_READER_EXPORT_SCALES   1   /* f16  [E][nb][2][I] */
+#define MOE_READER_EXPORT_RHO      2   /* f16  [E][nb][2][I] */
+#define MOE_READER_EXPORT_DNORM    3   /* f32  [E][I] */
+#define MOE_READER_EXPORT_DT       4   /* bf16 [E][I][H] */
+#define MOE_READER_EXPORT_U        5   /* f16  [H][r] */
+#define MOE_READER_EXPORT_B        6   /* f16  [E][I][r] */
+#define MOE_READER_EXPORT_SIGMA    7   /* i8   [Hp] */
+#define MOE_READER_EXPORT_EIGVALS  8   /* f64  [r]: top eigenvalues of sum_j d_j d_j^T */
+/* Intermediates of the last decode (B = its batch): */
+#define MOE_READER_EXPORT_MASK     9   /* u32  [B][nb][4]: screened coordinates, bit c%32 of word c/32 */
+#define MOE_READER_EXPORT_GHAT    10   /* f32  [B][N]: sketch gate estimates, n = slot*I + i */
+#define MOE_READER_EXPORT_VHAT    11   /* f32  [B][N]: sketch up estimates */
+#define MOE_READER_EXPORT_SCORE   12   /* f32  [B][N]: output-unit scores s */
+
+/* moe_reader_export_size -- bytes of an exportable array (negative error
+ * code for a bad `which` or an intermediate before any decode). */
+int64_t moe_reader_export_size(moe_reader_t* h, int32_t which);
+
+/* moe_reader_export -- copy an array to host memory `dst` (`bytes` must
+ * equal moe_reader_export_size).  Synchronizes the handle's device. */
+int moe_reader_export(moe_reader_t* h, int32_t which, void* dst, int64_t bytes);
+
+/* moe_reader_get_info -- derived sizes and resident bytes of a handle. */
+int moe_reader_get_info(moe_reader_t* h, moe_reader_info* out);
+
+/* Per-phase device timing of decode calls (CUDA events recorded around each
+ * decode kernel on the decode's stream; also inside a captured CUDA graph).
+ * Phases, in order: rotate/select, screen, score + top-k, exact gather +
+ * recovery partials, output.                                                */
+#define MOE_READER_PHASES 5
+
+/* moe_reader_set_profiling -- enable (1) or disable (0) recording; either
+ * call forgets what was recorded.  Up to 64 decode calls are kept between two
+ * reads (older ones are overwritten). */
+int moe_reader_set_profiling(moe_reader_t* h, int32_t enable);
+
+/* moe_reader_read_profile -- wait for the recorded decodes, write the summed
+ * milliseconds per phase to ms_out[MOE_READER_PHASES] (host) and the number
+ * of decode calls to *calls_out (host, may be NULL), then forget them. */
+int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t* calls_out);
+
+/* moe_reader_destroy -- free everything the handle owns (NULL is a no-op).
+ * Synchronizes the handle's device first. */
+void moe_reader_destroy(moe_reader_t* h);
+
+/* moe_reader_strerror -- static text of a status code. */
+const char* moe_reader_strerror(int code);
+
+/* moe_reader_abi_version -- MOE_READER_ABI_VERSION of the built library. */
+int moe_reader_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_READER_H */
