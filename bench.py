@@ -1,0 +1,544 @@
+#!/usr/bin/env python
+"""Decode throughput of the MoE channel reader on one GPU (or N replicas).
+
+One step = one decode of every batch size in --batches on each of --layers
+distinct prepared Qwen3-30B-A3B-shaped layers (H 2048, E 128, top-8, I 768,
+k 756 = the 17.8% read budget, c 80, r 32).  Cycling the layers keeps the
+data a step touches (hundreds of MB) far above the 129 MB L2, so no decode
+finds its weights in L2.  Every step is one CUDA-graph replay per batch size;
+timing uses CUDA events on the replay stream.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 oracle on
+the host cores instead (the reference arm: there is no runnable reference
+implementation of this method).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tokens/s at batch 1–16; achieved HBM GB/s vs GB300 peak"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--batches", default="1,4,8,16")
+    ap.add_argument("--input-sets", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value, world):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the oracle on host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_layer_from_bits(wl, G, V, D, sigma):
+    from oracle import reader as R
+
+    shape = R.Shape(H=wl.H, E=wl.E, topk=wl.topk, I=wl.I, c=wl.c, r=wl.r)
+    return R.Layer(shape, G, V, D, sigma)
+
+
+def time_oracle(layer, tokens, k, budget_s, min_tokens=1):
+    """Decode tokens one by one with the oracle until budget_s has passed.
+    Load-time work (U, b, sketches of the experts used) is done first."""
+    from oracle import reader as R
+
+    _ = layer.U
+    for x, ids, w in tokens:
+        for e in ids:
+            layer.sketch(int(e))
+            layer.b(int(e))
+            layer.dnorm(int(e))
+    n = 0
+    t0 = time.perf_counter()
+    for x, ids, w in tokens:
+        R.decode_token(layer, x, ids, w, k)
+        n += 1
+        if n >= min_tokens and time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n, dt
+
+
+def cpu_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            try:
+                return int(os.environ[var])
+            except ValueError:
+                pass
+    return os.cpu_count() or 1
+
+
+def sample_tokens(wl, n, seed):
+    from calibration_free_sparse_gb300 import synthetic as S
+
+    x = S.activations(seed, n, wl.H)
+    ids, w = S.routing(seed, n, wl.E, wl.topk)
+    return [(x[i], ids[i], w[i]) for i in range(n)]
+
+
+def host_layer_bits(wl, seed):
+    """Weights of one benchmark layer as host BF16 bit patterns."""
+    from calibration_free_sparse_gb300 import synthetic as S
+
+    try:
+        import torch
+
+        if torch.cuda.is_available():
+            g, v, d = S.weights_device(seed, wl.E, wl.I, wl.H, "cuda")
+            out = tuple(S.bf16_tensor_to_bits(t) for t in (g, v, d))
+            del g, v, d
+            torch.cuda.empty_cache()
+            return out
+    except ImportError:
+        pass
+    return S.weights(seed, wl.E, wl.I, wl.H)
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    from calibration_free_sparse_gb300 import synthetic as S
+
+    seed = 1000
+    G, V, D = host_layer_bits(wl, seed)
+    layer = oracle_layer_from_bits(wl, G, V, D, S.signs(seed, wl.Hp))
+    toks = sample_tokens(wl, args.warmup + args.steps, 77)
+    # load-time work and warm-up steps
+    time_oracle(layer, toks[: max(1, args.warmup)], wl.k, budget_s=1e9, min_tokens=len(toks))
+    n, dt = time_oracle(layer, toks[args.warmup:], wl.k, budget_s=1e9,
+                        min_tokens=len(toks) - args.warmup)
+    value = n / dt
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * dt / max(n, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "H": wl.H, "E": wl.E, "topk": wl.topk, "I": wl.I,
+                   "k": wl.k, "c": wl.c, "r": wl.r,
+                   "note": "each step decodes one token with the fp64 oracle; the oracle "
+                           "is per token, so its cost does not depend on the batch size"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} single-token decodes of one layer"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+PHASE_BYTES = {   # algorithmic parameter arrays each decode kernel reads
+    "rotate": (),
+    "screen": ("codes", "scales"),
+    "topk": ("dnorm",),
+    "exact": ("G", "V", "b"),
+    "out": ("Dt", "U"),
+}
+
+
+def traffic_for(kernel):
+    """Per-launch DRAM bytes of `kernel` from a committed ncu summary, if the
+    summary was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+
+    with open(path) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "calibration_free_sparse_gb300", "csrc", "decode.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    ent = rec.get(kernel)
+    if not ent or ent.get("decode_cu_sha256_16") != digest:
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def run_ours(args, wl, world, rank, local):
+    import torch
+
+    from calibration_free_sparse_gb300 import synthetic as S
+    from calibration_free_sparse_gb300.reader import PHASES, MoeReader
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    batches = [int(b) for b in args.batches.split(",")]
+    Bmax = max(batches)
+    L = args.layers
+    nsets = max(1, args.input_sets)
+
+    # -- prepared layers (weights drawn on the device, one seed per layer and rank)
+    readers, keep = [], []
+    for l in range(L):
+        seed = 1000 + l + 7919 * rank
+        g, v, d = S.weights_device(seed, wl.E, wl.I, wl.H, dev)
+        rd = MoeReader(wl.H, wl.E, wl.topk, wl.I, g, v, d, S.signs(seed, wl.Hp),
+                       screen_coords=wl.c, rank=wl.r, max_batch=Bmax)
+        del d
+        readers.append(rd)
+        keep.append((g, v))
+    torch.cuda.empty_cache()
+
+    # -- inputs: nsets distinct sets per (batch, layer)
+    inputs = {}
+    for si in range(nsets):
+        for B in batches:
+            for l in range(L):
+                sd = 10_000 * (si + 1) + 100 * B + l + 7919 * rank
+                x = S.activations(sd, B, wl.H)
+                ids, w = S.routing(sd, B, wl.E, wl.topk)
+                inputs[(si, B, l)] = (torch.from_numpy(x).to(dev), torch.from_numpy(ids).to(dev),
+                                      torch.from_numpy(w).to(dev), torch.empty((B, wl.H), device=dev),
+                                      (x, ids, w))
+
+    # -- algorithmic bytes per decode (library read accounting, per phase)
+    stream = torch.cuda.Stream(device=dev)
+    phase_bytes = {B: {p: 0 for p in PHASES} for B in batches}
+    sector_bytes = {B: 0 for B in batches}
+    dense_bytes = {B: 0 for B in batches}
+    with torch.cuda.stream(stream):
+        for B in batches:
+            for l, rd in enumerate(readers):
+                x, ids, w, y, _ = inputs[(0, B, l)]
+                rd.decode(x, ids, w, wl.k, y)
+                st = rd.stats()
+                for p, arrs in PHASE_BYTES.items():
+                    phase_bytes[B][p] += 32 * sum(st[a] for a in arrs)
+                sector_bytes[B] += 32 * sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V",
+                                                             "Dt", "b", "U"))
+                dense_bytes[B] += 32 * st["dense"]
+                code, bits = rd.status()
+                if code != 0:
+                    raise RuntimeError(f"device status {code} bits {bits}")
+
+    # -- CUDA graphs: one per (input set, batch), each decoding every layer
+    def capture(si, B):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for l, rd in enumerate(readers):
+                x, ids, w, y, _ = inputs[(si, B, l)]
+                rd.decode(x, ids, w, wl.k, y)
+        return graph
+
+    torch.cuda.synchronize()
+    graphs = {(si, B): capture(si, B) for si in range(nsets) for B in batches}
+    launches_per_decode = 5
+    launches_per_step = launches_per_decode * L * len(batches)
+
+    def step(i, events=None):
+        si = i % nsets
+        for bi, B in enumerate(batches):
+            if events is not None:
+                events[bi][0].record(stream)
+            graphs[(si, B)].replay()
+            if events is not None:
+                events[bi][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+
+    # -- timed region
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    clocks = ClockSampler(gpu_index)
+    per_b_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in batches] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.25)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, per_b_events[i])
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    time.sleep(0.15)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    per_b_ms = {B: sum(per_b_events[i][bi][0].elapsed_time(per_b_events[i][bi][1])
+                       for i in range(args.steps)) for bi, B in enumerate(batches)}
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    tokens_per_step = L * sum(batches)
+    value = tokens_per_step * args.steps * world / (elapsed_ms / 1000.0)
+
+    # -- per-phase device time (profiling events inside fresh graphs of set 0)
+    for rd in readers:
+        rd.set_profiling(True)
+    prof_graphs = {B: capture(0, B) for B in batches}
+    prof_steps = min(args.steps, 50)
+    phase_ms = {B: {p: 0.0 for p in PHASES} for B in batches}
+    for _ in range(prof_steps):
+        with torch.cuda.stream(stream):
+            for B in batches:
+                prof_graphs[B].replay()
+        for rd in readers:
+            rows = rd.read_profile()          # slot bi = the decode captured for batches[bi]
+            for bi, B in enumerate(batches):
+                for p in PHASES:
+                    phase_ms[B][p] += rows[bi][p]
+    for rd in readers:
+        rd.set_profiling(False)
+
+    peak, peak_kind = measured_peaks()
+    per_batch = {}
+    for B in batches:
+        ms_decode = per_b_ms[B] / (args.steps * L)
+        gbs = (sector_bytes[B] / L) / (ms_decode / 1000.0) / 1e9
+        per_batch[str(B)] = {
+            "tokens_per_s": B / (ms_decode / 1000.0),
+            "us_per_decode": 1000.0 * ms_decode,
+            "sector_bytes_per_decode": sector_bytes[B] / L,
+            "read_fraction": sector_bytes[B] / dense_bytes[B],
+            "hbm_gbs": gbs,
+            "frac_of_measured_peak": gbs / peak,
+            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+            "phase_us_per_decode": {p: 1000.0 * phase_ms[B][p] / (prof_steps * L) for p in PHASES},
+        }
+    # dominant kernel: most device time over the whole sweep
+    totals = {p: sum(phase_ms[B][p] for B in batches) for p in PHASES}
+    dom = max(totals, key=totals.get)
+    dom_bytes = sum(phase_bytes[B][dom] for B in batches)          # one step of set 0
+    dom_ms = totals[dom] / prof_steps                                # per step
+    achieved = dom_bytes / (dom_ms / 1000.0) / 1e9 if dom_ms > 0 else 0.0
+    kernel_names = {"rotate": "rotate_kernel", "screen": "screen_kernel", "topk": "topk_kernel",
+                    "exact": "exact_kernel", "out": "out_kernel"}
+    traffic = traffic_for(kernel_names[dom])
+    roofline = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_kind": f"{peak_kind} copy bandwidth",
+                "share_of_step_time": totals[dom] / sum(totals.values())}
+
+    # -- end to end through the host-buffer C ABI (pinned host memory)
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        for B in batches:
+            for l in range(L):
+                x, ids, w = inputs[(0, B, l)][4]
+                hx = torch.from_numpy(x).pin_memory()
+                hi = torch.from_numpy(ids).pin_memory()
+                hw = torch.from_numpy(w).pin_memory()
+                hy = torch.empty((B, wl.H), dtype=torch.float32).pin_memory()
+                host[(B, l)] = (hx.numpy(), hi.numpy(), hw.numpy(), hy.numpy())
+        e2e_steps = max(3, min(args.steps, 20))
+        h2d = sum(B * wl.H * 4 + B * wl.topk * 8 for B in batches) * L
+        d2h = sum(B * wl.H * 4 + 4 for B in batches) * L
+
+        def host_step():
+            for B in batches:
+                for l, rd in enumerate(readers):
+                    hx, hi, hw, hy = host[(B, l)]
+                    rd.decode_host(hx, hi, hw, wl.k, hy, stream=stream)
+
+        host_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            host_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        wall = max_over_ranks(wall, world)
+        e2e = {"value": tokens_per_step * e2e_steps * world / wall, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps,
+               "note": "moe_reader_decode_host per layer and batch: pinned H2D of x/ids/w, "
+                       "decode, D2H of y and the status word, stream synchronize"}
+
+    # -- the oracle on host cores (rank 0, N = 1 only)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        G = S.bf16_tensor_to_bits(keep[0][0])
+        V = S.bf16_tensor_to_bits(keep[0][1])
+        g, v, d = S.weights_device(1000, wl.E, wl.I, wl.H, dev)
+        D = S.bf16_tensor_to_bits(d)
+        del g, v, d
+        layer = oracle_layer_from_bits(wl, G, V, D, S.signs(1000, wl.Hp))
+        toks = []
+        for B in batches:
+            x, ids, w = inputs[(0, B, 0)][4]
+            toks += [(x[t], ids[t], w[t]) for t in range(B)]
+        n, dt = time_oracle(layer, toks * 4, wl.k, budget_s=args.cpu_seconds)
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{n} tokens of layer 0 from the benchmark batches, decoded one at a "
+                         f"time by the fp64 oracle in {dt:.1f} s (load-time work excluded)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {
+                "workload": wl.name, "H": wl.H, "E": wl.E, "topk": wl.topk, "I": wl.I,
+                "k": wl.k, "read_budget": 0.178, "screen_coords": wl.c, "rank": wl.r,
+                "batches": batches, "layers_per_step": L, "input_sets": nsets,
+                "weights": "bf16 experts + 2-bit ternary sketch (fp16 scales)",
+                "l2": "inputs larger than L2: each step decodes on %d distinct prepared "
+                      "layers (%.0f MB of sector-accounted reads per step vs 129 MB L2)"
+                      % (L, sum(sector_bytes.values()) / 1e6),
+                "parallelism": f"replicas x{world}",
+                "tokens": "layer-tokens: one token through one MoE layer",
+            },
+            "per_batch": per_batch,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    for rd in readers:
+        rd.close()
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    from calibration_free_sparse_gb300 import synthetic as S
+
+    wl = S.QWEN3_30B
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+    else:
+        run_ours(args, wl, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

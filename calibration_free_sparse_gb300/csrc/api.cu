@@ -467,22 +467,22 @@ int moe_reader_set_profiling(moe_reader_t* h, int32_t enable) {
   return MOE_READER_OK;
 }
 
-int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t* calls_out) {
-  if (!h || !ms_out) return MOE_READER_EINVAL;
-  for (int j = 0; j < mr::kPhases; ++j) ms_out[j] = 0.0;
+int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t capacity,
+                            int64_t* calls_out) {
+  if (!h || (!ms_out && capacity > 0)) return MOE_READER_EINVAL;
   const int used = h->prof_used < mr::kProfSlots ? h->prof_used : mr::kProfSlots;
   if (calls_out) *calls_out = used;
-  if (used == 0) return MOE_READER_OK;
-  cudaError_t ce = cudaEventSynchronize(h->prof_ev[(h->prof_used - 1) % mr::kProfSlots][mr::kPhases]);
-  if (ce != cudaSuccess) return cuda_status(ce);
-  for (int i = 0; i < used; ++i)
+  if (capacity < used) return MOE_READER_EINVAL;
+  for (int i = 0; i < used; ++i) {
+    cudaError_t ce = cudaEventSynchronize(h->prof_ev[i][mr::kPhases]);
+    if (ce != cudaSuccess) return cuda_status(ce);
     for (int j = 0; j < mr::kPhases; ++j) {
       float ms = 0.f;
       ce = cudaEventElapsedTime(&ms, h->prof_ev[i][j], h->prof_ev[i][j + 1]);
       if (ce != cudaSuccess) return cuda_status(ce);
-      ms_out[j] += ms;
+      ms_out[(size_t)i * mr::kPhases + j] = ms;
     }
-  h->prof_used = 0;
+  }
   return MOE_READER_OK;
 }
 

@@ -574,8 +574,16 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
   const Dims& d = h.d;
   const Workspace& ws = h.ws;
   cudaError_t err;
+  // Inside stream capture a plain event record is only a dependency marker;
+  // the External flag makes it an event-record node of the graph.
+  unsigned int rec_flags = cudaEventRecordDefault;
+  if (ev) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((err = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return err;
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
 #define MR_MARK(i) \
-  if (ev && (err = cudaEventRecord(ev[i], s)) != cudaSuccess) return err;
+  if (ev && (err = cudaEventRecordWithFlags(ev[i], s, rec_flags)) != cudaSuccess) return err;
   MR_MARK(0)
   const int rot_warps = B * d.nb;
   rotate_kernel<<<(rot_warps + 3) / 4, 128, 0, s>>>(d, B, x, ids, w, h.p.sigma, ws.rx, ws.mask,

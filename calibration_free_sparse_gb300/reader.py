@@ -95,7 +95,7 @@ def _lib():
         lib.moe_reader_strerror.restype = ctypes.c_char_p
         lib.moe_reader_set_profiling.argtypes = [vp, i32]
         lib.moe_reader_set_profiling.restype = ctypes.c_int
-        lib.moe_reader_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
+        lib.moe_reader_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_double), i64,
                                                 ctypes.POINTER(ctypes.c_int64)]
         lib.moe_reader_read_profile.restype = ctypes.c_int
         lib.moe_reader_abi_version.argtypes = []
@@ -247,11 +247,14 @@ class MoeReader:
         _check(_lib().moe_reader_set_profiling(self._h, 1 if enable else 0), "set_profiling")
 
     def read_profile(self):
-        """(ms per phase dict, number of decode calls) since the last read."""
-        ms = (ctypes.c_double * len(PHASES))()
+        """Per recorded decode slot, the milliseconds of each phase: list of dicts."""
+        cap = 64
+        ms = (ctypes.c_double * (cap * len(PHASES)))()
         calls = ctypes.c_int64(0)
-        _check(_lib().moe_reader_read_profile(self._h, ms, ctypes.byref(calls)), "read_profile")
-        return dict(zip(PHASES, list(ms))), int(calls.value)
+        _check(_lib().moe_reader_read_profile(self._h, ms, cap, ctypes.byref(calls)),
+               "read_profile")
+        n = int(calls.value)
+        return [dict(zip(PHASES, ms[i * len(PHASES):(i + 1) * len(PHASES)])) for i in range(n)]
 
     def info(self):
         inf = Info()

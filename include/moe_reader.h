@@ -213,14 +213,19 @@ int moe_reader_get_info(moe_reader_t* h, moe_reader_info* out);
 #define MOE_READER_PHASES 5
 
 /* moe_reader_set_profiling -- enable (1) or disable (0) recording; either
- * call forgets what was recorded.  Up to 64 decode calls are kept between two
- * reads (older ones are overwritten). */
+ * call empties the slots.  While enabled, decode call i records its events in
+ * slot i % 64. */
 int moe_reader_set_profiling(moe_reader_t* h, int32_t enable);
 
-/* moe_reader_read_profile -- wait for the recorded decodes, write the summed
- * milliseconds per phase to ms_out[MOE_READER_PHASES] (host) and the number
- * of decode calls to *calls_out (host, may be NULL), then forget them. */
-int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t* calls_out);
+/* moe_reader_read_profile -- for each of the n = min(decodes recorded since
+ * profiling was enabled, 64) slots, in slot order, wait for its events and
+ * write the milliseconds of every phase to ms_out[slot][MOE_READER_PHASES]
+ * (host, `capacity` >= n rows); *calls_out (host, may be NULL) = n.  A slot
+ * recorded while a CUDA graph was captured holds the times of that graph's
+ * latest replay; every slot must have been recorded (or replayed) before the
+ * read.  Reading does not empty the slots. */
+int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t capacity,
+                            int64_t* calls_out);
 
 /* moe_reader_destroy -- free everything the handle owns (NULL is a no-op).
  * Synchronizes the handle's device first. */
