@@ -152,6 +152,8 @@ const char* moe_reader_strerror(int code) {
     case MOE_READER_ETIMEOUT: return "a bounded device wait timed out";
     case MOE_READER_EDEVICE: return "device-side input check failed (expert ids, weights or x)";
     case MOE_READER_ESTATE: return "no completed decode on this handle";
+    case MOE_READER_ETOOBIG:
+      return "rows*cols exceeds the 2^18-element fixed scratch of moe_reader_topk_noalloc";
     default: return "unknown status";
   }
 }

@@ -15,7 +15,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmoe_reader.so")
 
-OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EDEVICE, ESTATE = 0, -1, -2, -3, -4, -5, -6
+OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EDEVICE, ESTATE, ETOOBIG = 0, -1, -2, -3, -4, -5, -6, -7
 ERR_EXPERT_RANGE, ERR_EXPERT_DUP, ERR_WEIGHT, ERR_X_NONFINITE, ERR_TIMEOUT = 1, 2, 4, 8, 16
 ARRAYS = ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")
 
@@ -27,7 +27,7 @@ EXPORTED_SYMBOLS = (
     "moe_reader_prepare", "moe_reader_decode", "moe_reader_decode_host", "moe_reader_status",
     "moe_reader_get_stats", "moe_reader_get_kept", "moe_reader_export_size", "moe_reader_export",
     "moe_reader_get_info", "moe_reader_destroy", "moe_reader_strerror", "moe_reader_abi_version",
-    "moe_reader_set_profiling", "moe_reader_read_profile",
+    "moe_reader_set_profiling", "moe_reader_read_profile", "moe_reader_topk_noalloc",
 )
 PHASES = ("rotate", "screen", "topk", "exact", "out")
 
@@ -98,6 +98,8 @@ def _lib():
         lib.moe_reader_read_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_double), i64,
                                                 ctypes.POINTER(ctypes.c_int64)]
         lib.moe_reader_read_profile.restype = ctypes.c_int
+        lib.moe_reader_topk_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+        lib.moe_reader_topk_noalloc.restype = ctypes.c_int
         lib.moe_reader_abi_version.argtypes = []
         lib.moe_reader_abi_version.restype = ctypes.c_int
         _LIB = lib
@@ -144,6 +146,15 @@ def _stream(stream):
 def _check(code, what):
     if code != OK:
         raise ReaderError(code, what)
+
+
+def topk_noalloc(scores, k, kept, ids=None, stream=None):
+    """Exact top-k per row of device scores [rows][cols] into device kept
+    [rows][k] (ascending column indices) without any device allocation."""
+    rows, cols = int(scores.shape[0]), int(scores.shape[1])
+    code = _lib().moe_reader_topk_noalloc(_ptr(scores), _ptr(ids), rows, cols, int(k),
+                                          _ptr(kept), _stream(stream))
+    _check(code, "moe_reader_topk_noalloc")
 
 
 class MoeReader:

@@ -52,6 +52,7 @@ extern "C" {
 #define MOE_READER_ETIMEOUT -4  /* a device-side wait exceeded its bound (never hangs) */
 #define MOE_READER_EDEVICE  -5  /* a device-side input check failed (see error bits) */
 #define MOE_READER_ESTATE   -6  /* call needs a completed decode that does not exist */
+#define MOE_READER_ETOOBIG  -7  /* request exceeds the fixed scratch of moe_reader_topk_noalloc */
 
 /* Device error bits reported by moe_reader_status(). */
 #define MOE_READER_ERR_EXPERT_RANGE  0x1u  /* expert id outside [0, E) (clamped) */
@@ -226,6 +227,35 @@ int moe_reader_set_profiling(moe_reader_t* h, int32_t enable);
  * read.  Reading does not empty the slots. */
 int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t capacity,
                             int64_t* calls_out);
+
+/*
+ * moe_reader_topk_noalloc -- exact top-k of every row of a score matrix,
+ * with the decode's selection rule (larger score first; on equal scores the
+ * lower id wins), using NO device allocation.  The pages have no counterpart
+ * of this entry point: it exists for callers that cannot call cudaMalloc --
+ * code running inside CUDA-graph stream capture, inference-engine plugins
+ * that may only touch memory the engine hands them, and processes whose
+ * allocator forbids device allocations after start-up.
+ *
+ *   scores  dev, fp32 [rows][cols]; any finite values (NaN sorts above all).
+ *   ids     dev, int32 [rows][cols] tie-break ids, or NULL to use the column
+ *           index (the decode passes global channel ids e*I + i).
+ *   k       0 <= k <= cols kept entries per row.
+ *   kept    dev, int32 [rows][k]: kept COLUMN indices, ascending per row.
+ *
+ * Scratch is one file-scope __device__ array of 2^18 elements x 9 bytes
+ * (about 2.3 MiB), held by every GPU that loads the library until the
+ * process exits; rows*cols above 2^18 returns MOE_READER_ETOOBIG and
+ * enqueues nothing.  Each call rewrites the scratch it reads, so no state
+ * carries over between calls, but every call shares the one array: calls
+ * that can overlap on the GPU (different streams, or graphs replayed
+ * concurrently) race and must be serialized by the caller.  The first call
+ * on a device looks up the array's device address (once per device, under
+ * a lock); make that first call before any stream capture.  Asynchronous
+ * on `stream`; returns EINVAL for bad sizes or NULL pointers.
+ */
+int moe_reader_topk_noalloc(const float* scores, const int32_t* ids, int32_t rows, int32_t cols,
+                            int32_t k, int32_t* kept, void* stream);
 
 /* moe_reader_destroy -- free everything the handle owns (NULL is a no-op).
  * Synchronizes the handle's device first. */
