@@ -251,11 +251,7 @@ def run_reference(args, wl, world, rank):
 # our arm
 # ---------------------------------------------------------------------------
 PHASE_BYTES = {   # algorithmic parameter arrays each decode kernel reads
-    "rotate": (),
-    "screen": ("codes", "scales"),
-    "topk": ("dnorm",),
-    "exact": ("G", "V", "b"),
-    "out": ("Dt", "U"),
+    "decode": ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U"),
 }
 
 
@@ -316,7 +312,7 @@ def run_ours(args, wl, world, rank, local):
 
     # -- algorithmic bytes per decode (library read accounting, per phase)
     stream = torch.cuda.Stream(device=dev)
-    phase_bytes = {B: {p: 0 for p in PHASES} for B in batches}
+    phase_bytes = {B: {p: 0 for p in PHASE_BYTES} for B in batches}
     sector_bytes = {B: 0 for B in batches}
     dense_bytes = {B: 0 for B in batches}
     with torch.cuda.stream(stream):
@@ -345,7 +341,7 @@ def run_ours(args, wl, world, rank, local):
 
     torch.cuda.synchronize()
     graphs = {(si, B): capture(si, B) for si in range(nsets) for B in batches}
-    launches_per_decode = 5
+    launches_per_decode = 1
     launches_per_step = launches_per_decode * L * len(batches)
 
     def step(i, events=None):
@@ -423,19 +419,14 @@ def run_ours(args, wl, world, rank, local):
             "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
             "phase_us_per_decode": {p: 1000.0 * phase_ms[B][p] / (prof_steps * L) for p in PHASES},
         }
-    # dominant kernel: most device time over the whole sweep
-    totals = {p: sum(phase_ms[B][p] for B in batches) for p in PHASES}
-    dom = max(totals, key=totals.get)
-    dom_bytes = sum(phase_bytes[B][dom] for B in batches)          # one step of set 0
-    dom_ms = totals[dom] / prof_steps                                # per step
+    # the decode is one persistent kernel: it is the dominant (only) kernel
+    dom_bytes = sum(phase_bytes[B]["decode"] for B in batches)      # one step of set 0
+    dom_ms = sum(phase_ms[B]["decode"] for B in batches) / prof_steps
     achieved = dom_bytes / (dom_ms / 1000.0) / 1e9 if dom_ms > 0 else 0.0
-    kernel_names = {"rotate": "rotate_kernel", "screen": "screen_kernel", "topk": "topk_kernel",
-                    "exact": "exact_kernel", "out": "out_kernel"}
-    traffic = traffic_for(kernel_names[dom])
-    roofline = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": achieved, "peak": peak,
+    traffic = traffic_for("decode_kernel")
+    roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                "peak_kind": f"{peak_kind} copy bandwidth",
-                "share_of_step_time": totals[dom] / sum(totals.values())}
+                "peak_kind": f"{peak_kind} copy bandwidth", "share_of_step_time": 1.0}
 
     # -- end to end through the host-buffer C ABI (pinned host memory)
     e2e = None

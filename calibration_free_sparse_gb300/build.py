@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libmoe_reader.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ("api.cu", "decode.cu", "prepare_sketch.cu", "prepare_svd.cu", "topk_noalloc.cu")
+SOURCES = ("api.cu", "decode.cu", "stats.cu", "prepare_sketch.cu", "prepare_svd.cu",
+           "topk_noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]

@@ -128,13 +128,21 @@ int check_decode_args(const moe_reader* h, const void* x, int32_t B, const void*
   return MOE_READER_OK;
 }
 
-// Events of the next profiling slot, or null when profiling is off.  Slots
-// wrap after kProfSlots decode calls without a read.
-const cudaEvent_t* profile_slot(moe_reader* h) {
-  if (!h->prof_on) return nullptr;
+// Next profiling slot (events + stamp rows), or -1 when profiling is off.
+// Slots wrap after kProfSlots decode calls.
+int profile_slot(moe_reader* h) {
+  if (!h->prof_on) return -1;
   const int slot = h->prof_used % mr::kProfSlots;
   h->prof_used++;
-  return h->prof_ev[slot];
+  return slot;
+}
+
+cudaError_t launch_profiled(moe_reader* h, const float* x, int B, const int32_t* ids,
+                            const float* w, int k, float* y, cudaStream_t s) {
+  const int slot = profile_slot(h);
+  if (slot < 0) return mr::launch_decode(*h, x, B, ids, w, k, y, s, nullptr, nullptr);
+  return mr::launch_decode(*h, x, B, ids, w, k, y, s, h->prof_ev[slot],
+                           h->prof_stamps + (size_t)slot * h->grid * 5);
 }
 
 }  // namespace
@@ -230,7 +238,9 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_kb = wa.take(Bm * (d.N / 32) * 4);
   const size_t w_kept = wa.take(Bm * d.N * 4);
   const size_t w_wa = wa.take(Bm * d.N * 4);
-  const size_t w_cp = wa.take(Bm * (d.N / 64) * d.r * 4);
+  const size_t w_ro = wa.take(Bm * d.N * 4);
+  const size_t w_sync = wa.take(mr::sync_words(d) * 4);
+  const size_t w_cp = wa.take(Bm * d.r * 4);
   const size_t w_xs = wa.take(Bm * d.H * 4);
   const size_t w_ys = wa.take(Bm * d.H * 4);
   const size_t w_is = wa.take(Bm * d.topk * 4);
@@ -261,6 +271,8 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.keptbits = reinterpret_cast<uint32_t*>(wb + w_kb);
   h->ws.kept = reinterpret_cast<int32_t*>(wb + w_kept);
   h->ws.wa = reinterpret_cast<float*>(wb + w_wa);
+  h->ws.rowoff = reinterpret_cast<int32_t*>(wb + w_ro);
+  h->ws.sync = reinterpret_cast<uint32_t*>(wb + w_sync);
   h->ws.cpart = reinterpret_cast<float*>(wb + w_cp);
   h->ws.x_stage = reinterpret_cast<float*>(wb + w_xs);
   h->ws.y_stage = reinterpret_cast<float*>(wb + w_ys);
@@ -291,6 +303,11 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
     if (st != MOE_READER_OK) break;
     if ((ce = mr::launch_project_b(d, h->p.Dt, h->p.U, h->p.b, s)) != cudaSuccess) break;
     if ((ce = mr::configure_decode_kernels(d)) != cudaSuccess) break;
+    h->grid = mr::decode_grid(d);
+    if (h->grid <= 0) {
+      ce = cudaErrorInvalidConfiguration;
+      break;
+    }
     ce = cudaStreamSynchronize(s);
   } while (0);
   if (ce != cudaSuccess || st != MOE_READER_OK) {
@@ -313,7 +330,7 @@ int moe_reader_decode(moe_reader_t* h, const float* x, int32_t B, const int32_t*
     return MOE_READER_EINVAL;
   if ((const void*)x == (const void*)y) return MOE_READER_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t ce = mr::launch_decode(*h, x, B, expert_ids, expert_w, k, y, s, profile_slot(h));
+  const cudaError_t ce = launch_profiled(h, x, B, expert_ids, expert_w, k, y, s);
   if (ce != cudaSuccess) return cuda_status(ce);
   h->has_decode = 1;
   h->last_B = B;
@@ -340,8 +357,8 @@ int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
   if ((ce = cudaMemcpyAsync(h->ws.w_stage, w_host, (size_t)B * d.topk * 4, cudaMemcpyHostToDevice,
                             s)) != cudaSuccess)
     return cuda_status(ce);
-  if ((ce = mr::launch_decode(*h, h->ws.x_stage, B, h->ws.ids_stage, h->ws.w_stage, k,
-                              h->ws.y_stage, s, profile_slot(h))) != cudaSuccess)
+  if ((ce = launch_profiled(h, h->ws.x_stage, B, h->ws.ids_stage, h->ws.w_stage, k,
+                            h->ws.y_stage, s)) != cudaSuccess)
     return cuda_status(ce);
   h->has_decode = 1;
   h->last_B = B;
@@ -354,7 +371,11 @@ int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
   if ((ce = cudaMemcpyAsync(&bits, h->ws.err, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
     return cuda_status(ce);
   if ((ce = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_status(ce);
-  if (bits & mr::kErrTimeout) return MOE_READER_ETIMEOUT;
+  if (bits & mr::kErrTimeout) {
+    cudaMemset(h->ws.sync, 0, mr::sync_words(d) * 4);
+    cudaMemset(h->ws.err, 0, 4);
+    return MOE_READER_ETIMEOUT;
+  }
   if (bits) return MOE_READER_EDEVICE;
   return MOE_READER_OK;
 }
@@ -367,6 +388,11 @@ int moe_reader_status(moe_reader_t* h, uint32_t* bits_out) {
   if ((ce = cudaMemcpy(&bits, h->ws.err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_status(ce);
   if ((ce = cudaMemset(h->ws.err, 0, 4)) != cudaSuccess) return cuda_status(ce);
+  if (bits & mr::kErrTimeout) {
+    // a timed-out decode leaves its counters behind: clear them for the next call
+    if ((ce = cudaMemset(h->ws.sync, 0, mr::sync_words(h->d) * 4)) != cudaSuccess)
+      return cuda_status(ce);
+  }
   if (bits_out) *bits_out = bits;
   if (bits & mr::kErrTimeout) return MOE_READER_ETIMEOUT;
   if (bits) return MOE_READER_EDEVICE;
@@ -458,10 +484,13 @@ int moe_reader_set_profiling(moe_reader_t* h, int32_t enable) {
   if (!h) return MOE_READER_EINVAL;
   if (enable && !h->prof_created) {
     for (int i = 0; i < mr::kProfSlots; ++i)
-      for (int j = 0; j <= mr::kPhases; ++j) {
+      for (int j = 0; j < 2; ++j) {
         const cudaError_t ce = cudaEventCreate(&h->prof_ev[i][j]);
         if (ce != cudaSuccess) return cuda_status(ce);
       }
+    const cudaError_t ce = cudaMalloc(
+        &h->prof_stamps, (size_t)mr::kProfSlots * h->grid * 5 * sizeof(unsigned long long));
+    if (ce != cudaSuccess) return cuda_status(ce);
     h->prof_created = 1;
   }
   h->prof_on = enable ? 1 : 0;
@@ -475,14 +504,32 @@ int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t capacity,
   const int used = h->prof_used < mr::kProfSlots ? h->prof_used : mr::kProfSlots;
   if (calls_out) *calls_out = used;
   if (capacity < used) return MOE_READER_EINVAL;
+  if (used == 0) return MOE_READER_OK;
+  std::vector<unsigned long long> st((size_t)used * h->grid * 5);
   for (int i = 0; i < used; ++i) {
-    cudaError_t ce = cudaEventSynchronize(h->prof_ev[i][mr::kPhases]);
+    const cudaError_t ce = cudaEventSynchronize(h->prof_ev[i][1]);
     if (ce != cudaSuccess) return cuda_status(ce);
-    for (int j = 0; j < mr::kPhases; ++j) {
-      float ms = 0.f;
-      ce = cudaEventElapsedTime(&ms, h->prof_ev[i][j], h->prof_ev[i][j + 1]);
-      if (ce != cudaSuccess) return cuda_status(ce);
-      ms_out[(size_t)i * mr::kPhases + j] = ms;
+  }
+  cudaError_t ce = cudaMemcpy(st.data(), h->prof_stamps, st.size() * sizeof(unsigned long long),
+                              cudaMemcpyDeviceToHost);
+  if (ce != cudaSuccess) return cuda_status(ce);
+  for (int i = 0; i < used; ++i) {
+    float ms = 0.f;
+    ce = cudaEventElapsedTime(&ms, h->prof_ev[i][0], h->prof_ev[i][1]);
+    if (ce != cudaSuccess) return cuda_status(ce);
+    double* row = ms_out + (size_t)i * mr::kPhases;
+    row[0] = ms;
+    // phase boundaries: the earliest start, then the latest end of each phase
+    unsigned long long t0 = ~0ull, e[4] = {0, 0, 0, 0};
+    for (int c = 0; c < h->grid; ++c) {
+      const unsigned long long* r = &st[((size_t)i * h->grid + c) * 5];
+      t0 = std::min(t0, r[0]);
+      for (int q = 0; q < 4; ++q) e[q] = std::max(e[q], r[q + 1]);
+    }
+    unsigned long long prev = t0;
+    for (int q = 0; q < 4; ++q) {
+      row[q + 1] = e[q] > prev ? (double)(e[q] - prev) * 1e-6 : 0.0;
+      prev = std::max(prev, e[q]);
     }
   }
   return MOE_READER_OK;
@@ -491,9 +538,11 @@ int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t capacity,
 void moe_reader_destroy(moe_reader_t* h) {
   if (!h) return;
   cudaDeviceSynchronize();
-  if (h->prof_created)
+  if (h->prof_created) {
     for (int i = 0; i < mr::kProfSlots; ++i)
-      for (int j = 0; j <= mr::kPhases; ++j) cudaEventDestroy(h->prof_ev[i][j]);
+      for (int j = 0; j < 2; ++j) cudaEventDestroy(h->prof_ev[i][j]);
+    cudaFree(h->prof_stamps);
+  }
   free_handle_memory(h);
   free(h);
 }

@@ -1,68 +1,167 @@
-// Decode kernels of the channel reader ("Channel Selection for
-// Mixture-of-Experts Decoding Needs No Calibration Data", Chinese summary
-// page, 方法步骤详情 decode steps (1)-(4) and 核心方法; Korean summary page,
-// 어떻게 쓰나).
+// Decode of the channel reader as ONE persistent cooperative kernel per call
+// ("Channel Selection for Mixture-of-Experts Decoding Needs No Calibration
+// Data", Chinese summary page, 方法步骤详情 decode steps (1)-(4) and 核心方法;
+// Korean summary page, 어떻게 쓰나).
 //
-//   rotate_kernel   Rx per 128-block (fp32 Sylvester butterfly of sigma*x) and
-//                   the c largest-|Rx| coordinates per block; routing checks
-//   screen_kernel   ghat/vhat partial sums per (token, expert, block) from the
-//                   2-bit codes of the screened coordinates, scaled by alpha
-//   topk_kernel     s_j = w_j ||d_j|| |phi(ghat_j) vhat_j|; exact top-k over all
-//                   routed channels by radix select (ties -> lower e*I + i)
-//   exact_kernel    kept channels: a_j from native BF16 g_j, v_j and fp32 x;
-//                   skipped channels: recovery partials sum w_j p_j b_j
-//   out_kernel      y = sum_K w_j a_j Dt_j + U c  (sector-wide column slices)
+// One CTA per SM, all co-resident (cooperative launch).  The phases hand work
+// to each other through counters and flags in global memory instead of
+// kernel boundaries; every wait is bounded (about one second of globaltimer),
+// after which the CTA raises the timeout bit and the abort flag and leaves.
+//
+//   phase 0  rotate x per (token, 128-block): fp32 Sylvester butterfly of
+//            sigma*x, the c largest |Rx| coordinates (ties -> lower index),
+//            routing checks; sets rot_flag[t][b]
+//   phase 1  screen unit per (token, expert slot, block): the 2-bit codes of
+//            the screened coordinates, alpha-scaled block partials of ghat and
+//            vhat.  The last unit of a (token, slot) sums the block partials in
+//            block order and scores the slot's channels,
+//            s = w ||d|| |phi(ghat) vhat|; the last slot of a token runs the
+//            exact top-k over the token's N channels (radix select on the fp32
+//            bits, ties -> lower e*I + i) and sets tok_flag[t]
+//   phase 2  warp items: kept channels (a_j = phi(g_j.x)(v_j.x) from native
+//            BF16 rows, fp32 x) and 64-channel recovery chunks
+//            (sum w_j p_j b_j over skipped channels)
+//   phase 3  output slices of 16 columns: y = sum_K w_j a_j Dt_j + U c
 #include "device_util.cuh"
 #include "internal.cuh"
 
 namespace mr {
 namespace {
 
-// ---------------------------------------------------------------------------
-// rotate_kernel: one warp per (token t, block b).  Lane l holds coordinates
-// l + 32 s (s = 0..3).  Butterfly strides 1..16 across lanes, then 32 and 64
-// in the lane: each pair (i, i+h) becomes (a + b, a - b) in fp32, the order
-// that fixes the selection decision.  Rx = z / sqrt(128) (fp32).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128)
-rotate_kernel(Dims d, int B, const float* __restrict__ x, const int32_t* __restrict__ ids_in,
-              const float* __restrict__ w_in, const int8_t* __restrict__ sigma,
-              float* __restrict__ rx, uint32_t* __restrict__ mask, int32_t* __restrict__ ids_ws,
-              float* __restrict__ w_ws, uint32_t* __restrict__ err) {
-  const int gwarp = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gwarp >= B * d.nb) return;
-  const int t = gwarp / d.nb, b = gwarp % d.nb;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kAhead = 8;              // code words a thread loads before using them
+constexpr int kMaxGroups = 16;         // coordinate groups of a screen unit
+constexpr unsigned long long kWaitNs = 1000000000ull;
 
-  // routing checks and sanitised copies (one warp per token)
+struct Params {
+  Dims d;
+  int B, k;
+  const float* x;
+  const int32_t* ids_in;
+  const float* w_in;
+  float* y;
+  const int8_t* sigma;
+  const uint8_t* codes;
+  const __half* scales;
+  const float* dnorm;
+  const __nv_bfloat16* G;
+  const __nv_bfloat16* V;
+  const __nv_bfloat16* Dt;
+  const __half* U;
+  const __half* bco;
+  int32_t* ids_ws;
+  float* w_ws;
+  float* rx;
+  uint32_t* mask;
+  float* partial;
+  float* ghat;
+  float* vhat;
+  float* p;
+  float* score;
+  uint32_t* keptbits;
+  int32_t* kept;
+  int32_t* rowoff;
+  float* wa;
+  float* cvec;                  // [Bmax][r] recovery vectors, accumulated atomically
+  unsigned long long* stamps;   // [grid][5] phase timestamps, or null
+  uint32_t* sync;
+  uint32_t* err;
+  int Q;    // coordinate groups of a screen unit
+  int W8;   // 8-byte code words per coordinate record (gate run + up run)
+};
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint2 ldg_nc2(const void* p) {
+  uint2 r;
+  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ldg_nc4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Wait (one thread) until *flag >= target.  false: timed out or aborted.
+__device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* abort_flag,
+                              uint32_t* err) {
+  if (ld_acquire(flag) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (ld_acquire(flag) >= target) return true;
+    if (ld_acquire(abort_flag)) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      atomicOr(err, kErrTimeout);
+      atomicExch(abort_flag, 1u);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Offsets (in uint32) of the synchronisation area, fixed per handle.
+struct SyncOff {
+  int rot, slot, tok, flag, total;
+};
+__host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
+  SyncOff o;
+  o.rot = 16;
+  o.slot = o.rot + d.Bmax * d.nb;
+  o.tok = o.slot + d.Bmax * d.topk;
+  o.flag = o.tok + d.Bmax;
+  o.total = o.flag + d.Bmax;
+  return o;
+}
+constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2;
+
+// ------------------------------- phase 0 -----------------------------------
+__device__ void rotate_item(const Params& P, int t, int b, int lane) {
+  const Dims& d = P.d;
+  uint32_t* err = P.err;
   if (b == 0) {
     for (int s = lane; s < d.topk; s += 32) {
-      int e = ids_in[t * d.topk + s];
-      const float wv = w_in[t * d.topk + s];
+      int e = P.ids_in[t * d.topk + s];
+      const float wv = P.w_in[t * d.topk + s];
       uint32_t bits = 0;
       if (e < 0 || e >= d.E) {
         bits |= kErrExpertRange;
         e = 0;
       }
       for (int s2 = 0; s2 < s; ++s2)
-        if (ids_in[t * d.topk + s2] == ids_in[t * d.topk + s]) bits |= kErrExpertDup;
+        if (P.ids_in[t * d.topk + s2] == P.ids_in[t * d.topk + s]) bits |= kErrExpertDup;
       if (!(wv >= 0.f) || !isfinite(wv)) bits |= kErrWeight;
       if (bits) atomicOr(err, bits);
-      ids_ws[t * d.topk + s] = e;
-      w_ws[t * d.topk + s] = wv;
+      P.ids_ws[t * d.topk + s] = e;
+      P.w_ws[t * d.topk + s] = wv;
     }
+    for (int j = lane; j < d.r; j += 32) P.cvec[(size_t)t * d.r + j] = 0.f;
   }
-
   float u[4];
   bool bad = false;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int col = b * kBlock + lane + 32 * s;
-    const float xv = col < d.H ? x[(size_t)t * d.H + col] : 0.f;
+    const float xv = col < d.H ? P.x[(size_t)t * d.H + col] : 0.f;
     bad |= !isfinite(xv);
-    u[s] = sigma[col] < 0 ? -xv : xv;
+    u[s] = P.sigma[col] < 0 ? -xv : xv;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrXNonFinite);
+  // Sylvester butterfly, strides 1, 2, ..., 64; pair (i, i+h) -> (a + b, a - b) in fp32
 #pragma unroll
   for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -79,136 +178,71 @@ rotate_kernel(Dims d, int B, const float* __restrict__ x, const int32_t* __restr
     u[0] = __fadd_rn(a0, a2); u[2] = __fsub_rn(a0, a2);
     u[1] = __fadd_rn(a1, a3); u[3] = __fsub_rn(a1, a3);
   }
-  float m[4];
+  // the c-th largest |z| by a bit search over its fp32 pattern, then ties by index
+  uint32_t m[4];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) m[s] = fabsf(u[s]);
-  // rank of each coordinate: how many coordinates beat it (larger |z|, or equal and lower index)
-  int rank[4] = {0, 0, 0, 0};
-  for (int src = 0; src < 32; ++src) {
+  for (int s = 0; s < 4; ++s) m[s] = __float_as_uint(fabsf(u[s]));
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    int cnt = 0;
 #pragma unroll
-    for (int s2 = 0; s2 < 4; ++s2) {
-      const float o = __shfl_sync(0xffffffffu, m[s2], src);
-      const int oi = src + 32 * s2;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int mi = lane + 32 * s;
-        rank[s] += (o > m[s]) || (o == m[s] && oi < mi);
-      }
-    }
+    for (int s = 0; s < 4; ++s) cnt += __popc(__ballot_sync(0xffffffffu, m[s] >= cand));
+    if (cnt >= d.c) T = cand;
   }
+  int gt = 0;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) gt += __popc(__ballot_sync(0xffffffffu, m[s] > T));
+  const int need = d.c - gt;
+  const uint32_t below = (1u << lane) - 1u;
+  int before = 0;
   const float inv = 0.08838834764831845f;   // 1/sqrt(128) rounded to fp32
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    const unsigned sel = __ballot_sync(0xffffffffu, rank[s] < d.c);
-    if (lane == 0) mask[((size_t)t * d.nb + b) * 4 + s] = sel;
-    rx[(size_t)t * d.Hp + b * kBlock + lane + 32 * s] = u[s] * inv;
+    const uint32_t eqb = __ballot_sync(0xffffffffu, m[s] == T);
+    const bool sel = m[s] > T || (m[s] == T && before + __popc(eqb & below) < need);
+    before += __popc(eqb);
+    const uint32_t word = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0) P.mask[((size_t)t * d.nb + b) * 4 + s] = word;
+    P.rx[(size_t)t * d.Hp + b * kBlock + lane + 32 * s] = u[s] * inv;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    atomicExch(&P.sync[sync_offsets(d).rot + t * d.nb + b], 1u);
   }
 }
 
-// ---------------------------------------------------------------------------
-// screen_kernel: one CTA per (token t, slot, block b).  Thread (q, j): word j
-// of the coordinate record (j < I/16: gate run, else up run; 16 channels per
-// 32-bit word), coordinate group q takes every Q-th screened coordinate.
-// A 2-bit code shifted to bits 31:30 and masked is the fp32 value 2t (code
-// 0b01 -> +2, 0b11 -> -2, 0b00 -> 0), so acc += (2t) * (r/2) is exact.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024)
-screen_kernel(Dims d, int Q, const uint8_t* __restrict__ codes, const __half* __restrict__ scales,
-              const float* __restrict__ rx, const uint32_t* __restrict__ mask,
-              const int32_t* __restrict__ ids, float* __restrict__ partial) {
-  extern __shared__ float red[];          // [Q][W*16]
-  __shared__ int clist[kBlock];
-  __shared__ float rlist[kBlock];
-  const int b = blockIdx.x % d.nb;
-  const int ts = blockIdx.x / d.nb;       // t * topk + slot
-  const int t = ts / d.topk;
-  const int e = ids[ts];
-  const int W = d.I / 8;                  // words per coordinate record (gate + up)
-  const int j = threadIdx.x % W;
-  const int q = threadIdx.x / W;
-
-  const uint32_t* mk = mask + ((size_t)t * d.nb + b) * 4;
-  for (int c = threadIdx.x; c < kBlock; c += blockDim.x) {
-    const uint32_t word = mk[c >> 5];
-    if ((word >> (c & 31)) & 1u) {
-      int pos = __popc(word & ((1u << (c & 31)) - 1u));
-      for (int w2 = 0; w2 < (c >> 5); ++w2) pos += __popc(mk[w2]);
-      clist[pos] = c;
-      rlist[pos] = 0.5f * rx[(size_t)t * d.Hp + b * kBlock + c];
-    }
-  }
-  __syncthreads();
-  const int nsel = d.c;
-
-  float acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  if (q < Q) {
-    const int half = d.I / 16;
-    const size_t run_off = j < half ? (size_t)j * 4 : (size_t)d.S + (size_t)(j - half) * 4;
-    const uint8_t* base = codes + (((size_t)e * d.nb + b) * kBlock) * 2 * d.S + run_off;
-    for (int p = q; p < nsel; p += Q) {
-      // a non-finite x can leave the mask without exactly c bits: keep the
-      // coordinate inside the block whatever the list holds
-      const int c = clist[p] & (kBlock - 1);
-      const float r = rlist[p];
-      const uint32_t w = ldg_stream1(reinterpret_cast<const uint32_t*>(base + (size_t)c * 2 * d.S));
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float tv = __uint_as_float((w << (30 - 2 * k)) & 0xC0000000u);
-        acc[k] = fmaf(tv, r, acc[k]);
-      }
-    }
-  }
-  const int WC = W * 16;
-  if (q < Q) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) red[q * WC + j * 16 + k] = acc[k];
-  }
-  __syncthreads();
-  // reduce over q and scale: channel slot (j, k) -> gv = j / (I/16), i = (j % (I/16)) * 16 + k
-  const __half* sc = scales + ((size_t)e * d.nb + b) * 2 * d.I;
-  float* out = partial + (((size_t)ts * d.nb + b) * 2) * d.I;
-  for (int o = threadIdx.x; o < WC; o += blockDim.x) {
-    float s = 0.f;
-    for (int qq = 0; qq < Q; ++qq) s += red[qq * WC + o];
-    const int jj = o / 16, k = o % 16;
-    const int half = d.I / 16;
-    const int gv = jj / half;
-    const int i = (jj % half) * 16 + k;
-    out[gv * d.I + i] = s * __half2float(sc[gv * d.I + i]);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// topk_kernel: one CTA (1024 threads) per token.  Keys are the fp32 bits of
-// s (s >= 0, so unsigned order = numeric order).  Radix select (4 x 8 bits)
-// finds the k-th largest key T; keys above T are kept, and among keys equal to
-// T the lowest global ids e*I + i are kept (second radix select on ~id).
-// ---------------------------------------------------------------------------
-__device__ uint32_t radix_select_desc(const uint32_t* keys, const uint8_t* valid, int N, int kth,
-                                      int* hist, int* shared_out, int* remaining_out) {
-  // returns the kth-largest key (1-based) among valid entries; *remaining_out =
-  // how many entries equal to it are needed to reach kth
+// ------------------------------- top-k -------------------------------------
+// k-th largest key among the entries keyfn accepts; per-warp histograms.
+template <typename KeyFn>
+__device__ uint32_t cta_radix_select(int N, int kth, KeyFn keyfn, int* hist, int* sh, int* rem) {
   uint32_t prefix = 0, pmask = 0;
   int remaining = kth;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for (int n = threadIdx.x; n < N; n += blockDim.x) {
-      if (valid && !valid[n]) continue;
-      const uint32_t kk = keys[n];
-      if ((kk & pmask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1);
+    for (int n = threadIdx.x; n < N; n += kThreads) {
+      uint32_t key;
+      if (!keyfn(n, key)) continue;
+      if ((key & pmask) == prefix) atomicAdd(&hist[warp * 256 + ((key >> shift) & 255u)], 1);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // suffix scan from digit 255 down, 8 digits per lane
-      const int lane = threadIdx.x;
+    if (threadIdx.x < 256) {
+      int tot = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) tot += hist[w * 256 + threadIdx.x];
+      hist[kWarps * 256 + threadIdx.x] = tot;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int* totals = hist + kWarps * 256;
       int local[8];
       int tot = 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        local[u] = hist[255 - (lane * 8 + u)];
+        local[u] = totals[255 - (lane * 8 + u)];
         tot += local[u];
       }
       int incl = tot;
@@ -217,118 +251,85 @@ __device__ uint32_t radix_select_desc(const uint32_t* keys, const uint8_t* valid
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      int before = incl - tot;   // count of digits above this lane's first digit
-      int found = -1, rem = 0;
+      int before = incl - tot, found = -1, r = 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         if (found < 0 && before + local[u] >= remaining) {
           found = 255 - (lane * 8 + u);
-          rem = remaining - before;
+          r = remaining - before;
         }
         before += local[u];
       }
       const unsigned bal = __ballot_sync(0xffffffffu, found >= 0);
-      const int first = __ffs(bal) - 1;
+      const int first = bal ? __ffs(bal) - 1 : 0;
       const int fd = __shfl_sync(0xffffffffu, found, first);
-      const int fr = __shfl_sync(0xffffffffu, rem, first);
+      const int fr = __shfl_sync(0xffffffffu, r, first);
       if (lane == 0) {
-        shared_out[0] = fd;
-        shared_out[1] = fr;
+        sh[0] = fd < 0 ? 0 : fd;
+        sh[1] = fr;
       }
     }
     __syncthreads();
-    const int digit = shared_out[0];
-    remaining = shared_out[1];
-    prefix |= (uint32_t)digit << shift;
+    prefix |= (uint32_t)sh[0] << shift;
     pmask |= 255u << shift;
+    remaining = sh[1];
     __syncthreads();
   }
-  *remaining_out = remaining;
+  *rem = remaining;
   return prefix;
 }
 
-__global__ void __launch_bounds__(1024)
-topk_kernel(Dims d, int k, const float* __restrict__ partial, const int32_t* __restrict__ ids,
-            const float* __restrict__ wts, const float* __restrict__ dnorm,
-            float* __restrict__ ghat, float* __restrict__ vhat, float* __restrict__ pout,
-            float* __restrict__ score, uint32_t* __restrict__ keptbits,
-            int32_t* __restrict__ kept) {
-  extern __shared__ uint32_t keys[];      // [N] then [N] tie keys, [N] bytes valid
-  uint32_t* keys2 = keys + d.N;
-  uint8_t* valid = reinterpret_cast<uint8_t*>(keys2 + d.N);
-  __shared__ int hist[256];
-  __shared__ int sout[2];
-  __shared__ int wsum[32];
-  const int t = blockIdx.x;
-  const int N = d.N;
-
-  for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    const int slot = n / d.I, i = n % d.I;
-    const float* pg = partial + (((size_t)(t * d.topk + slot) * d.nb) * 2) * d.I + i;
-    float g = 0.f, v = 0.f;
-    for (int b = 0; b < d.nb; ++b) {
-      g += pg[(size_t)b * 2 * d.I];
-      v += pg[(size_t)b * 2 * d.I + d.I];
-    }
-    const int e = ids[t * d.topk + slot];
-    const float p = silu_f(g) * v;
-    const float s = wts[t * d.topk + slot] * dnorm[(size_t)e * d.I + i] * fabsf(p);
-    const size_t o = (size_t)t * N + n;
-    ghat[o] = g;
-    vhat[o] = v;
-    pout[o] = p;
-    score[o] = s;
-    keys[n] = __float_as_uint(s);
-  }
+__device__ void topk_token(const Params& P, int t, unsigned char* smem) {
+  const Dims& d = P.d;
+  const int N = d.N, k = P.k, I = d.I;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);              // [N]
+  int* hist = reinterpret_cast<int*>(keys + N);                     // [kWarps + 1][256]
+  int* sh = hist + (kWarps + 1) * 256;                              // [4]
+  int* wsum = sh + 4;                                               // [kWarps]
+  int* eid = wsum + kWarps;                                         // [topk]
+  for (int s = threadIdx.x; s < d.topk; s += kThreads) eid[s] = __ldcg(P.ids_ws + t * d.topk + s);
+  for (int n = threadIdx.x; n < N; n += kThreads)
+    keys[n] = __float_as_uint(__ldcg(P.score + (size_t)t * N + n));
   __syncthreads();
 
-  uint32_t T = 0, T2 = 0;
-  int need = 0;
   const bool all = k >= N, none = k <= 0;
+  uint32_t T = 0, T2 = 0;
   if (!all && !none) {
-    T = radix_select_desc(keys, nullptr, N, k, hist, sout, &need);
-    // ties at T: keep the `need` lowest global ids
+    int need = 0;
+    T = cta_radix_select(
+        N, k, [&](int n, uint32_t& key) { key = keys[n]; return true; }, hist, sh, &need);
     int eq = 0;
-    for (int n = threadIdx.x; n < N; n += blockDim.x) {
-      const bool isT = keys[n] == T;
-      valid[n] = isT;
-      const int slot = n / d.I, i = n % d.I;
-      keys2[n] = 0xffffffffu - (uint32_t)(ids[t * d.topk + slot] * d.I + i);
-      eq += isT;
-    }
-    __syncthreads();
-    // count of equal keys (block reduction)
+    for (int n = threadIdx.x; n < N; n += kThreads) eq += keys[n] == T;
     eq = warp_sum_i(eq);
     if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = eq;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int tot = 0;
-      for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += wsum[q];
-      sout[0] = tot;
-    }
-    __syncthreads();
-    const int eq_total = sout[0];
+    int eq_total = 0;
+    for (int w = 0; w < kWarps; ++w) eq_total += wsum[w];
     __syncthreads();
     if (need < eq_total) {
       int dummy = 0;
-      T2 = radix_select_desc(keys2, valid, N, need, hist, sout, &dummy);
-    } else {
-      T2 = 0;   // keep every tied key
+      T2 = cta_radix_select(
+          N, need,
+          [&](int n, uint32_t& key) {
+            if (keys[n] != T) return false;
+            key = 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I);
+            return true;
+          },
+          hist, sh, &dummy);
     }
   }
-  // kept flags, bitmap and the ascending list of kept n
-  const int per = (N + blockDim.x - 1) / blockDim.x;
-  const int n0 = threadIdx.x * per;
-  const int n1 = min(N, n0 + per);
+  auto kept_fn = [&](int n) -> bool {
+    if (all) return true;
+    if (none) return false;
+    const uint32_t a = keys[n];
+    if (a != T) return a > T;
+    return (0xffffffffu - (uint32_t)(eid[n / I] * I + n % I)) >= T2;
+  };
+  // ascending compaction of kept n, and the kept bitmap
+  const int per = (N + kThreads - 1) / kThreads;
+  const int n0 = threadIdx.x * per, n1 = min(N, n0 + per);
   int cnt = 0;
-  for (int n = n0; n < n1; ++n) {
-    bool kp;
-    if (all) kp = true;
-    else if (none) kp = false;
-    else kp = keys[n] > T || (keys[n] == T && keys2[n] >= T2);
-    cnt += kp;
-  }
-  // exclusive scan of cnt over threads
+  for (int n = n0; n < n1; ++n) cnt += kept_fn(n);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int incl = cnt;
 #pragma unroll
@@ -336,335 +337,563 @@ topk_kernel(Dims d, int k, const float* __restrict__ partial, const int32_t* __r
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
-  __syncthreads();
   if (lane == 31) wsum[wid] = incl;
   __syncthreads();
+  int base = 0;
+  for (int w = 0; w < wid; ++w) base += wsum[w];
+  int pos = base + incl - cnt;
+  for (int n = n0; n < n1; ++n)
+    if (kept_fn(n)) {
+      if (pos < N) P.kept[(size_t)t * N + pos] = n;
+      ++pos;
+    }
+  for (int wd = threadIdx.x; wd < N / 32; wd += kThreads) {
+    uint32_t bits = 0;
+    for (int u = 0; u < 32; ++u) bits |= (uint32_t)kept_fn(wd * 32 + u) << u;
+    P.keptbits[(size_t)t * (N / 32) + wd] = bits;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    int run = 0;
-    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) {
-      const int v = wsum[q];
-      wsum[q] = run;
-      run += v;
+    __threadfence();
+    atomicExch(&P.sync[sync_offsets(d).flag + t], 1u);
+  }
+}
+
+// ------------------------------- phase 1 -----------------------------------
+// false: the CTA must stop (timeout / abort)
+__device__ bool screen_unit(const Params& P, int t, int slot, int b, unsigned char* smem) {
+  const Dims& d = P.d;
+  const SyncOff so = sync_offsets(d);
+  const int ts = t * d.topk + slot;
+  int e = P.ids_in[ts];
+  if (e < 0 || e >= d.E) e = 0;
+  const int I = d.I;
+  // shared memory: alpha [2I] half, clist [128] int, rlist [128] float, flags [4], red [Q][2I]
+  __half* alpha = reinterpret_cast<__half*>(smem);
+  int* clist = reinterpret_cast<int*>(smem + 4 * (size_t)I);
+  float* rlist = reinterpret_cast<float*>(clist + kBlock);
+  int* flags = reinterpret_cast<int*>(rlist + kBlock);
+  float* red = reinterpret_cast<float*>(flags + 4);
+
+  const __half* sc = P.scales + ((size_t)e * d.nb + b) * 2 * I;
+  for (int i = threadIdx.x; i < I / 4; i += kThreads)
+    reinterpret_cast<uint4*>(alpha)[i] = ldg_nc4(reinterpret_cast<const uint4*>(sc) + i);
+  if (threadIdx.x == 0)
+    flags[0] = wait_at_least(P.sync + so.rot + t * d.nb + b, 1u, P.sync + kSyncAbort, P.err);
+  __syncthreads();
+  if (!flags[0]) return false;
+  if (threadIdx.x < kBlock) {
+    const int c = threadIdx.x;
+    const uint32_t* mk = P.mask + ((size_t)t * d.nb + b) * 4;
+    const uint32_t word = __ldcg(mk + (c >> 5));
+    if ((word >> (c & 31)) & 1u) {
+      int pos = __popc(word & ((1u << (c & 31)) - 1u));
+      for (int w2 = 0; w2 < (c >> 5); ++w2) pos += __popc(__ldcg(mk + w2));
+      if (pos < kBlock) {
+        clist[pos] = c;
+        rlist[pos] = 0.5f * __ldcg(P.rx + (size_t)t * d.Hp + b * kBlock + c);
+      }
     }
   }
   __syncthreads();
-  int pos = wsum[wid] + incl - cnt;
-  for (int n = n0; n < n1; ++n) {
-    bool kp;
-    if (all) kp = true;
-    else if (none) kp = false;
-    else kp = keys[n] > T || (keys[n] == T && keys2[n] >= T2);
-    if (kp) kept[(size_t)t * N + pos++] = n;
-  }
-  // bitmap: one word per 32 channels
-  for (int wdx = threadIdx.x; wdx < N / 32; wdx += blockDim.x) {
-    uint32_t bits = 0;
-    for (int u = 0; u < 32; ++u) {
-      const int n = wdx * 32 + u;
-      bool kp;
-      if (all) kp = true;
-      else if (none) kp = false;
-      else kp = keys[n] > T || (keys[n] == T && keys2[n] >= T2);
-      bits |= (uint32_t)kp << u;
+
+  const int W8 = P.W8, Q = P.Q;
+  const int j = threadIdx.x % W8, q = threadIdx.x / W8;
+  const int half = I / 32;                          // 8-byte words per run
+  if (q < Q) {
+    float acc[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) acc[u] = 0.f;
+    const size_t run_off = j < half ? (size_t)j * 8 : (size_t)d.S + (size_t)(j - half) * 8;
+    const uint8_t* base = P.codes + (((size_t)e * d.nb + b) * kBlock) * 2 * d.S + run_off;
+    for (int p0 = q; p0 < d.c; p0 += Q * kAhead) {
+      uint2 wv[kAhead];
+      float rv[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+        const int pp = p0 + u * Q;
+        if (pp < d.c) {
+          const int cc = clist[pp] & (kBlock - 1);
+          wv[u] = ldg_nc2(base + (size_t)cc * 2 * d.S);
+          rv[u] = rlist[pp];
+        } else {
+          wv[u] = make_uint2(0u, 0u);
+          rv[u] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+        // a 2-bit code moved to bits 31:30 and masked is the fp32 value 2t;
+        // rv holds r/2, so each product is exactly +-r or 0
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          acc[kk] = fmaf(__uint_as_float((wv[u].x << (30 - 2 * kk)) & 0xC0000000u), rv[u], acc[kk]);
+          acc[16 + kk] =
+              fmaf(__uint_as_float((wv[u].y << (30 - 2 * kk)) & 0xC0000000u), rv[u], acc[16 + kk]);
+        }
+      }
     }
-    keptbits[(size_t)t * (N / 32) + wdx] = bits;
+    // code-major layout [q][kk][j]: consecutive threads (j) hit consecutive banks
+#pragma unroll
+    for (int u = 0; u < 32; ++u) red[(size_t)q * 2 * I + u * W8 + j] = acc[u];
+  }
+  __syncthreads();
+  float* out = P.partial + ((size_t)ts * d.nb + b) * 2 * I;
+  for (int o = threadIdx.x; o < 2 * I; o += kThreads) {
+    const int jj = o / 32, kk = o % 32;
+    float s = 0.f;
+    for (int qq = 0; qq < Q; ++qq) s += red[(size_t)qq * 2 * I + kk * W8 + jj];
+    const int gv = jj / half;
+    const int i = (jj % half) * 32 + kk;
+    out[gv * I + i] = s * __half2float(alpha[gv * I + i]);
+  }
+  // publish: the barrier orders the CTA's stores before thread 0's fence + atomic
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    flags[1] = atomicAdd(P.sync + so.slot + ts, 1u) == (uint32_t)(d.nb - 1);
+    if (flags[1]) __threadfence();
+  }
+  __syncthreads();
+  if (!flags[1]) return true;
+
+  // the last block of this (token, slot): score its channels
+  const float wv = P.w_in[ts];
+  for (int i = threadIdx.x; i < I; i += kThreads) {
+    const float* pg = P.partial + ((size_t)ts * d.nb) * 2 * I + i;
+    float g = 0.f, v = 0.f;
+    int bb = 0;
+    for (; bb + 8 <= d.nb; bb += 8) {   // loads first, then the sums in block order
+      float gg[8], vv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        gg[u] = __ldcg(pg + (size_t)(bb + u) * 2 * I);
+        vv[u] = __ldcg(pg + (size_t)(bb + u) * 2 * I + I);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        g += gg[u];
+        v += vv[u];
+      }
+    }
+    for (; bb < d.nb; ++bb) {
+      g += __ldcg(pg + (size_t)bb * 2 * I);
+      v += __ldcg(pg + (size_t)bb * 2 * I + I);
+    }
+    const float pv = silu_f(g) * v;
+    const float s = wv * __ldg(P.dnorm + (size_t)e * I + i) * fabsf(pv);
+    const size_t o = (size_t)t * d.N + (size_t)slot * I + i;
+    P.ghat[o] = g;
+    P.vhat[o] = v;
+    P.p[o] = pv;
+    P.score[o] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    flags[2] = atomicAdd(P.sync + so.tok + t, 1u) == (uint32_t)(d.topk - 1);
+    if (flags[2]) __threadfence();
+  }
+  __syncthreads();
+  if (!flags[2]) return true;
+  topk_token(P, t, smem);
+  __syncthreads();
+  return true;
+}
+
+// ------------------------------- phase 2 -----------------------------------
+__device__ __forceinline__ void dot8(const uint4& q, const float4& xa, const float4& xb, float& s) {
+  s = fmaf(bf16_lo(q.x), xa.x, s); s = fmaf(bf16_hi(q.x), xa.y, s);
+  s = fmaf(bf16_lo(q.y), xa.z, s); s = fmaf(bf16_hi(q.y), xa.w, s);
+  s = fmaf(bf16_lo(q.z), xb.x, s); s = fmaf(bf16_hi(q.z), xb.y, s);
+  s = fmaf(bf16_lo(q.w), xb.z, s); s = fmaf(bf16_hi(q.w), xb.w, s);
+}
+
+__device__ void kept_item(const Params& P, int t, int qi, int lane) {
+  const Dims& d = P.d;
+  const int n = __ldcg(P.kept + (size_t)t * d.N + qi);
+  const int slot = n / d.I, i = n % d.I;
+  const int e = __ldcg(P.ids_ws + t * d.topk + slot);
+  const size_t row = (size_t)e * d.I + i;
+  const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
+  const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
+  const float4* x4 = reinterpret_cast<const float4*>(P.x + (size_t)t * d.H);
+  float sg = 0.f, sv = 0.f;
+  const int n8 = d.H / 8;
+  int h8 = lane;
+  for (; h8 + 96 < n8; h8 += 128) {
+    uint4 gq[4], vq[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      gq[u] = ldg_nc4(g4 + h8 + 32 * u);
+      vq[u] = ldg_nc4(v4 + h8 + 32 * u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 xa = __ldg(x4 + 2 * (h8 + 32 * u)), xb = __ldg(x4 + 2 * (h8 + 32 * u) + 1);
+      dot8(gq[u], xa, xb, sg);
+      dot8(vq[u], xa, xb, sv);
+    }
+  }
+  for (; h8 < n8; h8 += 32) {
+    const uint4 gq = ldg_nc4(g4 + h8), vq = ldg_nc4(v4 + h8);
+    const float4 xa = __ldg(x4 + 2 * h8), xb = __ldg(x4 + 2 * h8 + 1);
+    dot8(gq, xa, xb, sg);
+    dot8(vq, xa, xb, sv);
+  }
+  sg = warp_sum(sg);
+  sv = warp_sum(sv);
+  if (lane == 0) {
+    P.wa[(size_t)t * d.N + qi] = __ldcg(P.w_ws + t * d.topk + slot) * silu_f(sg) * sv;
+    P.rowoff[(size_t)t * d.N + qi] = (int32_t)row;
   }
 }
 
-// ---------------------------------------------------------------------------
-// exact_kernel: warps [0, B*k) take kept channels (a_j from native rows),
-// warps [B*k, B*k + B*N/64) take 64-channel recovery chunks.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
-exact_kernel(Dims d, int B, int k, const float* __restrict__ x, const __nv_bfloat16* __restrict__ G,
-             const __nv_bfloat16* __restrict__ V, const int32_t* __restrict__ ids,
-             const float* __restrict__ wts, const int32_t* __restrict__ kept,
-             const uint32_t* __restrict__ keptbits, const float* __restrict__ p,
-             const __half* __restrict__ bco, float* __restrict__ wa, float* __restrict__ cpart) {
-  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const long long nk = (long long)B * k;
-  const int chunks = d.N / 64;
-  if (gw < nk) {
-    const int t = (int)(gw / k), qi = (int)(gw % k);
-    const int n = kept[(size_t)t * d.N + qi];
-    const int slot = n / d.I, i = n % d.I;
-    const int e = ids[t * d.topk + slot];
-    const uint4* g4 = reinterpret_cast<const uint4*>(G + ((size_t)e * d.I + i) * d.H);
-    const uint4* v4 = reinterpret_cast<const uint4*>(V + ((size_t)e * d.I + i) * d.H);
-    const float4* x4 = reinterpret_cast<const float4*>(x + (size_t)t * d.H);
-    float sg = 0.f, sv = 0.f;
-    for (int h8 = lane; h8 < d.H / 8; h8 += 32) {
-      const uint4 gq = ldg_stream(g4 + h8);
-      const uint4 vq = ldg_stream(v4 + h8);
-      const float4 xa = x4[2 * h8], xb = x4[2 * h8 + 1];
-      sg = fmaf(bf16_lo(gq.x), xa.x, sg); sg = fmaf(bf16_hi(gq.x), xa.y, sg);
-      sg = fmaf(bf16_lo(gq.y), xa.z, sg); sg = fmaf(bf16_hi(gq.y), xa.w, sg);
-      sg = fmaf(bf16_lo(gq.z), xb.x, sg); sg = fmaf(bf16_hi(gq.z), xb.y, sg);
-      sg = fmaf(bf16_lo(gq.w), xb.z, sg); sg = fmaf(bf16_hi(gq.w), xb.w, sg);
-      sv = fmaf(bf16_lo(vq.x), xa.x, sv); sv = fmaf(bf16_hi(vq.x), xa.y, sv);
-      sv = fmaf(bf16_lo(vq.y), xa.z, sv); sv = fmaf(bf16_hi(vq.y), xa.w, sv);
-      sv = fmaf(bf16_lo(vq.z), xb.x, sv); sv = fmaf(bf16_hi(vq.z), xb.y, sv);
-      sv = fmaf(bf16_lo(vq.w), xb.z, sv); sv = fmaf(bf16_hi(vq.w), xb.w, sv);
-    }
-    sg = warp_sum(sg);
-    sv = warp_sum(sv);
-    if (lane == 0) wa[(size_t)t * d.N + qi] = wts[t * d.topk + slot] * silu_f(sg) * sv;
-    return;
-  }
-  const long long rw = gw - nk;
-  if (rw >= (long long)B * chunks) return;
-  const int t = (int)(rw / chunks), ch = (int)(rw % chunks);
+__device__ void recovery_item(const Params& P, int t, int ch, int lane) {
+  // 64 channels: lane l takes channels l and l + 32 (full b rows), then the
+  // warp transposes and sums the 32 lane vectors; lane j ends with component j
+  const Dims& d = P.d;
   const int n0 = ch * 64;
   const int slot = n0 / d.I;
-  const int e = ids[t * d.topk + slot];
-  const float wv = wts[t * d.topk + slot];
-  const uint32_t kb0 = keptbits[(size_t)t * (d.N / 32) + ch * 2];
-  const uint32_t kb1 = keptbits[(size_t)t * (d.N / 32) + ch * 2 + 1];
-  float a0 = 0.f, a1 = 0.f;
-  for (int u = 0; u < 64; ++u) {
-    const uint32_t kb = u < 32 ? kb0 : kb1;
-    if ((kb >> (u & 31)) & 1u) continue;
-    const int n = n0 + u;
-    const int i = n % d.I;
-    const float coef = wv * p[(size_t)t * d.N + n];
-    const __half* brow = bco + ((size_t)e * d.I + i) * d.r;
-    if (lane < d.r) a0 = fmaf(coef, __half2float(brow[lane]), a0);
-    if (lane + 32 < d.r) a1 = fmaf(coef, __half2float(brow[lane + 32]), a1);
+  const int e = __ldcg(P.ids_ws + t * d.topk + slot);
+  const float wv = __ldcg(P.w_ws + t * d.topk + slot);
+  const uint32_t kb0 = __ldcg(P.keptbits + (size_t)t * (d.N / 32) + ch * 2);
+  const uint32_t kb1 = __ldcg(P.keptbits + (size_t)t * (d.N / 32) + ch * 2 + 1);
+  const bool s0 = !((kb0 >> lane) & 1u), s1 = !((kb1 >> lane) & 1u);
+  const float c0 = s0 ? wv * __ldcg(P.p + (size_t)t * d.N + n0 + lane) : 0.f;
+  const float c1 = s1 ? wv * __ldcg(P.p + (size_t)t * d.N + n0 + 32 + lane) : 0.f;
+  const __half* b0 = P.bco + ((size_t)e * d.I + (n0 % d.I) + lane) * d.r;
+  const __half* b1 = b0 + (size_t)32 * d.r;
+  for (int j0 = 0; j0 < d.r; j0 += 32) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    const int jn = min(32, d.r - j0);
+    if ((d.r & 7) == 0) {
+      // rows are 16-byte aligned: 8 components per load
+      uint4 q0[4], q1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool in = 8 * u < jn;
+        q0[u] = (in && s0) ? ldg_nc4(b0 + j0 + 8 * u) : make_uint4(0, 0, 0, 0);
+        q1[u] = (in && s1) ? ldg_nc4(b1 + j0 + 8 * u) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t w0[4] = {q0[u].x, q0[u].y, q0[u].z, q0[u].w};
+        const uint32_t w1[4] = {q1[u].x, q1[u].y, q1[u].z, q1[u].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&w0[h]));
+          const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&w1[h]));
+          v[8 * u + 2 * h] = fmaf(c1, f1.x, c0 * f0.x);
+          v[8 * u + 2 * h + 1] = fmaf(c1, f1.y, c0 * f0.y);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j < jn) {
+          const float x0 = s0 ? c0 * __half2float(b0[j0 + j]) : 0.f;
+          v[j] = s1 ? fmaf(c1, __half2float(b1[j0 + j]), x0) : x0;
+        }
+      }
+    }
+    // recursive halving: after 5 rounds lane l holds the warp sum of component l
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int j = 0; j < off; ++j) {
+        const float send = upper ? v[j] : v[j + off];
+        const float keep = upper ? v[j + off] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    if (lane < jn) atomicAdd(P.cvec + (size_t)t * d.r + j0 + lane, v[0]);
   }
-  float* cp = cpart + ((size_t)t * chunks + ch) * d.r;
-  if (lane < d.r) cp[lane] = a0;
-  if (lane + 32 < d.r) cp[lane + 32] = a1;
 }
 
-// ---------------------------------------------------------------------------
-// out_kernel: one CTA per 16-column slice h0..h0+15 (one 32-byte sector of
-// each transposed down row).  Thread (rg, half): kept rows rg, rg+128, ...;
-// 8 columns each.  y = sum_K (w a)_j Dt_j + U c, c = sum over recovery chunks.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
-out_kernel(Dims d, int B, int k, const __nv_bfloat16* __restrict__ Dt,
-           const int32_t* __restrict__ ids, const int32_t* __restrict__ kept,
-           const float* __restrict__ wa, const float* __restrict__ cpart,
-           const __half* __restrict__ U, float* __restrict__ y) {
-  __shared__ float red[128][17];
-  __shared__ float cvec[kMaxRank];
-  const int h0 = blockIdx.x * 16;
-  const int rg = threadIdx.x >> 1, hf = threadIdx.x & 1;
-  const int chunks = d.N / 64;
-  for (int t = 0; t < B; ++t) {
-    float acc[8];
+// ------------------------------- phase 3 -----------------------------------
+__device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
+  acc[0] = fmaf(c, bf16_lo(v.x), acc[0]); acc[1] = fmaf(c, bf16_hi(v.x), acc[1]);
+  acc[2] = fmaf(c, bf16_lo(v.y), acc[2]); acc[3] = fmaf(c, bf16_hi(v.y), acc[3]);
+  acc[4] = fmaf(c, bf16_lo(v.z), acc[4]); acc[5] = fmaf(c, bf16_hi(v.z), acc[5]);
+  acc[6] = fmaf(c, bf16_lo(v.w), acc[6]); acc[7] = fmaf(c, bf16_hi(v.w), acc[7]);
+}
+
+constexpr int kTokGroup = 4;
+
+__device__ void out_slice(const Params& P, int s, unsigned char* smem) {
+  const Dims& d = P.d;
+  float* wred = reinterpret_cast<float*>(smem);       // [kTokGroup][kWarps][16]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h0 = s * 16;
+  const int rg = threadIdx.x >> 1, hf = threadIdx.x & 1;   // 256 row groups x 2 halves
+  const int hh = h0 + hf * 8;
+  for (int t0 = 0; t0 < P.B; t0 += kTokGroup) {
+    float acc[kTokGroup][8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-    const int hh = h0 + hf * 8;
+    for (int tt = 0; tt < kTokGroup; ++tt)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[tt][u] = 0.f;
     if (hh < d.H) {
-      for (int q = rg; q < k; q += 128) {
-        const int n = kept[(size_t)t * d.N + q];
-        const int slot = n / d.I, i = n % d.I;
-        const int e = ids[t * d.topk + slot];
-        const float c = wa[(size_t)t * d.N + q];
-        const uint4 dq = ldg_stream(reinterpret_cast<const uint4*>(Dt + ((size_t)e * d.I + i) * d.H + hh));
-        acc[0] = fmaf(c, bf16_lo(dq.x), acc[0]); acc[1] = fmaf(c, bf16_hi(dq.x), acc[1]);
-        acc[2] = fmaf(c, bf16_lo(dq.y), acc[2]); acc[3] = fmaf(c, bf16_hi(dq.y), acc[3]);
-        acc[4] = fmaf(c, bf16_lo(dq.z), acc[4]); acc[5] = fmaf(c, bf16_hi(dq.z), acc[5]);
-        acc[6] = fmaf(c, bf16_lo(dq.w), acc[6]); acc[7] = fmaf(c, bf16_hi(dq.w), acc[7]);
-      }
-    }
+      for (int q = rg; q < P.k; q += 256) {
+        int32_t r[kTokGroup];
+        float c[kTokGroup];
+        uint4 v[kTokGroup];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) red[rg][hf * 8 + u] = acc[u];
-    // recovery vector c for token t
-    if (threadIdx.x < d.r) {
-      float s = 0.f;
-      if (k < d.N)
-        for (int ch = 0; ch < chunks; ++ch) s += cpart[((size_t)t * chunks + ch) * d.r + threadIdx.x];
-      cvec[threadIdx.x] = s;
+        for (int tt = 0; tt < kTokGroup; ++tt) {
+          const int t = t0 + tt;
+          r[tt] = t < P.B ? __ldcg(P.rowoff + (size_t)t * d.N + q) : 0;
+          c[tt] = t < P.B ? __ldcg(P.wa + (size_t)t * d.N + q) : 0.f;
+        }
+#pragma unroll
+        for (int tt = 0; tt < kTokGroup; ++tt)
+          v[tt] = t0 + tt < P.B ? ldg_nc4(P.Dt + (size_t)r[tt] * d.H + hh) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int tt = 0; tt < kTokGroup; ++tt) axpy8(c[tt], v[tt], acc[tt]);
+      }
     }
+    // sum the 16 row groups of the warp (lane bits 1..4), then the 16 warps
+#pragma unroll
+    for (int tt = 0; tt < kTokGroup; ++tt)
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int o = 2; o < 32; o <<= 1) acc[tt][u] += __shfl_xor_sync(0xffffffffu, acc[tt][u], o);
+    if (lane < 2)
+#pragma unroll
+      for (int tt = 0; tt < kTokGroup; ++tt)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wred[(tt * kWarps + warp) * 16 + lane * 8 + u] = acc[tt][u];
     __syncthreads();
-    if (threadIdx.x < 16) {
-      const int h = h0 + threadIdx.x;
-      float s = 0.f;
-      for (int q = 0; q < 128; ++q) s += red[q][threadIdx.x];
-      if (h < d.H) {
-        if (k < d.N)
-          for (int j = 0; j < d.r; ++j) s = fmaf(__half2float(U[(size_t)h * d.r + j]), cvec[j], s);
-        y[(size_t)t * d.H + h] = s;
+    if (threadIdx.x < 16 * kTokGroup) {
+      const int tt = threadIdx.x >> 4, col = threadIdx.x & 15;
+      const int t = t0 + tt, h = h0 + col;
+      if (t < P.B && h < d.H) {
+        float sum = 0.f;
+        for (int w = 0; w < kWarps; ++w) sum += wred[(tt * kWarps + w) * 16 + col];
+        if (P.k < d.N)
+          for (int jj = 0; jj < d.r; ++jj)
+            sum = fmaf(__half2float(P.U[(size_t)h * d.r + jj]),
+                       __ldcg(P.cvec + (size_t)t * d.r + jj), sum);
+        P.y[(size_t)t * d.H + h] = sum;
       }
     }
     __syncthreads();
   }
 }
 
-// ---------------------------------------------------------------------------
-// Read accounting of the last decode (union over the batch).
-// ---------------------------------------------------------------------------
-__global__ void stats_mark_kernel(Dims d, int B, const int32_t* __restrict__ ids,
-                                  const uint32_t* __restrict__ mask,
-                                  const uint32_t* __restrict__ keptbits,
-                                  uint32_t* __restrict__ bm_codes, uint32_t* __restrict__ bm_kept,
-                                  uint32_t* __restrict__ bm_skip, uint32_t* __restrict__ bm_expert) {
-  const int ts = blockIdx.x;   // t * topk + slot
-  const int t = ts / d.topk, slot = ts % d.topk;
-  const int e = ids[ts];
-  if (threadIdx.x == 0) atomicOr(&bm_expert[e >> 5], 1u << (e & 31));
-  for (int q = threadIdx.x; q < d.nb * 4; q += blockDim.x)
-    atomicOr(&bm_codes[(size_t)e * d.nb * 4 + q], mask[(size_t)t * d.nb * 4 + q]);
-  for (int wd = threadIdx.x; wd < d.I / 32; wd += blockDim.x) {
-    const uint32_t kb = keptbits[(size_t)t * (d.N / 32) + slot * (d.I / 32) + wd];
-    atomicOr(&bm_kept[(size_t)e * (d.I / 32) + wd], kb);
-    atomicOr(&bm_skip[(size_t)e * (d.I / 32) + wd], ~kb);
-  }
-}
+// ------------------------------- the kernel --------------------------------
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int ctl[2];
+  const Dims& d = P.d;
+  const SyncOff so = sync_offsets(d);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nctas = gridDim.x;
+  uint32_t* abort_flag = P.sync + kSyncAbort;
+  unsigned long long* stamp = P.stamps ? P.stamps + (size_t)blockIdx.x * 5 : nullptr;
+  if (stamp && threadIdx.x == 0) stamp[0] = globaltimer();
 
-__global__ void stats_count_kernel(Dims d, const uint32_t* __restrict__ bm_codes,
-                                   const uint32_t* __restrict__ bm_kept,
-                                   const uint32_t* __restrict__ bm_skip,
-                                   const uint32_t* __restrict__ bm_expert,
-                                   unsigned long long* __restrict__ out) {
-  // out: [0] coordinate runs, [1] kept rows, [2] skipped rows, [3] routed experts,
-  //      [4] b sectors
-  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  unsigned long long runs = 0, kr = 0, sr = 0, ex = 0, bsec = 0;
-  for (long long q = gtid; q < (long long)d.E * d.nb * 4; q += nthreads) runs += __popc(bm_codes[q]);
-  for (long long q = gtid; q < (long long)d.E * (d.I / 32); q += nthreads) {
-    kr += __popc(bm_kept[q]);
-    sr += __popc(bm_skip[q]);
+  // phase 0: rotations, one warp per (token, block), spread over CTAs first
+  {
+    const int items = P.B * d.nb;
+    for (int it = blockIdx.x + nctas * warp; it < items; it += nctas * kWarps)
+      rotate_item(P, it / d.nb, it % d.nb, lane);
   }
-  for (long long q = gtid; q < (d.E + 31) / 32; q += nthreads) ex += __popc(bm_expert[q]);
-  // b sectors: sector s of the b array covers bytes [32 s, 32 s + 32)
-  const long long rowb = 2LL * d.r;
-  const long long nsec = ((long long)d.E * d.I * rowb + 31) / 32;
-  for (long long s = gtid; s < nsec; s += nthreads) {
-    const long long r0 = (32 * s) / rowb, r1 = (32 * s + 31) / rowb;
-    bool any = false;
-    for (long long rr = r0; rr <= r1 && rr < (long long)d.E * d.I; ++rr)
-      any |= (bm_skip[rr >> 5] >> (rr & 31)) & 1u;
-    bsec += any;
+  if (stamp) {
+    __syncthreads();
+    if (threadIdx.x == 0) stamp[1] = globaltimer();
   }
-  if (runs) atomicAdd(&out[0], runs);
-  if (kr) atomicAdd(&out[1], kr);
-  if (sr) atomicAdd(&out[2], sr);
-  if (ex) atomicAdd(&out[3], ex);
-  if (bsec) atomicAdd(&out[4], bsec);
-}
-
-__global__ void gather_kept_kernel(Dims d, int B, int k, const int32_t* __restrict__ ids,
-                                   const int32_t* __restrict__ kept, int32_t* __restrict__ out) {
-  const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (q >= (long long)B * k) return;
-  const int t = (int)(q / k), qi = (int)(q % k);
-  const int n = kept[(size_t)t * d.N + qi];
-  const int slot = n / d.I, i = n % d.I;
-  out[q] = ids[t * d.topk + slot] * d.I + i;
+  // phase 1: screen units (token, slot, block)
+  {
+    const int units = P.B * d.topk * d.nb;
+    for (int u = blockIdx.x; u < units; u += nctas) {
+      const int b = u % d.nb, ts = u / d.nb;
+      if (!screen_unit(P, ts / d.topk, ts % d.topk, b, smem)) return;
+      __syncthreads();
+    }
+  }
+  if (stamp && threadIdx.x == 0) stamp[2] = globaltimer();
+  // phase 2: kept channels and recovery chunks, one warp each
+  const int per_tok = P.k + d.N / 64;
+  const long long M = (long long)P.B * per_tok;
+  {
+    const long long wtot = (long long)nctas * kWarps;
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    int cur_t = -1;
+    for (long long q = gw; q < M; q += wtot) {
+      const int t = (int)(q / per_tok), local = (int)(q % per_tok);
+      if (t != cur_t) {
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_at_least(P.sync + so.flag + t, 1u, abort_flag, P.err);
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) break;
+        __syncwarp();
+        cur_t = t;
+      }
+      if (local < P.k)
+        kept_item(P, t, local, lane);
+      else
+        recovery_item(P, t, local - P.k, lane);
+    }
+  }
+  __syncthreads();
+  if (stamp && threadIdx.x == 0) stamp[3] = globaltimer();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int ok = ld_acquire(abort_flag) == 0u;
+    if (ok) {
+      long long mine = 0;
+      const long long wtot = (long long)nctas * kWarps;
+      for (int w = 0; w < kWarps; ++w) {
+        const long long gw = (long long)blockIdx.x * kWarps + w;
+        if (gw < M) mine += (M - 1 - gw) / wtot + 1;
+      }
+      atomicAdd(P.sync + kSyncExact, (uint32_t)mine);
+      ok = wait_at_least(P.sync + kSyncExact, (uint32_t)M, abort_flag, P.err);
+    }
+    ctl[1] = ok;
+  }
+  __syncthreads();
+  if (!ctl[1]) return;
+  // phase 3: output slices
+  {
+    const int slices = (d.H + 15) / 16;
+    for (int s = blockIdx.x; s < slices; s += nctas) out_slice(P, s, smem);
+  }
+  if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
+  // the last CTA out resets the synchronisation area for the next call
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    ctl[0] = atomicAdd(P.sync + kSyncDone, 1u) == (uint32_t)(nctas - 1);
+  }
+  __syncthreads();
+  if (ctl[0]) {
+    for (int i = threadIdx.x; i < P.B * d.nb; i += kThreads) P.sync[so.rot + i] = 0u;
+    for (int i = threadIdx.x; i < P.B * d.topk; i += kThreads) P.sync[so.slot + i] = 0u;
+    for (int i = threadIdx.x; i < P.B; i += kThreads) {
+      P.sync[so.tok + i] = 0u;
+      P.sync[so.flag + i] = 0u;
+    }
+    if (threadIdx.x == 0) {
+      P.sync[kSyncExact] = 0u;
+      P.sync[kSyncDone] = 0u;
+    }
+  }
 }
 
 int screen_groups(const Dims& d) {
-  const int W = d.I / 8;
-  int Q = 1024 / W;
-  if (Q > 8) Q = 8;
+  const int W8 = d.I / 16;
+  int Q = kThreads / W8;
+  if (Q > kMaxGroups) Q = kMaxGroups;
   if (Q < 1) Q = 1;
   return Q;
 }
 
+size_t decode_smem_bytes(const Dims& d) {
+  const int Q = screen_groups(d);
+  const size_t screen = (size_t)4 * d.I + kBlock * 8 + 16 + (size_t)Q * 2 * d.I * 4;
+  const size_t topk = (size_t)4 * d.N + (size_t)(kWarps + 1) * 256 * 4 + 16 + kWarps * 4 +
+                      kMaxTopk * 4;
+  const size_t out = (size_t)kTokGroup * kWarps * 16 * 4;
+  const size_t m = screen > topk ? screen : topk;
+  return m > out ? m : out;
+}
+
 }  // namespace
 
+size_t sync_words(const Dims& d) { return (size_t)sync_offsets(d).total; }
+
+cudaError_t configure_decode_kernels(const Dims& d) {
+  const size_t smem = decode_smem_bytes(d);
+  cudaFuncAttributes fa;
+  cudaError_t err = cudaFuncGetAttributes(&fa, decode_kernel);
+  if (err != cudaSuccess) return err;
+  if ((size_t)fa.maxDynamicSharedSizeBytes < smem)
+    err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+  return err;
+}
+
+int decode_grid(const Dims& d) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads,
+                                                    decode_smem_bytes(d)) != cudaSuccess)
+    return 0;
+  return per_sm >= 1 ? sms : 0;   // one CTA per SM, all co-resident
+}
+
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
-                          const float* w, int k, float* y, cudaStream_t s,
-                          const cudaEvent_t* ev) {
+                          const float* w, int k, float* y, cudaStream_t s, const cudaEvent_t* ev,
+                          unsigned long long* stamps) {
   const Dims& d = h.d;
   const Workspace& ws = h.ws;
   cudaError_t err;
-  // Inside stream capture a plain event record is only a dependency marker;
-  // the External flag makes it an event-record node of the graph.
   unsigned int rec_flags = cudaEventRecordDefault;
   if (ev) {
+    // inside stream capture a plain record is only a dependency marker; the
+    // External flag makes it an event-record node of the graph
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if ((err = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return err;
     if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+    if ((err = cudaEventRecordWithFlags(ev[0], s, rec_flags)) != cudaSuccess) return err;
   }
-#define MR_MARK(i) \
-  if (ev && (err = cudaEventRecordWithFlags(ev[i], s, rec_flags)) != cudaSuccess) return err;
-  MR_MARK(0)
-  const int rot_warps = B * d.nb;
-  rotate_kernel<<<(rot_warps + 3) / 4, 128, 0, s>>>(d, B, x, ids, w, h.p.sigma, ws.rx, ws.mask,
-                                                    ws.ids, ws.w, ws.err);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  MR_MARK(1)
+  Params P;
+  P.d = d;
+  P.B = B;
+  P.k = k;
+  P.x = x;
+  P.ids_in = ids;
+  P.w_in = w;
+  P.y = y;
+  P.sigma = h.p.sigma;
+  P.codes = h.p.codes;
+  P.scales = h.p.scales;
+  P.dnorm = h.p.dnorm;
+  P.G = h.G;
+  P.V = h.V;
+  P.Dt = h.p.Dt;
+  P.U = h.p.U;
+  P.bco = h.p.b;
+  P.ids_ws = ws.ids;
+  P.w_ws = ws.w;
+  P.rx = ws.rx;
+  P.mask = ws.mask;
+  P.partial = ws.partial;
+  P.ghat = ws.ghat;
+  P.vhat = ws.vhat;
+  P.p = ws.p;
+  P.score = ws.score;
+  P.keptbits = ws.keptbits;
+  P.kept = ws.kept;
+  P.rowoff = ws.rowoff;
+  P.wa = ws.wa;
+  P.cvec = ws.cpart;
+  P.stamps = stamps;
+  P.sync = ws.sync;
+  P.err = ws.err;
+  P.Q = screen_groups(d);
+  P.W8 = d.I / 16;
 
-  const int Q = screen_groups(d);
-  const int W = d.I / 8;
-  const size_t ssm = (size_t)Q * W * 16 * sizeof(float);
-  screen_kernel<<<B * d.topk * d.nb, W * Q, ssm, s>>>(d, Q, h.p.codes, h.p.scales, ws.rx, ws.mask,
-                                                      ws.ids, ws.partial);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  MR_MARK(2)
-
-  const size_t tsm = (size_t)d.N * 9;
-  topk_kernel<<<B, 1024, tsm, s>>>(d, k, ws.partial, ws.ids, ws.w, h.p.dnorm, ws.ghat, ws.vhat,
-                                   ws.p, ws.score, ws.keptbits, ws.kept);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  MR_MARK(3)
-
-  const long long warps = (long long)B * k + (long long)B * (d.N / 64);
-  exact_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(d, B, k, x, h.G, h.V, ws.ids, ws.w,
-                                                           ws.kept, ws.keptbits, ws.p, h.p.b,
-                                                           ws.wa, ws.cpart);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  MR_MARK(4)
-
-  out_kernel<<<(d.H + 15) / 16, 256, 0, s>>>(d, B, k, h.p.Dt, ws.ids, ws.kept, ws.wa, ws.cpart,
-                                              h.p.U, y);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  MR_MARK(5)
-#undef MR_MARK
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(h.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = decode_smem_bytes(d);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((err = cudaLaunchKernelEx(&cfg, decode_kernel, P)) != cudaSuccess) return err;
+  if (ev && (err = cudaEventRecordWithFlags(ev[1], s, rec_flags)) != cudaSuccess) return err;
   return cudaSuccess;
-}
-
-// Dynamic shared memory limits are per kernel, not per handle: only ever raise them.
-template <typename K>
-cudaError_t raise_smem_limit(K kernel, size_t bytes) {
-  cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, kernel);
-  if (err != cudaSuccess) return err;
-  if ((size_t)fa.maxDynamicSharedSizeBytes >= bytes) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
-cudaError_t configure_decode_kernels(const Dims& d) {
-  const int Q = screen_groups(d);
-  const int W = d.I / 8;
-  cudaError_t err = raise_smem_limit(screen_kernel, (size_t)Q * W * 16 * sizeof(float));
-  if (err != cudaSuccess) return err;
-  return raise_smem_limit(topk_kernel, (size_t)d.N * 9);
-}
-
-cudaError_t launch_stats(const moe_reader& h, int B, int k, cudaStream_t s) {
-  const Dims& d = h.d;
-  const Workspace& ws = h.ws;
-  cudaError_t err;
-  (void)k;
-  if ((err = cudaMemsetAsync(ws.bm_codes, 0, (size_t)d.E * d.nb * 4 * 4, s)) != cudaSuccess) return err;
-  if ((err = cudaMemsetAsync(ws.bm_kept, 0, (size_t)d.E * (d.I / 32) * 4, s)) != cudaSuccess) return err;
-  if ((err = cudaMemsetAsync(ws.bm_skip, 0, (size_t)d.E * (d.I / 32) * 4, s)) != cudaSuccess) return err;
-  if ((err = cudaMemsetAsync(ws.bm_expert, 0, (size_t)((d.E + 31) / 32) * 4, s)) != cudaSuccess) return err;
-  if ((err = cudaMemsetAsync(ws.counters, 0, 16 * sizeof(unsigned long long), s)) != cudaSuccess) return err;
-  if (B > 0) {
-    stats_mark_kernel<<<B * d.topk, 128, 0, s>>>(d, B, ws.ids, ws.mask, ws.keptbits, ws.bm_codes,
-                                                 ws.bm_kept, ws.bm_skip, ws.bm_expert);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    stats_count_kernel<<<152, 256, 0, s>>>(d, ws.bm_codes, ws.bm_kept, ws.bm_skip, ws.bm_expert,
-                                           ws.counters);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
-  return cudaSuccess;
-}
-
-cudaError_t launch_gather_kept(const moe_reader& h, int B, int k, int32_t* out_dev, cudaStream_t s) {
-  const long long n = (long long)B * k;
-  if (n == 0) return cudaSuccess;
-  gather_kept_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(h.d, B, k, h.ws.ids, h.ws.kept,
-                                                                out_dev);
-  return cudaGetLastError();
 }
 
 }  // namespace mr

@@ -16,7 +16,7 @@ constexpr int kMaxTopk = 64;
 constexpr int kMaxRank = 64;
 constexpr int kMaxBatch = 1024;
 constexpr int kMaxInter = 8192;
-constexpr int kPhases = 5;           // rotate, screen, topk, exact, out
+constexpr int kPhases = 5;           // kernel, rotate, screen+top-k, exact, output
 constexpr int kProfSlots = 64;       // decode calls recorded between two reads
 
 // Device error word bits (mirror the public MOE_READER_ERR_* values).
@@ -48,7 +48,8 @@ struct Workspace {
   uint32_t* keptbits;   // [Bmax][N/32]   1 = kept
   int32_t* kept;        // [Bmax][N]      kept n = slot*I + i, ascending n (first k used)
   float* wa;            // [Bmax][N]      w * a for kept list entries
-  float* cpart;         // [Bmax][N/64][r] recovery partials per 64-channel chunk
+  int32_t* rowoff;      // [Bmax][N]      e*I + i of kept list entries
+  float* cpart;         // [Bmax][r] recovery vector c = sum_S w_j p_j b_j
   // host-ABI staging
   float* x_stage;       // [Bmax][H]
   float* y_stage;       // [Bmax][H]
@@ -61,6 +62,7 @@ struct Workspace {
   uint32_t* bm_expert;  // [E/32 + 1]
   unsigned long long* counters;  // [16]
   uint32_t* err;        // [1] device error word
+  uint32_t* sync;       // counters and flags of the persistent decode (zero between calls)
 };
 
 struct Prepared {
@@ -86,11 +88,13 @@ struct moe_reader {
   mr::Prepared p;
   mr::Workspace ws;
   uint64_t resident[9];
+  int grid;                 // CTAs of the persistent decode (one per SM)
   // per-phase profiling (events around each decode kernel)
   int prof_on;
   int prof_used;
   int prof_created;
-  cudaEvent_t prof_ev[mr::kProfSlots][mr::kPhases + 1];
+  cudaEvent_t prof_ev[mr::kProfSlots][2];
+  unsigned long long* prof_stamps;      // device [kProfSlots][grid][5]
   // last decode
   int has_decode;
   int last_B, last_k;
@@ -113,11 +117,14 @@ cudaError_t launch_project_b(const Dims& d, const __nv_bfloat16* Dt, const __hal
                              cudaStream_t s);
 
 // ---- decode launchers (decode.cu) ----
-// `ev` (may be null): kPhases + 1 events recorded at the phase boundaries.
+// `ev` (may be null): 2 events recorded around the kernel; `stamps` (may be
+// null): [grid][5] globaltimer stamps of the phase ends.
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
                           const float* w, int k, float* y, cudaStream_t s,
-                          const cudaEvent_t* ev);
+                          const cudaEvent_t* ev, unsigned long long* stamps);
 cudaError_t configure_decode_kernels(const Dims& d);
+int decode_grid(const Dims& d);          // 0 if the decode kernel cannot be co-resident
+size_t sync_words(const Dims& d);        // uint32 words of the synchronisation area
 cudaError_t launch_stats(const moe_reader& h, int B, int k, cudaStream_t s);
 cudaError_t launch_gather_kept(const moe_reader& h, int B, int k, int32_t* out_dev,
                                cudaStream_t s);

@@ -207,10 +207,15 @@ int moe_reader_export(moe_reader_t* h, int32_t which, void* dst, int64_t bytes);
 /* moe_reader_get_info -- derived sizes and resident bytes of a handle. */
 int moe_reader_get_info(moe_reader_t* h, moe_reader_info* out);
 
-/* Per-phase device timing of decode calls (CUDA events recorded around each
- * decode kernel on the decode's stream; also inside a captured CUDA graph).
- * Phases, in order: rotate/select, screen, score + top-k, exact gather +
- * recovery partials, output.                                                */
+/* Device timing of decode calls.  The decode is one persistent kernel; its
+ * time comes from CUDA events recorded around it on the decode's stream (also
+ * inside a captured CUDA graph), and its phases from globaltimer stamps every
+ * CTA writes at the end of each phase.  Phase slots, in order:
+ *   0 the whole kernel (events)
+ *   1 rotation of x and coordinate selection   (to the last CTA's end)
+ *   2 sketch screen, scores and global top-k   (from the end of slot 1)
+ *   3 exact kept channels and recovery vector  (from the end of slot 2)
+ *   4 output                                   (from the end of slot 3)  */
 #define MOE_READER_PHASES 5
 
 /* moe_reader_set_profiling -- enable (1) or disable (0) recording; either

@@ -124,7 +124,8 @@ def test_host_abi_matches_device(pair):
     x, ids, w = pair.tokens(3, 21)
     y_dev = pair.decode_gpu(x, ids, w, K)
     y_host = pair.reader.decode_host(x, ids, w, K)
-    assert np.array_equal(y_dev, y_host)
+    # the recovery vector is summed with fp32 atomics: equal up to summation order
+    assert np.abs(y_dev - y_host).max() <= 1e-6 * np.abs(y_dev).max()
 
 
 def test_empty_batch_and_argument_errors(pair):
