@@ -127,7 +127,7 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   o.total = o.flag + d.Bmax;
   return o;
 }
-constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2;
+constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2, kSyncNext = 3;
 
 // ------------------------------- phase 0 -----------------------------------
 __device__ void rotate_item(const Params& P, int t, int b, int lane) {
@@ -279,78 +279,159 @@ __device__ uint32_t cta_radix_select(int N, int kth, KeyFn keyfn, int* hist, int
   return prefix;
 }
 
+constexpr int kDigitBits = 12;               // first histogram: key bits 30..19
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kCandMax = 1024;               // candidates ranked exactly; more -> radix
+
+__device__ __forceinline__ int key_digit(uint32_t key) { return (int)((key >> 19) & (kBins - 1)); }
+
+// Shared-memory layout of the top-k step (offsets in bytes from smem).
+__host__ __device__ inline size_t topk_smem_bytes(int N) {
+  return (size_t)4 * N                       // keys
+         + (size_t)(kWarps + 1) * 256 * 4    // histogram (4096 bins, or the radix rows)
+         + (size_t)N                         // keep flags
+         + (size_t)kCandMax * 12             // candidate keys, ids, ranks
+         + 512;                              // scalars, warp sums, expert ids
+}
+
 __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   const Dims& d = P.d;
   const int N = d.N, k = P.k, I = d.I;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);              // [N]
-  int* hist = reinterpret_cast<int*>(keys + N);                     // [kWarps + 1][256]
-  int* sh = hist + (kWarps + 1) * 256;                              // [4]
-  int* wsum = sh + 4;                                               // [kWarps]
-  int* eid = wsum + kWarps;                                         // [topk]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                      // [N]
+  int* hist = reinterpret_cast<int*>(keys + N);                             // [(kWarps+1)*256]
+  uint8_t* keep = reinterpret_cast<uint8_t*>(hist + (kWarps + 1) * 256);    // [N]
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(keep + ((N + 15) & ~15));    // [kCandMax]
+  uint32_t* cgid = ckey + kCandMax;                                         // [kCandMax]
+  int* crank = reinterpret_cast<int*>(cgid + kCandMax);                     // [kCandMax]
+  int* sh = crank + kCandMax;                                               // [8]
+  int* wsum = sh + 8;                                                       // [kWarps]
+  int* eid = wsum + kWarps;                                                 // [topk]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int s = threadIdx.x; s < d.topk; s += kThreads) eid[s] = __ldcg(P.ids_ws + t * d.topk + s);
   for (int n = threadIdx.x; n < N; n += kThreads)
     keys[n] = __float_as_uint(__ldcg(P.score + (size_t)t * N + n));
+  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+  if (threadIdx.x == 0) sh[2] = 0;
   __syncthreads();
 
   const bool all = k >= N, none = k <= 0;
-  uint32_t T = 0, T2 = 0;
-  if (!all && !none) {
-    int need = 0;
-    T = cta_radix_select(
-        N, k, [&](int n, uint32_t& key) { key = keys[n]; return true; }, hist, sh, &need);
-    int eq = 0;
-    for (int n = threadIdx.x; n < N; n += kThreads) eq += keys[n] == T;
-    eq = warp_sum_i(eq);
-    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = eq;
+  if (all || none) {
+    for (int n = threadIdx.x; n < N; n += kThreads) keep[n] = all;
+  } else {
+    // 1. histogram of the 12-bit digit (keys spread over hundreds of bins)
+    for (int n = threadIdx.x; n < N; n += kThreads) atomicAdd(&hist[key_digit(keys[n])], 1);
     __syncthreads();
-    int eq_total = 0;
-    for (int w = 0; w < kWarps; ++w) eq_total += wsum[w];
-    __syncthreads();
-    if (need < eq_total) {
-      int dummy = 0;
-      T2 = cta_radix_select(
-          N, need,
-          [&](int n, uint32_t& key) {
-            if (keys[n] != T) return false;
-            key = 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I);
-            return true;
-          },
-          hist, sh, &dummy);
-    }
-  }
-  auto kept_fn = [&](int n) -> bool {
-    if (all) return true;
-    if (none) return false;
-    const uint32_t a = keys[n];
-    if (a != T) return a > T;
-    return (0xffffffffu - (uint32_t)(eid[n / I] * I + n % I)) >= T2;
-  };
-  // ascending compaction of kept n, and the kept bitmap
-  const int per = (N + kThreads - 1) / kThreads;
-  const int n0 = threadIdx.x * per, n1 = min(N, n0 + per);
-  int cnt = 0;
-  for (int n = n0; n < n1; ++n) cnt += kept_fn(n);
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int incl = cnt;
+    // 2. the digit D holding the k-th largest key: 8 digits per thread, from the top
+    constexpr int kPer = kBins / kThreads;
+    int cnt[kPer], tot = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) wsum[wid] = incl;
-  __syncthreads();
-  int base = 0;
-  for (int w = 0; w < wid; ++w) base += wsum[w];
-  int pos = base + incl - cnt;
-  for (int n = n0; n < n1; ++n)
-    if (kept_fn(n)) {
-      if (pos < N) P.kept[(size_t)t * N + pos] = n;
-      ++pos;
+    for (int u = 0; u < kPer; ++u) {
+      cnt[u] = hist[kBins - 1 - (threadIdx.x * kPer + u)];
+      tot += cnt[u];
     }
-  for (int wd = threadIdx.x; wd < N / 32; wd += kThreads) {
-    uint32_t bits = 0;
-    for (int u = 0; u < 32; ++u) bits |= (uint32_t)kept_fn(wd * 32 + u) << u;
-    P.keptbits[(size_t)t * (N / 32) + wd] = bits;
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    int before = incl - tot;
+    for (int w = 0; w < wid; ++w) before += wsum[w];
+    if (before < k && before + tot >= k) {
+      int above = before;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        if (above + cnt[u] >= k) {
+          sh[0] = kBins - 1 - (threadIdx.x * kPer + u);
+          sh[1] = k - above;       // keys of digit D that are kept
+          sh[3] = cnt[u];          // keys of digit D
+          break;
+        }
+        above += cnt[u];
+      }
+    }
+    __syncthreads();
+    const int D = sh[0], need = sh[1], m = sh[3];
+    if (m <= kCandMax) {
+      // 3. the candidates (digit D) ranked exactly: larger key, then lower global id
+      for (int n = threadIdx.x; n < N; n += kThreads) {
+        const int dg = key_digit(keys[n]);
+        keep[n] = dg > D;
+        if (dg == D) {
+          const int c = atomicAdd(&sh[2], 1);
+          ckey[c] = keys[n] | 0u;
+          cgid[c] = (uint32_t)(eid[n / I] * I + n % I);
+          crank[c] = n;             // the channel for now; the rank below
+        }
+      }
+      __syncthreads();
+      // every (ci, cj) pair once, spread over the threads
+      const int pairs = m * m;
+      int* rk = hist;               // reuse: rank counters [m]
+      for (int c = threadIdx.x; c < m; c += kThreads) rk[c] = 0;
+      __syncthreads();
+      for (int q = threadIdx.x; q < pairs; q += kThreads) {
+        const int ci = q / m, cj = q - ci * m;
+        const uint32_t ki = ckey[ci], kj = ckey[cj];
+        if (kj > ki || (kj == ki && cgid[cj] < cgid[ci])) atomicAdd(&rk[ci], 1);
+      }
+      __syncthreads();
+      for (int c = threadIdx.x; c < m; c += kThreads) keep[crank[c]] = rk[c] < need;
+    } else {
+      // degenerate spread (too many keys in one digit): full radix select
+      int need2 = 0;
+      const uint32_t T = cta_radix_select(
+          N, k, [&](int n, uint32_t& key) { key = keys[n]; return true; }, hist, sh + 4, &need2);
+      int eq = 0;
+      for (int n = threadIdx.x; n < N; n += kThreads) eq += keys[n] == T;
+      eq = warp_sum_i(eq);
+      if (lane == 0) wsum[wid] = eq;
+      __syncthreads();
+      int eq_total = 0;
+      for (int w = 0; w < kWarps; ++w) eq_total += wsum[w];
+      __syncthreads();
+      uint32_t T2 = 0;
+      if (need2 < eq_total) {
+        int dummy = 0;
+        T2 = cta_radix_select(
+            N, need2,
+            [&](int n, uint32_t& key) {
+              if (keys[n] != T) return false;
+              key = 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I);
+              return true;
+            },
+            hist, sh + 4, &dummy);
+      }
+      for (int n = threadIdx.x; n < N; n += kThreads) {
+        const uint32_t a = keys[n];
+        keep[n] = a > T || (a == T && 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I) >= T2);
+      }
+    }
+  }
+  __syncthreads();
+  // 4. compaction in ascending n and the kept bitmap: warp w owns a contiguous
+  //    range of whole 32-channel words; one ballot per word
+  const int words = N / 32;
+  const int wper = (words + kWarps - 1) / kWarps;
+  const int w0 = wid * wper, w1 = min(words, w0 + wper);
+  int mine = 0;
+  for (int wd = w0; wd < w1; ++wd) mine += __popc(__ballot_sync(0xffffffffu, keep[wd * 32 + lane]));
+  if (lane == 0) wsum[wid] = mine;
+  __syncthreads();
+  int pos = 0;
+  for (int w = 0; w < wid; ++w) pos += wsum[w];
+  const uint32_t below = (1u << lane) - 1u;
+  for (int wd = w0; wd < w1; ++wd) {
+    const int n = wd * 32 + lane;
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep[n]);
+    if (keep[n]) {
+      const int at = pos + __popc(bal & below);
+      if (at < N) P.kept[(size_t)t * N + at] = n;
+    }
+    if (lane == 0) P.keptbits[(size_t)t * words + wd] = bal;
+    pos += __popc(bal);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -360,45 +441,79 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
 }
 
 // ------------------------------- phase 1 -----------------------------------
-// false: the CTA must stop (timeout / abort)
-__device__ bool screen_unit(const Params& P, int t, int slot, int b, unsigned char* smem) {
+// A screen unit runs on UT threads of the CTA: the whole CTA (UT = 512) when
+// there are fewer units than CTAs, otherwise each half of the CTA (UT = 256)
+// runs its own unit, synchronised by a named barrier, so two units' memory
+// round trips overlap on every SM.
+struct UnitCtx {
+  int ut;              // thread index within the unit
+  int UT;              // threads of the unit
+  int bar;             // named barrier id (0 = __syncthreads)
+  unsigned char* sm;   // this unit's shared memory
+};
+
+__device__ __forceinline__ void unit_sync(const UnitCtx& c) {
+  if (c.UT == kThreads)
+    __syncthreads();
+  else
+    asm volatile("bar.sync %0, %1;" ::"r"(c.bar), "r"(c.UT) : "memory");
+}
+
+__host__ __device__ inline int unit_groups(int W8, int UT) {
+  int Q = UT / W8;
+  if (Q > kMaxGroups) Q = kMaxGroups;
+  return Q < 1 ? 1 : Q;
+}
+
+__host__ __device__ inline size_t unit_smem_bytes(int I, int Q) {
+  const int Wp = (I / 16) | 1;
+  return (size_t)4 * I + kBlock * 8 + 16 + (size_t)Q * 32 * Wp * 4;
+}
+
+// One (token, slot, block) unit: alpha-scaled block partials of ghat/vhat.
+// false: the CTA must stop (timeout / abort).
+__device__ bool screen_unit(const Params& P, int t, int slot, int b, const UnitCtx& cx) {
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int ts = t * d.topk + slot;
   int e = P.ids_in[ts];
   if (e < 0 || e >= d.E) e = 0;
   const int I = d.I;
-  // shared memory: alpha [2I] half, clist [128] int, rlist [128] float, flags [4], red [Q][2I]
-  __half* alpha = reinterpret_cast<__half*>(smem);
-  int* clist = reinterpret_cast<int*>(smem + 4 * (size_t)I);
+  // shared memory: alpha [2I] half, clist [128] int, rlist [128] float, flags [4], red [Q][32][Wp]
+  __half* alpha = reinterpret_cast<__half*>(cx.sm);
+  int* clist = reinterpret_cast<int*>(cx.sm + 4 * (size_t)I);
   float* rlist = reinterpret_cast<float*>(clist + kBlock);
   int* flags = reinterpret_cast<int*>(rlist + kBlock);
   float* red = reinterpret_cast<float*>(flags + 4);
 
+  // alpha, the mask words and the rotation flag are requested together
   const __half* sc = P.scales + ((size_t)e * d.nb + b) * 2 * I;
-  for (int i = threadIdx.x; i < I / 4; i += kThreads)
+  for (int i = cx.ut; i < I / 4; i += cx.UT)
     reinterpret_cast<uint4*>(alpha)[i] = ldg_nc4(reinterpret_cast<const uint4*>(sc) + i);
-  if (threadIdx.x == 0)
+  if (cx.ut == 0)
     flags[0] = wait_at_least(P.sync + so.rot + t * d.nb + b, 1u, P.sync + kSyncAbort, P.err);
-  __syncthreads();
+  unit_sync(cx);
   if (!flags[0]) return false;
-  if (threadIdx.x < kBlock) {
-    const int c = threadIdx.x;
+  if (cx.ut < kBlock) {
+    const int c = cx.ut;
     const uint32_t* mk = P.mask + ((size_t)t * d.nb + b) * 4;
-    const uint32_t word = __ldcg(mk + (c >> 5));
+    const uint4 mw = __ldcg(reinterpret_cast<const uint4*>(mk));
+    const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
+    const uint32_t word = words[c >> 5];
     if ((word >> (c & 31)) & 1u) {
       int pos = __popc(word & ((1u << (c & 31)) - 1u));
-      for (int w2 = 0; w2 < (c >> 5); ++w2) pos += __popc(__ldcg(mk + w2));
+#pragma unroll
+      for (int w2 = 0; w2 < 3; ++w2) pos += w2 < (c >> 5) ? __popc(words[w2]) : 0;
       if (pos < kBlock) {
         clist[pos] = c;
         rlist[pos] = 0.5f * __ldcg(P.rx + (size_t)t * d.Hp + b * kBlock + c);
       }
     }
   }
-  __syncthreads();
+  unit_sync(cx);
 
-  const int W8 = P.W8, Q = P.Q;
-  const int j = threadIdx.x % W8, q = threadIdx.x / W8;
+  const int W8 = P.W8, Q = unit_groups(W8, cx.UT), Wp = W8 | 1;
+  const int j = cx.ut % W8, q = cx.ut / W8;
   const int half = I / 32;                          // 8-byte words per run
   if (q < Q) {
     float acc[32];
@@ -433,45 +548,56 @@ __device__ bool screen_unit(const Params& P, int t, int slot, int b, unsigned ch
         }
       }
     }
-    // code-major layout [q][kk][j]: consecutive threads (j) hit consecutive banks
+    // layout [q][kk][j] with an odd row stride Wp: the stores (consecutive j) and
+    // the loads below (consecutive kk) both fall in distinct banks
 #pragma unroll
-    for (int u = 0; u < 32; ++u) red[(size_t)q * 2 * I + u * W8 + j] = acc[u];
+    for (int u = 0; u < 32; ++u) red[(size_t)q * 32 * Wp + u * Wp + j] = acc[u];
   }
-  __syncthreads();
+  unit_sync(cx);
   float* out = P.partial + ((size_t)ts * d.nb + b) * 2 * I;
-  for (int o = threadIdx.x; o < 2 * I; o += kThreads) {
+  for (int o = cx.ut; o < 2 * I; o += cx.UT) {
     const int jj = o / 32, kk = o % 32;
     float s = 0.f;
-    for (int qq = 0; qq < Q; ++qq) s += red[(size_t)qq * 2 * I + kk * W8 + jj];
+    for (int qq = 0; qq < Q; ++qq) s += red[(size_t)qq * 32 * Wp + kk * Wp + jj];
     const int gv = jj / half;
     const int i = (jj % half) * 32 + kk;
     out[gv * I + i] = s * __half2float(alpha[gv * I + i]);
   }
-  // publish: the barrier orders the CTA's stores before thread 0's fence + atomic
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  // publish: the barrier orders the unit's stores before the leader's fence + add
+  unit_sync(cx);
+  if (cx.ut == 0) {
     __threadfence();
-    flags[1] = atomicAdd(P.sync + so.slot + ts, 1u) == (uint32_t)(d.nb - 1);
-    if (flags[1]) __threadfence();
+    atomicAdd(P.sync + so.slot + ts, 1u);
   }
-  __syncthreads();
-  if (!flags[1]) return true;
+  return true;
+}
 
-  // the last block of this (token, slot): score its channels
+// Score the channels of one (token, slot) once all its blocks are in: sum
+// the block partials in block order, s = w ||d|| |phi(ghat) vhat|.
+__device__ bool score_task(const Params& P, int ts, int* flag) {
+  const Dims& d = P.d;
+  const SyncOff so = sync_offsets(d);
+  const int t = ts / d.topk, slot = ts % d.topk, I = d.I;
+  if (threadIdx.x == 0)
+    *flag = wait_at_least(P.sync + so.slot + ts, (uint32_t)d.nb, P.sync + kSyncAbort, P.err);
+  __syncthreads();
+  if (!*flag) return false;
+  int e = P.ids_in[ts];
+  if (e < 0 || e >= d.E) e = 0;
   const float wv = P.w_in[ts];
   for (int i = threadIdx.x; i < I; i += kThreads) {
     const float* pg = P.partial + ((size_t)ts * d.nb) * 2 * I + i;
     float g = 0.f, v = 0.f;
     int bb = 0;
-    for (; bb + 8 <= d.nb; bb += 8) {   // loads first, then the sums in block order
-      float gg[8], vv[8];
+    for (; bb + 16 <= d.nb; bb += 16) {   // loads first, then the sums in block order
+      float gg[16], vv[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         gg[u] = __ldcg(pg + (size_t)(bb + u) * 2 * I);
         vv[u] = __ldcg(pg + (size_t)(bb + u) * 2 * I + I);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         g += gg[u];
         v += vv[u];
       }
@@ -491,13 +617,8 @@ __device__ bool screen_unit(const Params& P, int t, int slot, int b, unsigned ch
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    flags[2] = atomicAdd(P.sync + so.tok + t, 1u) == (uint32_t)(d.topk - 1);
-    if (flags[2]) __threadfence();
+    atomicAdd(P.sync + so.tok + t, 1u);
   }
-  __syncthreads();
-  if (!flags[2]) return true;
-  topk_token(P, t, smem);
-  __syncthreads();
   return true;
 }
 
@@ -626,9 +747,17 @@ constexpr int kTokGroup = 4;
 
 __device__ void out_slice(const Params& P, int s, unsigned char* smem) {
   const Dims& d = P.d;
-  float* wred = reinterpret_cast<float*>(smem);       // [kTokGroup][kWarps][16]
+  float* wred = reinterpret_cast<float*>(smem);        // [kTokGroup][kWarps][16]
+  float* us = wred + kTokGroup * kWarps * 16;          // [16][r]  U rows of the slice
+  float* cs = us + 16 * kMaxRank;                      // [kTokGroup][r] recovery vectors
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int h0 = s * 16;
+  const bool recover = P.k < d.N;
+  if (recover)
+    for (int q = threadIdx.x; q < 16 * d.r; q += kThreads) {
+      const int h = h0 + q / d.r;
+      us[q] = h < d.H ? __half2float(P.U[(size_t)h * d.r + q % d.r]) : 0.f;
+    }
   const int rg = threadIdx.x >> 1, hf = threadIdx.x & 1;   // 256 row groups x 2 halves
   const int hh = h0 + hf * 8;
   for (int t0 = 0; t0 < P.B; t0 += kTokGroup) {
@@ -637,6 +766,11 @@ __device__ void out_slice(const Params& P, int s, unsigned char* smem) {
     for (int tt = 0; tt < kTokGroup; ++tt)
 #pragma unroll
       for (int u = 0; u < 8; ++u) acc[tt][u] = 0.f;
+    if (recover)
+      for (int q = threadIdx.x; q < kTokGroup * d.r; q += kThreads) {
+        const int t = t0 + q / d.r;
+        cs[q] = t < P.B ? __ldcg(P.cvec + (size_t)t * d.r + q % d.r) : 0.f;
+      }
     if (hh < d.H) {
       for (int q = rg; q < P.k; q += 256) {
         int32_t r[kTokGroup];
@@ -674,10 +808,8 @@ __device__ void out_slice(const Params& P, int s, unsigned char* smem) {
       if (t < P.B && h < d.H) {
         float sum = 0.f;
         for (int w = 0; w < kWarps; ++w) sum += wred[(tt * kWarps + w) * 16 + col];
-        if (P.k < d.N)
-          for (int jj = 0; jj < d.r; ++jj)
-            sum = fmaf(__half2float(P.U[(size_t)h * d.r + jj]),
-                       __ldcg(P.cvec + (size_t)t * d.r + jj), sum);
+        if (recover)
+          for (int jj = 0; jj < d.r; ++jj) sum = fmaf(us[col * d.r + jj], cs[tt * d.r + jj], sum);
         P.y[(size_t)t * d.H + h] = sum;
       }
     }
@@ -689,6 +821,7 @@ __device__ void out_slice(const Params& P, int s, unsigned char* smem) {
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int ctl[2];
+  if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -707,12 +840,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     __syncthreads();
     if (threadIdx.x == 0) stamp[1] = globaltimer();
   }
-  // phase 1: screen units (token, slot, block)
+  // phase 1a: screen units (token, slot, block) from a shared queue
   {
     const int units = P.B * d.topk * d.nb;
-    for (int u = blockIdx.x; u < units; u += nctas) {
+    const bool halves = units > nctas;
+    const int UT = halves ? kThreads / 2 : kThreads;
+    const int hid = halves ? (int)(threadIdx.x / UT) : 0;
+    UnitCtx cx;
+    cx.ut = threadIdx.x - hid * UT;
+    cx.UT = UT;
+    cx.bar = 1 + hid;
+    cx.sm = smem + (size_t)hid * unit_smem_bytes(d.I, unit_groups(P.W8, UT));
+    int* next = reinterpret_cast<int*>(cx.sm + 4 * (size_t)d.I + kBlock * 8);   // flags[0..3]
+    if (cx.ut == 0) next[1] = (int)atomicAdd(P.sync + kSyncNext, 1u);
+    unit_sync(cx);
+    int u = next[1];
+    bool ok = true;
+    while (u < units) {
+      // take the following unit now so the round trip overlaps this one
+      if (cx.ut == 0) next[2] = (int)atomicAdd(P.sync + kSyncNext, 1u);
       const int b = u % d.nb, ts = u / d.nb;
-      if (!screen_unit(P, ts / d.topk, ts % d.topk, b, smem)) return;
+      if (!screen_unit(P, ts / d.topk, ts % d.topk, b, cx)) {
+        ok = false;
+        break;
+      }
+      unit_sync(cx);
+      u = next[2];
+      unit_sync(cx);
+    }
+    if (!ok) ctl[0] = 1;
+    __syncthreads();
+    if (ctl[0] == 1) return;
+  }
+  // phase 1b: scoring tasks, then 1c: top-k tasks, spread over the CTAs
+  {
+    int* flag = reinterpret_cast<int*>(smem);
+    for (int ts = blockIdx.x; ts < P.B * d.topk; ts += nctas) {
+      if (!score_task(P, ts, flag)) return;
+      __syncthreads();
+    }
+    for (int t = blockIdx.x; t < P.B; t += nctas) {
+      if (threadIdx.x == 0)
+        ctl[1] = wait_at_least(P.sync + so.tok + t, (uint32_t)d.topk, abort_flag, P.err);
+      __syncthreads();
+      if (!ctl[1]) return;
+      topk_token(P, t, smem);
       __syncthreads();
     }
   }
@@ -781,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     }
     if (threadIdx.x == 0) {
       P.sync[kSyncExact] = 0u;
+      P.sync[kSyncNext] = 0u;
       P.sync[kSyncDone] = 0u;
     }
   }
@@ -795,11 +968,11 @@ int screen_groups(const Dims& d) {
 }
 
 size_t decode_smem_bytes(const Dims& d) {
-  const int Q = screen_groups(d);
-  const size_t screen = (size_t)4 * d.I + kBlock * 8 + 16 + (size_t)Q * 2 * d.I * 4;
-  const size_t topk = (size_t)4 * d.N + (size_t)(kWarps + 1) * 256 * 4 + 16 + kWarps * 4 +
-                      kMaxTopk * 4;
-  const size_t out = (size_t)kTokGroup * kWarps * 16 * 4;
+  const size_t whole = unit_smem_bytes(d.I, unit_groups(d.I / 16, kThreads));
+  const size_t halves = 2 * unit_smem_bytes(d.I, unit_groups(d.I / 16, kThreads / 2));
+  const size_t screen = whole > halves ? whole : halves;
+  const size_t topk = topk_smem_bytes(d.N);
+  const size_t out = ((size_t)kTokGroup * kWarps * 16 + 16 * kMaxRank + kTokGroup * kMaxRank) * 4;
   const size_t m = screen > topk ? screen : topk;
   return m > out ? m : out;
 }
