@@ -630,27 +630,38 @@ __device__ __forceinline__ void dot8(const uint4& q, const float4& xa, const flo
   s = fmaf(bf16_lo(q.w), xb.z, s); s = fmaf(bf16_hi(q.w), xb.w, s);
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
 __device__ void kept_item(const Params& P, int t, int qi, int lane) {
   const Dims& d = P.d;
   const int n = __ldcg(P.kept + (size_t)t * d.N + qi);
   const int slot = n / d.I, i = n % d.I;
   const int e = __ldcg(P.ids_ws + t * d.topk + slot);
   const size_t row = (size_t)e * d.I + i;
+  // the output phase reads this channel's transposed down row in 32-byte
+  // pieces from many CTAs: bring the whole row into L2 now
+  {
+    const char* dt = reinterpret_cast<const char*>(P.Dt + row * d.H);
+    for (int off = lane * 128; off < d.H * 2; off += 32 * 128) prefetch_l2(dt + off);
+  }
   const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
   const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
   const float4* x4 = reinterpret_cast<const float4*>(P.x + (size_t)t * d.H);
   float sg = 0.f, sv = 0.f;
   const int n8 = d.H / 8;
   int h8 = lane;
-  for (; h8 + 96 < n8; h8 += 128) {
-    uint4 gq[4], vq[4];
+  constexpr int kU = 8;   // 16-byte loads per lane and row issued together
+  for (; h8 + 32 * (kU - 1) < n8; h8 += 32 * kU) {
+    uint4 gq[kU], vq[kU];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kU; ++u) {
       gq[u] = ldg_nc4(g4 + h8 + 32 * u);
       vq[u] = ldg_nc4(v4 + h8 + 32 * u);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kU; ++u) {
       const float4 xa = __ldg(x4 + 2 * (h8 + 32 * u)), xb = __ldg(x4 + 2 * (h8 + 32 * u) + 1);
       dot8(gq[u], xa, xb, sg);
       dot8(vq[u], xa, xb, sv);
@@ -743,9 +754,13 @@ __device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
   acc[6] = fmaf(c, bf16_lo(v.w), acc[6]); acc[7] = fmaf(c, bf16_hi(v.w), acc[7]);
 }
 
-constexpr int kTokGroup = 4;
+constexpr int kTokGroup = 2;
+constexpr int kRowBatch = 4;   // rows per token and thread whose loads are issued together
 
-__device__ void out_slice(const Params& P, int s, unsigned char* smem) {
+// One output item: 16 columns h0..h0+15 (one 32-byte piece of every kept
+// transposed down row) for tokens t0, t0+1.  Thread (rg, half): rows
+// rg, rg+256, ...; 8 columns each.  y = sum_K (w a)_j Dt_j + U c.
+__device__ void out_item(const Params& P, int s, int t0, unsigned char* smem) {
   const Dims& d = P.d;
   float* wred = reinterpret_cast<float*>(smem);        // [kTokGroup][kWarps][16]
   float* us = wred + kTokGroup * kWarps * 16;          // [16][r]  U rows of the slice
@@ -753,68 +768,74 @@ __device__ void out_slice(const Params& P, int s, unsigned char* smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int h0 = s * 16;
   const bool recover = P.k < d.N;
-  if (recover)
+  if (recover) {
     for (int q = threadIdx.x; q < 16 * d.r; q += kThreads) {
       const int h = h0 + q / d.r;
       us[q] = h < d.H ? __half2float(P.U[(size_t)h * d.r + q % d.r]) : 0.f;
     }
+    for (int q = threadIdx.x; q < kTokGroup * d.r; q += kThreads) {
+      const int t = t0 + q / d.r;
+      cs[q] = t < P.B ? __ldcg(P.cvec + (size_t)t * d.r + q % d.r) : 0.f;
+    }
+  }
   const int rg = threadIdx.x >> 1, hf = threadIdx.x & 1;   // 256 row groups x 2 halves
   const int hh = h0 + hf * 8;
-  for (int t0 = 0; t0 < P.B; t0 += kTokGroup) {
-    float acc[kTokGroup][8];
+  float acc[kTokGroup][8];
 #pragma unroll
-    for (int tt = 0; tt < kTokGroup; ++tt)
+  for (int tt = 0; tt < kTokGroup; ++tt)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc[tt][u] = 0.f;
-    if (recover)
-      for (int q = threadIdx.x; q < kTokGroup * d.r; q += kThreads) {
-        const int t = t0 + q / d.r;
-        cs[q] = t < P.B ? __ldcg(P.cvec + (size_t)t * d.r + q % d.r) : 0.f;
-      }
-    if (hh < d.H) {
-      for (int q = rg; q < P.k; q += 256) {
-        int32_t r[kTokGroup];
-        float c[kTokGroup];
-        uint4 v[kTokGroup];
-#pragma unroll
-        for (int tt = 0; tt < kTokGroup; ++tt) {
-          const int t = t0 + tt;
-          r[tt] = t < P.B ? __ldcg(P.rowoff + (size_t)t * d.N + q) : 0;
-          c[tt] = t < P.B ? __ldcg(P.wa + (size_t)t * d.N + q) : 0.f;
-        }
-#pragma unroll
-        for (int tt = 0; tt < kTokGroup; ++tt)
-          v[tt] = t0 + tt < P.B ? ldg_nc4(P.Dt + (size_t)r[tt] * d.H + hh) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int tt = 0; tt < kTokGroup; ++tt) axpy8(c[tt], v[tt], acc[tt]);
-      }
-    }
-    // sum the 16 row groups of the warp (lane bits 1..4), then the 16 warps
-#pragma unroll
-    for (int tt = 0; tt < kTokGroup; ++tt)
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int o = 2; o < 32; o <<= 1) acc[tt][u] += __shfl_xor_sync(0xffffffffu, acc[tt][u], o);
-    if (lane < 2)
+    for (int u = 0; u < 8; ++u) acc[tt][u] = 0.f;
+  if (hh < d.H) {
+    for (int q0 = rg; q0 < P.k; q0 += 256 * kRowBatch) {
+      int32_t r[kTokGroup][kRowBatch];
+      float c[kTokGroup][kRowBatch];
 #pragma unroll
       for (int tt = 0; tt < kTokGroup; ++tt)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) wred[(tt * kWarps + warp) * 16 + lane * 8 + u] = acc[tt][u];
-    __syncthreads();
-    if (threadIdx.x < 16 * kTokGroup) {
-      const int tt = threadIdx.x >> 4, col = threadIdx.x & 15;
-      const int t = t0 + tt, h = h0 + col;
-      if (t < P.B && h < d.H) {
-        float sum = 0.f;
-        for (int w = 0; w < kWarps; ++w) sum += wred[(tt * kWarps + w) * 16 + col];
-        if (recover)
-          for (int jj = 0; jj < d.r; ++jj) sum = fmaf(us[col * d.r + jj], cs[tt * d.r + jj], sum);
-        P.y[(size_t)t * d.H + h] = sum;
-      }
+        for (int u = 0; u < kRowBatch; ++u) {
+          const int q = q0 + 256 * u;
+          const bool ok = t0 + tt < P.B && q < P.k;
+          r[tt][u] = ok ? __ldcg(P.rowoff + (size_t)(t0 + tt) * d.N + q) : -1;
+          c[tt][u] = ok ? __ldcg(P.wa + (size_t)(t0 + tt) * d.N + q) : 0.f;
+        }
+      uint4 v[kTokGroup][kRowBatch];
+#pragma unroll
+      for (int tt = 0; tt < kTokGroup; ++tt)
+#pragma unroll
+        for (int u = 0; u < kRowBatch; ++u)
+          v[tt][u] = r[tt][u] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(P.Dt + (size_t)r[tt][u] * d.H + hh))
+                                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int tt = 0; tt < kTokGroup; ++tt)
+#pragma unroll
+        for (int u = 0; u < kRowBatch; ++u) axpy8(c[tt][u], v[tt][u], acc[tt]);
     }
-    __syncthreads();
   }
+  // sum the 16 row groups of the warp (lane bits 1..4), then the 16 warps
+#pragma unroll
+  for (int tt = 0; tt < kTokGroup; ++tt)
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) acc[tt][u] += __shfl_xor_sync(0xffffffffu, acc[tt][u], o);
+  if (lane < 2)
+#pragma unroll
+    for (int tt = 0; tt < kTokGroup; ++tt)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) wred[(tt * kWarps + warp) * 16 + lane * 8 + u] = acc[tt][u];
+  __syncthreads();
+  if (threadIdx.x < 16 * kTokGroup) {
+    const int tt = threadIdx.x >> 4, col = threadIdx.x & 15;
+    const int t = t0 + tt, h = h0 + col;
+    if (t < P.B && h < d.H) {
+      float sum = 0.f;
+      for (int w = 0; w < kWarps; ++w) sum += wred[(tt * kWarps + w) * 16 + col];
+      if (recover)
+        for (int jj = 0; jj < d.r; ++jj) sum = fmaf(us[col * d.r + jj], cs[tt * d.r + jj], sum);
+      P.y[(size_t)t * d.H + h] = sum;
+    }
+  }
+  __syncthreads();
 }
 
 // ------------------------------- the kernel --------------------------------
@@ -931,10 +952,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   }
   __syncthreads();
   if (!ctl[1]) return;
-  // phase 3: output slices
+  // phase 3: output items (16-column slice, token pair)
   {
     const int slices = (d.H + 15) / 16;
-    for (int s = blockIdx.x; s < slices; s += nctas) out_slice(P, s, smem);
+    const int groups = (P.B + kTokGroup - 1) / kTokGroup;
+    for (int it = blockIdx.x; it < slices * groups; it += nctas)
+      out_item(P, it % slices, (it / slices) * kTokGroup, smem);
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
   // the last CTA out resets the synchronisation area for the next call
