@@ -67,9 +67,9 @@ struct Allocs {
 void free_handle_memory(moe_reader* h) {
   if (!h) return;
   if (h->p.codes) cudaFree(h->p.codes);   // start of the prepared block
-  if (h->ws.rx) cudaFree(h->ws.rx);       // start of the workspace block
+  if (h->ws.rsel) cudaFree(h->ws.rsel);   // start of the workspace block
   h->p.codes = nullptr;
-  h->ws.rx = nullptr;
+  h->ws.rsel = nullptr;
 }
 
 int cuda_status(cudaError_t e) {
@@ -195,6 +195,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t o_dnorm = pa.take((size_t)d.E * d.I * 4);
   const size_t o_dt = pa.take((size_t)d.E * d.I * d.H * 2);
   const size_t o_u = pa.take((size_t)d.H * d.r * 2);
+  const size_t o_ut = pa.take((size_t)d.H * d.r * 2);
   const size_t o_b = pa.take((size_t)d.E * d.I * d.r * 2);
   const size_t o_sigma = pa.take((size_t)d.Hp);
   const size_t o_eig = pa.take((size_t)d.r * 8);
@@ -211,6 +212,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->p.dnorm = reinterpret_cast<float*>(pb + o_dnorm);
   h->p.Dt = reinterpret_cast<__nv_bfloat16*>(pb + o_dt);
   h->p.U = reinterpret_cast<__half*>(pb + o_u);
+  h->p.Ut = reinterpret_cast<__half*>(pb + o_ut);
   h->p.b = reinterpret_cast<__half*>(pb + o_b);
   h->p.sigma = reinterpret_cast<int8_t*>(pb + o_sigma);
   h->p.eigvals = reinterpret_cast<double*>(pb + o_eig);
@@ -226,7 +228,8 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   // ---- decode workspace ----
   const size_t Bm = (size_t)d.Bmax;
   Arena wa;
-  const size_t w_rx = wa.take(Bm * d.Hp * 4);
+  const size_t w_rsel = wa.take(Bm * d.Hp * 4);
+  const size_t w_clist = wa.take(Bm * d.Hp);
   const size_t w_mask = wa.take(Bm * d.nb * 16);
   const size_t w_ids = wa.take(Bm * d.topk * 4);
   const size_t w_w = wa.take(Bm * d.topk * 4);
@@ -241,6 +244,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_ro = wa.take(Bm * d.N * 4);
   const size_t w_sync = wa.take(mr::sync_words(d) * 4);
   const size_t w_cp = wa.take(Bm * d.r * 4);
+  const size_t w_yp = wa.take(Bm * (size_t)((d.H + 255) / 256) * 32 * 256 * 4);
   const size_t w_xs = wa.take(Bm * d.H * 4);
   const size_t w_ys = wa.take(Bm * d.H * 4);
   const size_t w_is = wa.take(Bm * d.topk * 4);
@@ -259,7 +263,8 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
     return MOE_READER_ENOMEM;
   }
   char* wb = static_cast<char*>(wbase);
-  h->ws.rx = reinterpret_cast<float*>(wb + w_rx);
+  h->ws.rsel = reinterpret_cast<float*>(wb + w_rsel);
+  h->ws.clist = reinterpret_cast<uint8_t*>(wb + w_clist);
   h->ws.mask = reinterpret_cast<uint32_t*>(wb + w_mask);
   h->ws.ids = reinterpret_cast<int32_t*>(wb + w_ids);
   h->ws.w = reinterpret_cast<float*>(wb + w_w);
@@ -274,6 +279,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.rowoff = reinterpret_cast<int32_t*>(wb + w_ro);
   h->ws.sync = reinterpret_cast<uint32_t*>(wb + w_sync);
   h->ws.cpart = reinterpret_cast<float*>(wb + w_cp);
+  h->ws.ypart = reinterpret_cast<float*>(wb + w_yp);
   h->ws.x_stage = reinterpret_cast<float*>(wb + w_xs);
   h->ws.y_stage = reinterpret_cast<float*>(wb + w_ys);
   h->ws.ids_stage = reinterpret_cast<int32_t*>(wb + w_is);
@@ -301,6 +307,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
     if ((ce = mr::launch_dnorm(d, h->p.Dt, h->p.dnorm, s)) != cudaSuccess) break;
     st = mr::build_recovery_basis(d, h->p.Dt, h->p.U, h->p.eigvals, s);
     if (st != MOE_READER_OK) break;
+    if ((ce = mr::launch_transpose_u(d, h->p.U, h->p.Ut, s)) != cudaSuccess) break;
     if ((ce = mr::launch_project_b(d, h->p.Dt, h->p.U, h->p.b, s)) != cudaSuccess) break;
     if ((ce = mr::configure_decode_kernels(d)) != cudaSuccess) break;
     h->grid = mr::decode_grid(d);

@@ -30,9 +30,46 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kAhead = 8;              // code words a thread loads before using them
-constexpr int kMaxGroups = 16;         // coordinate groups of a screen unit
 constexpr unsigned long long kWaitNs = 1000000000ull;
+
+// Shared-memory plan of the screen (host-computed, passed to the kernel).
+constexpr size_t kSmemBudget = 226 * 1024 - 128;   // dynamic shared memory: 227 KB less static, slack
+struct ScreenPlan {
+  int wpt;           // 4-byte code words per thread (16 channels each)
+  int tw;            // warps per team
+  int nteams;        // teams side by side (at most 15: one named barrier each)
+  int coord_off;     // within a unit buffer: the coordinates after the pair tables
+  int buf_bytes;     // one unit buffer
+  int team_bytes;    // 128-byte flag area + two unit buffers
+  size_t bytes;      // shared memory of the screen; 0: the shape does not fit
+};
+
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+ScreenPlan screen_plan(const Dims& d) {
+  ScreenPlan sp{};
+  const int W4 = d.I / 8;                        // 4-byte words per coordinate record
+  double best = 0.0;
+  for (int wpt = 1; wpt <= 3; ++wpt) {           // most useful lanes per issue slot
+    const int tw = (W4 + 32 * wpt - 1) / (32 * wpt);
+    if (tw > kWarps) continue;
+    const int nteams = std::min(15, kWarps / tw);
+    const double score = (double)nteams / wpt;
+    if (score > best + 1e-9) {
+      best = score;
+      sp.wpt = wpt;
+      sp.tw = tw;
+      sp.nteams = nteams;
+    }
+  }
+  if (best == 0.0) return sp;
+  sp.coord_off = (int)round_up(64 * (size_t)((d.c + 1) / 2), 128);
+  sp.buf_bytes = sp.coord_off + 128;
+  sp.team_bytes = 128 + 2 * sp.buf_bytes;
+  sp.bytes = (size_t)sp.nteams * sp.team_bytes;
+  if (sp.bytes > kSmemBudget) sp.bytes = 0;
+  return sp;
+}
 
 struct Params {
   Dims d;
@@ -49,10 +86,10 @@ struct Params {
   const __nv_bfloat16* V;
   const __nv_bfloat16* Dt;
   const __half* U;
+  const __half* Ut;
   const __half* bco;
   int32_t* ids_ws;
   float* w_ws;
-  float* rx;
   uint32_t* mask;
   float* partial;
   float* ghat;
@@ -64,11 +101,13 @@ struct Params {
   int32_t* rowoff;
   float* wa;
   float* cvec;                  // [Bmax][r] recovery vectors, accumulated atomically
+  float* ypart;                 // [Bmax][ncb][kOutChunksMax][kOutCols] output partials
   unsigned long long* stamps;   // [grid][5] phase timestamps, or null
   uint32_t* sync;
   uint32_t* err;
-  int Q;    // coordinate groups of a screen unit
-  int W8;   // 8-byte code words per coordinate record (gate run + up run)
+  uint8_t* clist;               // [Bmax][nb][128] screened coordinates, ascending
+  float* rsel;                  // [Bmax][nb][128] their fp32 Rx values, same order
+  ScreenPlan sp;
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -83,10 +122,37 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-__device__ __forceinline__ uint2 ldg_nc2(const void* p) {
-  uint2 r;
-  asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+// L2 eviction policies: streamed-once weights go first, the kept transposed
+// down rows (read again by the output phase) stay.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ldg_nc4_hint(const void* p, uint64_t pol) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(pol));
   return r;
+}
+__device__ __forceinline__ uint4 ldcg4_hint(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+// whole-row L2 prefetch (16-byte aligned address, size a multiple of 16)
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes),
+               "l"(pol)
+               : "memory");
 }
 
 __device__ __forceinline__ uint4 ldg_nc4(const void* p) {
@@ -116,18 +182,18 @@ __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* a
 
 // Offsets (in uint32) of the synchronisation area, fixed per handle.
 struct SyncOff {
-  int rot, slot, tok, flag, total;
+  int slot, tok, flag, out, total;
 };
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
-  o.rot = 16;
-  o.slot = o.rot + d.Bmax * d.nb;
+  o.slot = 16;
   o.tok = o.slot + d.Bmax * d.topk;
   o.flag = o.tok + d.Bmax;
-  o.total = o.flag + d.Bmax;
+  o.out = o.flag + d.Bmax;
+  o.total = o.out + d.Bmax * ((d.H + 255) / 256);
   return o;
 }
-constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2, kSyncNext = 3;
+constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2, kSyncRot = 3;
 
 // ------------------------------- phase 0 -----------------------------------
 __device__ void rotate_item(const Params& P, int t, int b, int lane) {
@@ -197,6 +263,9 @@ __device__ void rotate_item(const Params& P, int t, int b, int lane) {
   const uint32_t below = (1u << lane) - 1u;
   int before = 0;
   const float inv = 0.08838834764831845f;   // 1/sqrt(128) rounded to fp32
+  // the screened list in ascending coordinate order, with its Rx values
+  const size_t row = ((size_t)t * d.nb + b) * kBlock;
+  int listed = 0;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const uint32_t eqb = __ballot_sync(0xffffffffu, m[s] == T);
@@ -204,13 +273,17 @@ __device__ void rotate_item(const Params& P, int t, int b, int lane) {
     before += __popc(eqb);
     const uint32_t word = __ballot_sync(0xffffffffu, sel);
     if (lane == 0) P.mask[((size_t)t * d.nb + b) * 4 + s] = word;
-    P.rx[(size_t)t * d.Hp + b * kBlock + lane + 32 * s] = u[s] * inv;
+    const int pos = listed + __popc(word & below);
+    if (sel && pos < kBlock) {
+      P.clist[row + pos] = (uint8_t)(lane + 32 * s);
+      P.rsel[row + pos] = u[s] * inv;
+    }
+    listed += __popc(word);
   }
   __syncwarp();
-  if (lane == 0) {
-    __threadfence();
-    atomicExch(&P.sync[sync_offsets(d).rot + t * d.nb + b], 1u);
-  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicAdd(P.sync + kSyncRot, 1u);
 }
 
 // ------------------------------- top-k -------------------------------------
@@ -441,135 +514,220 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
 }
 
 // ------------------------------- phase 1 -----------------------------------
-// A screen unit runs on UT threads of the CTA: the whole CTA (UT = 512) when
-// there are fewer units than CTAs, otherwise each half of the CTA (UT = 256)
-// runs its own unit, synchronised by a named barrier, so two units' memory
-// round trips overlap on every SM.
-struct UnitCtx {
-  int ut;              // thread index within the unit
-  int UT;              // threads of the unit
-  int bar;             // named barrier id (0 = __syncthreads)
-  unsigned char* sm;   // this unit's shared memory
-};
+// Screen units (token, slot, block) are dealt to the CTAs round-robin; all
+// cost the same.  Inside a CTA the warps form teams that each compute whole
+// units, several units side by side.  Shared memory per team: a flag area and
+// two unit buffers, each the unit's pair tables [ceil(c/2)][16] fp32 (64-byte
+// aligned) and its screened coordinates [128] u8.
 
-__device__ __forceinline__ void unit_sync(const UnitCtx& c) {
-  if (c.UT == kThreads)
-    __syncthreads();
-  else
-    asm volatile("bar.sync %0, %1;" ::"r"(c.bar), "r"(c.UT) : "memory");
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__host__ __device__ inline int unit_groups(int W8, int UT) {
-  int Q = UT / W8;
-  if (Q > kMaxGroups) Q = kMaxGroups;
-  return Q < 1 ? 1 : Q;
+// Entry of a 64-byte aligned pair table at shared address `tab` indexed by
+// nibble mm of z (byte offset = nibble * 4, or-ed into the aligned base).
+__device__ __forceinline__ float lut_entry(uint32_t tab, uint32_t z, int mm) {
+  const uint32_t off = mm == 0 ? (z << 2) & 0x3Cu : (z >> (4 * mm - 2)) & 0x3Cu;
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(tab | off));
+  return v;
 }
 
-__host__ __device__ inline size_t unit_smem_bytes(int I, int Q) {
-  const int Wp = (I / 16) | 1;
-  return (size_t)4 * I + kBlock * 8 + 16 + (size_t)Q * 32 * Wp * 4;
+__device__ __forceinline__ uint32_t ldg_nc1(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
 }
 
-// One (token, slot, block) unit: alpha-scaled block partials of ghat/vhat.
-// false: the CTA must stop (timeout / abort).
-__device__ bool screen_unit(const Params& P, int t, int slot, int b, const UnitCtx& cx) {
+__device__ __forceinline__ void team_sync(int team, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(threads) : "memory");
+}
+
+// Publish a stored unit: the warp's partial stores, then its share of the
+// (token, slot) counter (complete at nb * tw).
+__device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicAdd(P.sync + sync_offsets(P.d).slot + ts, 1u);
+}
+
+// A team of tw warps owns whole units (team k takes the CTA's units k,
+// k + nteams, ...).  Per unit the team's first warp writes the pair tables
+// and the screened coordinates into one of the team's two buffers; then
+// thread tt reads WPT 4-byte code words (16 channels each) of every screened
+// coordinate record straight into registers, a batch of kU pairs ahead of
+// the one being summed, two coordinates per table read.  The team's warps
+// meet once per unit (named barrier); a warp publishes a unit once the next
+// one is computed, so the fence finds the stores long done.
+template <int WPT>
+__device__ void screen_team(const Params& P, unsigned char* tsm, int team, int tt) {
   const Dims& d = P.d;
-  const SyncOff so = sync_offsets(d);
-  const int ts = t * d.topk + slot;
-  int e = P.ids_in[ts];
-  if (e < 0 || e >= d.E) e = 0;
-  const int I = d.I;
-  // shared memory: alpha [2I] half, clist [128] int, rlist [128] float, flags [4], red [Q][32][Wp]
-  __half* alpha = reinterpret_cast<__half*>(cx.sm);
-  int* clist = reinterpret_cast<int*>(cx.sm + 4 * (size_t)I);
-  float* rlist = reinterpret_cast<float*>(clist + kBlock);
-  int* flags = reinterpret_cast<int*>(rlist + kBlock);
-  float* red = reinterpret_cast<float*>(flags + 4);
-
-  // alpha, the mask words and the rotation flag are requested together
-  const __half* sc = P.scales + ((size_t)e * d.nb + b) * 2 * I;
-  for (int i = cx.ut; i < I / 4; i += cx.UT)
-    reinterpret_cast<uint4*>(alpha)[i] = ldg_nc4(reinterpret_cast<const uint4*>(sc) + i);
-  if (cx.ut == 0)
-    flags[0] = wait_at_least(P.sync + so.rot + t * d.nb + b, 1u, P.sync + kSyncAbort, P.err);
-  unit_sync(cx);
-  if (!flags[0]) return false;
-  if (cx.ut < kBlock) {
-    const int c = cx.ut;
-    const uint32_t* mk = P.mask + ((size_t)t * d.nb + b) * 4;
-    const uint4 mw = __ldcg(reinterpret_cast<const uint4*>(mk));
-    const uint32_t words[4] = {mw.x, mw.y, mw.z, mw.w};
-    const uint32_t word = words[c >> 5];
-    if ((word >> (c & 31)) & 1u) {
-      int pos = __popc(word & ((1u << (c & 31)) - 1u));
+  const ScreenPlan& sp = P.sp;
+  const int lane = threadIdx.x & 31, tw_i = tt >> 5;
+  const int TT = 32 * sp.tw, R16 = d.I / 16, W4 = 2 * R16;
+  const int units = P.B * d.topk * d.nb, nctas = gridDim.x;
+  const uint32_t S2 = 2u * (uint32_t)d.S;
+  const int np = (d.c + 1) >> 1;
+  constexpr int kU = WPT == 1 ? 6 : (WPT == 2 ? 2 : 1);   // pairs per load batch
+  volatile int* flag = reinterpret_cast<volatile int*>(tsm);   // [0] ok, [2 + n % 2] expert id
+  uint32_t off[WPT];
+  int gv[WPT], jw[WPT];
+  bool has[WPT];
 #pragma unroll
-      for (int w2 = 0; w2 < 3; ++w2) pos += w2 < (c >> 5) ? __popc(words[w2]) : 0;
-      if (pos < kBlock) {
-        clist[pos] = c;
-        rlist[pos] = 0.5f * __ldcg(P.rx + (size_t)t * d.Hp + b * kBlock + c);
-      }
-    }
+  for (int x = 0; x < WPT; ++x) {
+    const int w = tt + TT * x;
+    has[x] = w < W4;
+    gv[x] = has[x] ? w / R16 : 0;
+    jw[x] = has[x] ? w % R16 : 0;
+    off[x] = (uint32_t)(gv[x] * d.S + jw[x] * 4);
   }
-  unit_sync(cx);
-
-  const int W8 = P.W8, Q = unit_groups(W8, cx.UT), Wp = W8 | 1;
-  const int j = cx.ut % W8, q = cx.ut / W8;
-  const int half = I / 32;                          // 8-byte words per run
-  if (q < Q) {
-    float acc[32];
+  if (blockIdx.x + team * nctas >= units) return;   // no unit for this team
+  if (tt == 0)
+    flag[0] = wait_at_least(P.sync + kSyncRot, (uint32_t)(P.B * d.nb), P.sync + kSyncAbort, P.err);
+  // the first warp keeps the next unit's list in registers
+  uint32_t cl = 0;
+  float4 rs = make_float4(0.f, 0.f, 0.f, 0.f);
+  int enext = 0;
+  auto load_list = [&](int uu) {
+    const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
+    const size_t row = ((size_t)t * d.nb + b) * 32 + lane;
+    cl = __ldcg(reinterpret_cast<const uint32_t*>(P.clist) + row);
+    rs = __ldcg(reinterpret_cast<const float4*>(P.rsel) + row);
+    enext = __ldcg(P.ids_ws + ts);
+  };
+  team_sync(team, TT);
+  if (!flag[0]) return;
+  if (tw_i == 0) load_list(blockIdx.x + team * nctas);
+  int pend = -1;
+  for (int ul = team, n = 0;; ul += sp.nteams, ++n) {
+    const int u = blockIdx.x + ul * nctas;
+    if (u >= units) break;
+    unsigned char* buf = tsm + 128 + (size_t)(n & 1) * sp.buf_bytes;
+    if (tw_i == 0) {
+      // pair tables: lane l holds list positions 4l .. 4l+3, i.e. pairs 2l, 2l+1
+      const float rv[4] = {rs.x, rs.y, rs.z, rs.w};
 #pragma unroll
-    for (int u = 0; u < 32; ++u) acc[u] = 0.f;
-    const size_t run_off = j < half ? (size_t)j * 8 : (size_t)d.S + (size_t)(j - half) * 8;
-    const uint8_t* base = P.codes + (((size_t)e * d.nb + b) * kBlock) * 2 * d.S + run_off;
-    for (int p0 = q; p0 < d.c; p0 += Q * kAhead) {
-      uint2 wv[kAhead];
-      float rv[kAhead];
+      for (int h = 0; h < 2; ++h) {
+        const int p = 4 * lane + 2 * h;
+        if (p < d.c) {
+          const float r0 = rv[2 * h], r1 = p + 1 < d.c ? rv[2 * h + 1] : 0.f;
+          float4* tab = reinterpret_cast<float4*>(buf) + (p >> 1) * 4;
 #pragma unroll
-      for (int u = 0; u < kAhead; ++u) {
-        const int pp = p0 + u * Q;
-        if (pp < d.c) {
-          const int cc = clist[pp] & (kBlock - 1);
-          wv[u] = ldg_nc2(base + (size_t)cc * 2 * d.S);
-          rv[u] = rlist[pp];
-        } else {
-          wv[u] = make_uint2(0u, 0u);
-          rv[u] = 0.f;
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const float t1 = g4 == 1 ? r1 : (g4 == 3 ? -r1 : 0.f);   // code of the odd position
+            tab[g4] = make_float4(t1, r0 + t1, t1, t1 - r0);         // even position 00 01 10 11
+          }
         }
       }
+      // coordinates; an odd count's spare position repeats the last one
+      uint32_t c4 = cl;
+      if ((d.c & 1) && (d.c >> 2) == lane) {
+        const int v = d.c & 3;
+        const uint32_t lastc = (c4 >> (8 * (v - 1))) & 0xffu;
+        c4 = (c4 & ~(0xffu << (8 * v))) | (lastc << (8 * v));
+      }
+      reinterpret_cast<uint32_t*>(buf + sp.coord_off)[lane] = c4;
+      if (lane == 0) flag[2 + (n & 1)] = enext;
+      const int un = u + sp.nteams * nctas;
+      if (un < units) load_list(un);   // in flight while this unit is summed
+    }
+    team_sync(team, TT);
+    int e = flag[2 + (n & 1)];
+    if (e < 0 || e >= d.E) e = 0;
+    const int ts = u / d.nb, b = u % d.nb;
+    const uint8_t* rec = P.codes + ((size_t)e * d.nb + b) * kBlock * S2;
+    const uint32_t lut0 = smem_addr(buf);
+    const uint16_t* cpair = reinterpret_cast<const uint16_t*>(buf + sp.coord_off);
+    // alpha of the thread's channels, requested now, used at the end
+    uint4 al[WPT][2];
 #pragma unroll
-      for (int u = 0; u < kAhead; ++u) {
-        // a 2-bit code moved to bits 31:30 and masked is the fp32 value 2t;
-        // rv holds r/2, so each product is exactly +-r or 0
+    for (int x = 0; x < WPT; ++x) {
+      const uint4* a4 = reinterpret_cast<const uint4*>(
+          P.scales + (((size_t)e * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
+      al[x][0] = has[x] ? ldg_nc4(a4) : make_uint4(0u, 0u, 0u, 0u);
+      al[x][1] = has[x] ? ldg_nc4(a4 + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float acc[WPT][16];
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          acc[kk] = fmaf(__uint_as_float((wv[u].x << (30 - 2 * kk)) & 0xC0000000u), rv[u], acc[kk]);
-          acc[16 + kk] =
-              fmaf(__uint_as_float((wv[u].y << (30 - 2 * kk)) & 0xC0000000u), rv[u], acc[16 + kk]);
+    for (int x = 0; x < WPT; ++x)
+#pragma unroll
+      for (int q = 0; q < 16; ++q) acc[x][q] = 0.f;
+    uint32_t wa[2][kU][WPT], wb[2][kU][WPT];
+    auto issue = [&](int pp0, uint32_t (&ra)[kU][WPT], uint32_t (&rb)[kU][WPT]) {
+#pragma unroll
+      for (int v = 0; v < kU; ++v) {
+        const int pp = pp0 + v;
+        const uint32_t cp = pp < np ? cpair[pp] : 0u;
+        const uint8_t* ra_p = rec + (size_t)(cp & 0xffu) * S2;
+        const uint8_t* rb_p = rec + (size_t)(cp >> 8) * S2;
+#pragma unroll
+        for (int x = 0; x < WPT; ++x) {
+          const bool in = pp < np && has[x];
+          ra[v][x] = in ? ldg_nc1(ra_p + off[x]) : 0u;
+          rb[v][x] = in ? ldg_nc1(rb_p + off[x]) : 0u;
         }
       }
-    }
-    // layout [q][kk][j] with an odd row stride Wp: the stores (consecutive j) and
-    // the loads below (consecutive kk) both fall in distinct banks
+    };
+    auto sum = [&](int pp0, const uint32_t (&ra)[kU][WPT], const uint32_t (&rb)[kU][WPT]) {
 #pragma unroll
-    for (int u = 0; u < 32; ++u) red[(size_t)q * 32 * Wp + u * Wp + j] = acc[u];
+      for (int v = 0; v < kU; ++v) {
+        const uint32_t lb = lut0 + 64u * (uint32_t)min(pp0 + v, np - 1);   // index 0 of a table is 0
+#pragma unroll
+        for (int x = 0; x < WPT; ++x) {
+          // nibble mm: (even-position code) | (odd-position code) << 2 of channel 2mm / 2mm+1
+          const uint32_t ze = (ra[v][x] & 0x33333333u) | ((rb[v][x] << 2) & 0xCCCCCCCCu);
+          const uint32_t zo = ((ra[v][x] >> 2) & 0x33333333u) | (rb[v][x] & 0xCCCCCCCCu);
+#pragma unroll
+          for (int mm = 0; mm < 8; ++mm) {
+            acc[x][2 * mm] += lut_entry(lb, ze, mm);
+            acc[x][2 * mm + 1] += lut_entry(lb, zo, mm);
+          }
+        }
+      }
+    };
+    issue(0, wa[0], wb[0]);
+    for (int pp0 = 0; pp0 < np; pp0 += 2 * kU) {
+      if (pp0 + kU < np) issue(pp0 + kU, wa[1], wb[1]);
+      sum(pp0, wa[0], wb[0]);
+      if (pp0 + kU >= np) break;
+      if (pp0 + 2 * kU < np) issue(pp0 + 2 * kU, wa[0], wb[0]);
+      sum(pp0 + kU, wa[1], wb[1]);
+    }
+    if (pend >= 0) publish_unit(P, pend, lane);
+#pragma unroll
+    for (int x = 0; x < WPT; ++x) {
+      if (!has[x]) continue;
+      const uint32_t hw[8] = {al[x][0].x, al[x][0].y, al[x][0].z, al[x][0].w,
+                              al[x][1].x, al[x][1].y, al[x][1].z, al[x][1].w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[q]));
+        acc[x][2 * q] *= f.x;
+        acc[x][2 * q + 1] *= f.y;
+      }
+      float4* out = reinterpret_cast<float4*>(
+          P.partial + (((size_t)ts * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        out[q] = make_float4(acc[x][4 * q], acc[x][4 * q + 1], acc[x][4 * q + 2], acc[x][4 * q + 3]);
+    }
+    pend = ts;
   }
-  unit_sync(cx);
-  float* out = P.partial + ((size_t)ts * d.nb + b) * 2 * I;
-  for (int o = cx.ut; o < 2 * I; o += cx.UT) {
-    const int jj = o / 32, kk = o % 32;
-    float s = 0.f;
-    for (int qq = 0; qq < Q; ++qq) s += red[(size_t)qq * 32 * Wp + kk * Wp + jj];
-    const int gv = jj / half;
-    const int i = (jj % half) * 32 + kk;
-    out[gv * I + i] = s * __half2float(alpha[gv * I + i]);
-  }
-  // publish: the barrier orders the unit's stores before the leader's fence + add
-  unit_sync(cx);
-  if (cx.ut == 0) {
-    __threadfence();
-    atomicAdd(P.sync + so.slot + ts, 1u);
-  }
-  return true;
+  if (pend >= 0) publish_unit(P, pend, lane);
+}
+
+__device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
+  const ScreenPlan& sp = P.sp;
+  const int team = warp / sp.tw;
+  if (team >= sp.nteams) return;   // warps left over by the team size
+  unsigned char* tsm = smem + (size_t)team * sp.team_bytes;
+  const int tt = (warp % sp.tw) * 32 + (threadIdx.x & 31);
+  if (sp.wpt == 1)
+    screen_team<1>(P, tsm, team, tt);
+  else if (sp.wpt == 2)
+    screen_team<2>(P, tsm, team, tt);
+  else
+    screen_team<3>(P, tsm, team, tt);
 }
 
 // Score the channels of one (token, slot) once all its blocks are in: sum
@@ -579,7 +737,8 @@ __device__ bool score_task(const Params& P, int ts, int* flag) {
   const SyncOff so = sync_offsets(d);
   const int t = ts / d.topk, slot = ts % d.topk, I = d.I;
   if (threadIdx.x == 0)
-    *flag = wait_at_least(P.sync + so.slot + ts, (uint32_t)d.nb, P.sync + kSyncAbort, P.err);
+    *flag = wait_at_least(P.sync + so.slot + ts, (uint32_t)(d.nb * P.sp.tw), P.sync + kSyncAbort,
+                          P.err);
   __syncthreads();
   if (!*flag) return false;
   int e = P.ids_in[ts];
@@ -630,9 +789,6 @@ __device__ __forceinline__ void dot8(const uint4& q, const float4& xa, const flo
   s = fmaf(bf16_lo(q.w), xb.z, s); s = fmaf(bf16_hi(q.w), xb.w, s);
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
-}
 
 __device__ void kept_item(const Params& P, int t, int qi, int lane) {
   const Dims& d = P.d;
@@ -641,11 +797,9 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane) {
   const int e = __ldcg(P.ids_ws + t * d.topk + slot);
   const size_t row = (size_t)e * d.I + i;
   // the output phase reads this channel's transposed down row in 32-byte
-  // pieces from many CTAs: bring the whole row into L2 now
-  {
-    const char* dt = reinterpret_cast<const char*>(P.Dt + row * d.H);
-    for (int off = lane * 128; off < d.H * 2; off += 32 * 128) prefetch_l2(dt + off);
-  }
+  // pieces from many CTAs: bring the whole row into L2 now, to stay there
+  if (lane == 0) bulk_prefetch_l2(P.Dt + row * d.H, 2u * (uint32_t)d.H, policy_evict_last());
+  const uint64_t pol = policy_evict_first();
   const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
   const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
   const float4* x4 = reinterpret_cast<const float4*>(P.x + (size_t)t * d.H);
@@ -657,8 +811,8 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane) {
     uint4 gq[kU], vq[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      gq[u] = ldg_nc4(g4 + h8 + 32 * u);
-      vq[u] = ldg_nc4(v4 + h8 + 32 * u);
+      gq[u] = ldg_nc4_hint(g4 + h8 + 32 * u, pol);
+      vq[u] = ldg_nc4_hint(v4 + h8 + 32 * u, pol);
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
@@ -668,7 +822,7 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane) {
     }
   }
   for (; h8 < n8; h8 += 32) {
-    const uint4 gq = ldg_nc4(g4 + h8), vq = ldg_nc4(v4 + h8);
+    const uint4 gq = ldg_nc4_hint(g4 + h8, pol), vq = ldg_nc4_hint(v4 + h8, pol);
     const float4 xa = __ldg(x4 + 2 * h8), xb = __ldg(x4 + 2 * h8 + 1);
     dot8(gq, xa, xb, sg);
     dot8(vq, xa, xb, sv);
@@ -754,93 +908,145 @@ __device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
   acc[6] = fmaf(c, bf16_lo(v.w), acc[6]); acc[7] = fmaf(c, bf16_hi(v.w), acc[7]);
 }
 
-constexpr int kTokGroup = 2;
-constexpr int kRowBatch = 4;   // rows per token and thread whose loads are issued together
+constexpr int kOutCols = 256;        // columns of an output block: 8 per lane
+constexpr int kOutChunksMax = 32;    // row chunks per (token, output block)
+constexpr int kOutBatch = 12;        // kept rows whose loads a warp issues together
 
-// One output item: 16 columns h0..h0+15 (one 32-byte piece of every kept
-// transposed down row) for tokens t0, t0+1.  Thread (rg, half): rows
-// rg, rg+256, ...; 8 columns each.  y = sum_K (w a)_j Dt_j + U c.
-__device__ void out_item(const Params& P, int s, int t0, unsigned char* smem) {
+struct OutPlan {
+  int ncb;   // output blocks
+  int R;     // kept-row chunks per (token, block)
+  int RC;    // kept rows per chunk
+  int NR;    // chunks per (token, block): R, plus the recovery chunk U c when k < N
+};
+
+// Enough (token, block, chunk) warp items to occupy every warp once.
+__device__ __forceinline__ OutPlan out_plan(const Params& P, int nwarps) {
+  OutPlan op;
+  op.ncb = (P.d.H + kOutCols - 1) / kOutCols;
+  const int per = P.B * op.ncb;
+  const int rec = P.k < P.d.N ? 1 : 0;
+  int R = nwarps / per - rec;                 // one round of warp items
+  R = min(R, kOutChunksMax - 1);
+  R = max(1, min(R, P.k));
+  op.RC = (P.k + R - 1) / R;
+  op.R = op.RC > 0 ? (P.k + op.RC - 1) / op.RC : 1;
+  op.NR = op.R + rec;
+  return op;
+}
+
+__device__ __forceinline__ void axpy8h(float c, const uint4& v, float* acc) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[h]));
+    acc[2 * h] = fmaf(c, f.x, acc[2 * h]);
+    acc[2 * h + 1] = fmaf(c, f.y, acc[2 * h + 1]);
+  }
+}
+
+// One warp item: columns cb*256 + 8 lane .. +7 of token t over kept rows
+// [rc RC, (rc+1) RC) of Dt, each row read as one coalesced 512-byte piece, or
+// for rc = R the recovery U c as the r rows of U^T weighted by c.  The
+// partial goes to ypart; the warp that completes a (token, block) sums its
+// chunks in chunk order and writes y.
+__device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int rc, int lane) {
   const Dims& d = P.d;
-  float* wred = reinterpret_cast<float*>(smem);        // [kTokGroup][kWarps][16]
-  float* us = wred + kTokGroup * kWarps * 16;          // [16][r]  U rows of the slice
-  float* cs = us + 16 * kMaxRank;                      // [kTokGroup][r] recovery vectors
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int h0 = s * 16;
-  const bool recover = P.k < d.N;
-  if (recover) {
-    for (int q = threadIdx.x; q < 16 * d.r; q += kThreads) {
-      const int h = h0 + q / d.r;
-      us[q] = h < d.H ? __half2float(P.U[(size_t)h * d.r + q % d.r]) : 0.f;
-    }
-    for (int q = threadIdx.x; q < kTokGroup * d.r; q += kThreads) {
-      const int t = t0 + q / d.r;
-      cs[q] = t < P.B ? __ldcg(P.cvec + (size_t)t * d.r + q % d.r) : 0.f;
-    }
-  }
-  const int rg = threadIdx.x >> 1, hf = threadIdx.x & 1;   // 256 row groups x 2 halves
-  const int hh = h0 + hf * 8;
-  float acc[kTokGroup][8];
+  const int c0 = cb * kOutCols + lane * 8;
+  const bool on = c0 < d.H;                  // H is a multiple of 8
+  const int qb0 = rc * op.RC, qe = min(P.k, qb0 + op.RC);
+  const uint64_t pol = policy_evict_first();  // the last read of these rows
+  const int32_t* ro_t = P.rowoff + (size_t)t * d.N;
+  const float* wa_t = P.wa + (size_t)t * d.N;
+  float acc[8];
 #pragma unroll
-  for (int tt = 0; tt < kTokGroup; ++tt)
+  for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+  if (rc == op.R) {   // recovery chunk
+    const float* c_t = P.cvec + (size_t)t * d.r;
+    for (int jb = 0; jb < d.r; jb += 32) {
+      const int nj = min(32, d.r - jb);
+      const float cj_l = lane < nj ? __ldcg(c_t + jb + lane) : 0.f;
+      for (int i0 = 0; i0 < nj; i0 += kOutBatch) {
+        uint4 v[kOutBatch];
+        float c[kOutBatch];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) acc[tt][u] = 0.f;
-  if (hh < d.H) {
-    for (int q0 = rg; q0 < P.k; q0 += 256 * kRowBatch) {
-      int32_t r[kTokGroup][kRowBatch];
-      float c[kTokGroup][kRowBatch];
-#pragma unroll
-      for (int tt = 0; tt < kTokGroup; ++tt)
-#pragma unroll
-        for (int u = 0; u < kRowBatch; ++u) {
-          const int q = q0 + 256 * u;
-          const bool ok = t0 + tt < P.B && q < P.k;
-          r[tt][u] = ok ? __ldcg(P.rowoff + (size_t)(t0 + tt) * d.N + q) : -1;
-          c[tt][u] = ok ? __ldcg(P.wa + (size_t)(t0 + tt) * d.N + q) : 0.f;
+        for (int u = 0; u < kOutBatch; ++u) {
+          const int i = i0 + u;
+          const float cw = __shfl_sync(0xffffffffu, cj_l, i & 31);
+          c[u] = i < nj ? cw : 0.f;
+          v[u] = i < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(jb + i) * d.H + c0))
+                              : make_uint4(0u, 0u, 0u, 0u);
         }
-      uint4 v[kTokGroup][kRowBatch];
 #pragma unroll
-      for (int tt = 0; tt < kTokGroup; ++tt)
-#pragma unroll
-        for (int u = 0; u < kRowBatch; ++u)
-          v[tt][u] = r[tt][u] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(P.Dt + (size_t)r[tt][u] * d.H + hh))
-                                   : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int tt = 0; tt < kTokGroup; ++tt)
-#pragma unroll
-        for (int u = 0; u < kRowBatch; ++u) axpy8(c[tt][u], v[tt][u], acc[tt]);
+        for (int u = 0; u < kOutBatch; ++u) axpy8h(c[u], v[u], acc);
+      }
     }
   }
-  // sum the 16 row groups of the warp (lane bits 1..4), then the 16 warps
+  for (int qb = qb0; qb < qe; qb += 32) {
+    const int nq = min(32, qe - qb);
+    const int32_t ro_l = lane < nq ? __ldcg(ro_t + qb + lane) : 0;
+    const float cw_l = lane < nq ? __ldcg(wa_t + qb + lane) : 0.f;
+    for (int i0 = 0; i0 < nq; i0 += kOutBatch) {
+      uint4 v[kOutBatch];
+      float c[kOutBatch];
 #pragma unroll
-  for (int tt = 0; tt < kTokGroup; ++tt)
+      for (int u = 0; u < kOutBatch; ++u) {
+        const int i = i0 + u;
+        const int ro = __shfl_sync(0xffffffffu, ro_l, i & 31);
+        const float cw = __shfl_sync(0xffffffffu, cw_l, i & 31);
+        const bool use = i < nq && on;
+        c[u] = i < nq ? cw : 0.f;
+        v[u] = use ? ldcg4_hint(P.Dt + (size_t)ro * d.H + c0, pol) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int o = 2; o < 32; o <<= 1) acc[tt][u] += __shfl_xor_sync(0xffffffffu, acc[tt][u], o);
-  if (lane < 2)
-#pragma unroll
-    for (int tt = 0; tt < kTokGroup; ++tt)
-#pragma unroll
-      for (int u = 0; u < 8; ++u) wred[(tt * kWarps + warp) * 16 + lane * 8 + u] = acc[tt][u];
-  __syncthreads();
-  if (threadIdx.x < 16 * kTokGroup) {
-    const int tt = threadIdx.x >> 4, col = threadIdx.x & 15;
-    const int t = t0 + tt, h = h0 + col;
-    if (t < P.B && h < d.H) {
-      float sum = 0.f;
-      for (int w = 0; w < kWarps; ++w) sum += wred[(tt * kWarps + w) * 16 + col];
-      if (recover)
-        for (int jj = 0; jj < d.r; ++jj) sum = fmaf(us[col * d.r + jj], cs[tt * d.r + jj], sum);
-      P.y[(size_t)t * d.H + h] = sum;
+      for (int u = 0; u < kOutBatch; ++u) axpy8(c[u], v[u], acc);
     }
   }
-  __syncthreads();
+  const size_t blk = ((size_t)t * op.ncb + cb) * kOutChunksMax;
+  float4* part = reinterpret_cast<float4*>(P.ypart + (blk + rc) * kOutCols + lane * 8);
+  part[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  part[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __threadfence();
+  __syncwarp();
+  uint32_t* cnt = P.sync + sync_offsets(d).out + t * op.ncb + cb;
+  uint32_t prev = 0;
+  if (lane == 0) prev = atomicAdd(cnt, 1u);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  if (prev != (uint32_t)(op.NR - 1)) return;
+  // the last chunk in: sum the chunks in order
+  __threadfence();
+  float y8[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) y8[u] = 0.f;
+  for (int r0 = 0; r0 < op.NR; r0 += 8) {   // loads in groups of 8 chunks, sums in order
+    float4 a[8], b[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float4* pp = reinterpret_cast<const float4*>(P.ypart + (blk + r0 + u) * kOutCols + lane * 8);
+      a[u] = r0 + u < op.NR ? __ldcg(pp) : make_float4(0.f, 0.f, 0.f, 0.f);
+      b[u] = r0 + u < op.NR ? __ldcg(pp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (r0 + u < op.NR) {
+        y8[0] += a[u].x; y8[1] += a[u].y; y8[2] += a[u].z; y8[3] += a[u].w;
+        y8[4] += b[u].x; y8[5] += b[u].y; y8[6] += b[u].z; y8[7] += b[u].w;
+      }
+    }
+  }
+  if (on) {
+    float4* yo = reinterpret_cast<float4*>(P.y + (size_t)t * d.H + c0);
+    yo[0] = make_float4(y8[0], y8[1], y8[2], y8[3]);
+    yo[1] = make_float4(y8[4], y8[5], y8[6], y8[7]);
+  }
+  if (lane == 0) *cnt = 0u;   // every chunk of this block is in: ready for the next call
 }
 
 // ------------------------------- the kernel --------------------------------
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // the pair tables are addressed by or-ing offsets into 64-byte aligned
+  // bases: align the working area to 128 bytes whatever the window offset
+  unsigned char* const smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
   __shared__ int ctl[2];
   if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
@@ -861,38 +1067,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     __syncthreads();
     if (threadIdx.x == 0) stamp[1] = globaltimer();
   }
-  // phase 1a: screen units (token, slot, block) from a shared queue
-  {
-    const int units = P.B * d.topk * d.nb;
-    const bool halves = units > nctas;
-    const int UT = halves ? kThreads / 2 : kThreads;
-    const int hid = halves ? (int)(threadIdx.x / UT) : 0;
-    UnitCtx cx;
-    cx.ut = threadIdx.x - hid * UT;
-    cx.UT = UT;
-    cx.bar = 1 + hid;
-    cx.sm = smem + (size_t)hid * unit_smem_bytes(d.I, unit_groups(P.W8, UT));
-    int* next = reinterpret_cast<int*>(cx.sm + 4 * (size_t)d.I + kBlock * 8);   // flags[0..3]
-    if (cx.ut == 0) next[1] = (int)atomicAdd(P.sync + kSyncNext, 1u);
-    unit_sync(cx);
-    int u = next[1];
-    bool ok = true;
-    while (u < units) {
-      // take the following unit now so the round trip overlaps this one
-      if (cx.ut == 0) next[2] = (int)atomicAdd(P.sync + kSyncNext, 1u);
-      const int b = u % d.nb, ts = u / d.nb;
-      if (!screen_unit(P, ts / d.topk, ts % d.topk, b, cx)) {
-        ok = false;
-        break;
-      }
-      unit_sync(cx);
-      u = next[2];
-      unit_sync(cx);
-    }
-    if (!ok) ctl[0] = 1;
-    __syncthreads();
-    if (ctl[0] == 1) return;
-  }
+  // phase 1a: screen units, computed by teams of warps
+  screen_compute(P, smem, warp);
+  __syncthreads();
   // phase 1b: scoring tasks, then 1c: top-k tasks, spread over the CTAs
   {
     int* flag = reinterpret_cast<int*>(smem);
@@ -952,12 +1129,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   }
   __syncthreads();
   if (!ctl[1]) return;
-  // phase 3: output items (16-column slice, token pair)
+  // phase 3: output warp items (token, 256-column block, row chunk)
   {
-    const int slices = (d.H + 15) / 16;
-    const int groups = (P.B + kTokGroup - 1) / kTokGroup;
-    for (int it = blockIdx.x; it < slices * groups; it += nctas)
-      out_item(P, it % slices, (it / slices) * kTokGroup, smem);
+    const int nwarps = nctas * kWarps;
+    const OutPlan op = out_plan(P, nwarps);
+    const int items = P.B * op.ncb * op.NR;
+    for (int it = blockIdx.x + nctas * warp; it < items; it += nwarps)
+      out_chunk(P, op, it / (op.ncb * op.NR), (it / op.NR) % op.ncb, it % op.NR, lane);
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
   // the last CTA out resets the synchronisation area for the next call
@@ -968,7 +1146,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   }
   __syncthreads();
   if (ctl[0]) {
-    for (int i = threadIdx.x; i < P.B * d.nb; i += kThreads) P.sync[so.rot + i] = 0u;
     for (int i = threadIdx.x; i < P.B * d.topk; i += kThreads) P.sync[so.slot + i] = 0u;
     for (int i = threadIdx.x; i < P.B; i += kThreads) {
       P.sync[so.tok + i] = 0u;
@@ -976,28 +1153,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     }
     if (threadIdx.x == 0) {
       P.sync[kSyncExact] = 0u;
-      P.sync[kSyncNext] = 0u;
+      P.sync[kSyncRot] = 0u;
       P.sync[kSyncDone] = 0u;
     }
   }
 }
 
-int screen_groups(const Dims& d) {
-  const int W8 = d.I / 16;
-  int Q = kThreads / W8;
-  if (Q > kMaxGroups) Q = kMaxGroups;
-  if (Q < 1) Q = 1;
-  return Q;
-}
-
 size_t decode_smem_bytes(const Dims& d) {
-  const size_t whole = unit_smem_bytes(d.I, unit_groups(d.I / 16, kThreads));
-  const size_t halves = 2 * unit_smem_bytes(d.I, unit_groups(d.I / 16, kThreads / 2));
-  const size_t screen = whole > halves ? whole : halves;
+  const size_t screen = screen_plan(d).bytes;
   const size_t topk = topk_smem_bytes(d.N);
-  const size_t out = ((size_t)kTokGroup * kWarps * 16 + 16 * kMaxRank + kTokGroup * kMaxRank) * 4;
   const size_t m = screen > topk ? screen : topk;
-  return m > out ? m : out;
+  return m + 128;   // + alignment slack of the working area
 }
 
 }  // namespace
@@ -1005,6 +1171,7 @@ size_t decode_smem_bytes(const Dims& d) {
 size_t sync_words(const Dims& d) { return (size_t)sync_offsets(d).total; }
 
 cudaError_t configure_decode_kernels(const Dims& d) {
+  if (screen_plan(d).bytes == 0) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes(d);
   cudaFuncAttributes fa;
   cudaError_t err = cudaFuncGetAttributes(&fa, decode_kernel);
@@ -1056,10 +1223,12 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
   P.V = h.V;
   P.Dt = h.p.Dt;
   P.U = h.p.U;
+  P.Ut = h.p.Ut;
   P.bco = h.p.b;
   P.ids_ws = ws.ids;
   P.w_ws = ws.w;
-  P.rx = ws.rx;
+  P.clist = ws.clist;
+  P.rsel = ws.rsel;
   P.mask = ws.mask;
   P.partial = ws.partial;
   P.ghat = ws.ghat;
@@ -1071,11 +1240,11 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
   P.rowoff = ws.rowoff;
   P.wa = ws.wa;
   P.cvec = ws.cpart;
+  P.ypart = ws.ypart;
   P.stamps = stamps;
   P.sync = ws.sync;
   P.err = ws.err;
-  P.Q = screen_groups(d);
-  P.W8 = d.I / 16;
+  P.sp = screen_plan(d);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h.grid);

@@ -36,7 +36,8 @@ struct Dims {
 
 // Decode workspace (device), sized for Bmax tokens.
 struct Workspace {
-  float* rx;            // [Bmax][Hp]     fp32 rotated x
+  float* rsel;          // [Bmax][nb][128] fp32 Rx of the screened coordinates, ascending order
+  uint8_t* clist;       // [Bmax][nb][128] the screened coordinates, ascending
   uint32_t* mask;       // [Bmax][nb][4]  screened coordinates
   int32_t* ids;         // [Bmax][topk]   sanitized expert ids
   float* w;             // [Bmax][topk]   routing weights
@@ -50,6 +51,7 @@ struct Workspace {
   float* wa;            // [Bmax][N]      w * a for kept list entries
   int32_t* rowoff;      // [Bmax][N]      e*I + i of kept list entries
   float* cpart;         // [Bmax][r] recovery vector c = sum_S w_j p_j b_j
+  float* ypart;         // [Bmax][ceil(H/256)][32][256] output partials per row chunk
   // host-ABI staging
   float* x_stage;       // [Bmax][H]
   float* y_stage;       // [Bmax][H]
@@ -72,6 +74,7 @@ struct Prepared {
   float* dnorm;         // [E][I]
   __nv_bfloat16* Dt;    // [E][I][H]
   __half* U;            // [H][r]
+  __half* Ut;           // [r][H]  U transposed: rank components as rows
   __half* b;            // [E][I][r]
   int8_t* sigma;        // [Hp]
   double* eigvals;      // [r]
@@ -113,6 +116,7 @@ cudaError_t launch_dnorm(const Dims& d, const __nv_bfloat16* Dt, float* dnorm, c
 // Recovery basis: U (fp16 [H][r]) and eigenvalues from Dt; returns ETIMEOUT via *timeout.
 int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, double* eigvals,
                          cudaStream_t s);
+cudaError_t launch_transpose_u(const Dims& d, const __half* U, __half* Ut, cudaStream_t s);
 cudaError_t launch_project_b(const Dims& d, const __nv_bfloat16* Dt, const __half* U, __half* b,
                              cudaStream_t s);
 

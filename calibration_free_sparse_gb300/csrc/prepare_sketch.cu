@@ -222,6 +222,15 @@ project_b_kernel(Dims d, const __nv_bfloat16* __restrict__ Dt, const __half* __r
 
 }  // namespace
 
+// Ut[j][h] = U[h][j]: the output phase reads rank components as rows.
+__global__ void transpose_u_kernel(int H, int r, const __half* __restrict__ U,
+                                   __half* __restrict__ Ut) {
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= H * r) return;
+  const int j = q / H, h = q % H;
+  Ut[q] = U[(size_t)h * r + j];
+}
+
 cudaError_t launch_sketch(const Dims& d, const __nv_bfloat16* G, const __nv_bfloat16* V,
                           const int8_t* sigma, uint8_t* codes, __half* scales, __half* rho,
                           cudaStream_t s) {
@@ -245,6 +254,12 @@ cudaError_t launch_transpose_down(const Dims& d, const __nv_bfloat16* D, __nv_bf
 cudaError_t launch_dnorm(const Dims& d, const __nv_bfloat16* Dt, float* dnorm, cudaStream_t s) {
   const int rows = d.E * d.I;
   dnorm_kernel<<<(rows + 7) / 8, 256, 0, s>>>(d, Dt, dnorm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_u(const Dims& d, const __half* U, __half* Ut, cudaStream_t s) {
+  const int n = d.H * d.r;
+  transpose_u_kernel<<<(n + 255) / 256, 256, 0, s>>>(d.H, d.r, U, Ut);
   return cudaGetLastError();
 }
 

@@ -102,7 +102,8 @@ typedef struct {
   int32_t num_blocks;           /* nb = Hp / 128 */
   int32_t routed_channels;      /* N = topk * I */
   int32_t run_stride;           /* S: bytes per coordinate run, ceil(ceil(I/4)/32)*32 */
-  uint64_t resident_bytes[9];   /* codes, scales, rho, dnorm, Dt, U, b, sigma, workspace */
+  uint64_t resident_bytes[9];   /* codes, scales, rho, dnorm, Dt, U (with its transpose), b,
+                                   sigma, workspace */
 } moe_reader_info;
 
 /*
