@@ -40,7 +40,10 @@ struct ScreenPlan {
   int nteams;        // teams side by side (at most 15: one named barrier each)
   int coord_off;     // within a unit buffer: the coordinates after the pair tables
   int buf_bytes;     // one unit buffer
-  int team_bytes;    // 128-byte flag area + two unit buffers
+  int cc;            // list positions per copy chunk (even unless one chunk holds the list)
+  int nch;           // chunks per unit
+  int stage_bytes;   // one chunk stage: cc + 1 records (the spare slot of an odd count)
+  int team_bytes;    // 128-byte flag area, two unit buffers, two chunk stages
   size_t bytes;      // shared memory of the screen; 0: the shape does not fit
 };
 
@@ -65,9 +68,19 @@ ScreenPlan screen_plan(const Dims& d) {
   if (best == 0.0) return sp;
   sp.coord_off = (int)round_up(64 * (size_t)((d.c + 1) / 2), 128);
   sp.buf_bytes = sp.coord_off + 128;
-  sp.team_bytes = 128 + 2 * sp.buf_bytes;
+  const size_t S2 = 2 * (size_t)d.S;
+  const size_t per_team = kSmemBudget / sp.nteams / 128 * 128;
+  const size_t fixed = 128 + 2 * (size_t)sp.buf_bytes;
+  for (int nch = 1; nch <= d.c && !sp.cc; ++nch) {
+    int c1 = (d.c + nch - 1) / nch;
+    if (nch > 1) c1 += c1 & 1;                  // chunks hold whole pairs
+    if (fixed + 2 * round_up((size_t)(c1 + 1) * S2, 128) <= per_team) sp.cc = c1;
+  }
+  if (!sp.cc) return sp;
+  sp.nch = (d.c + sp.cc - 1) / sp.cc;
+  sp.stage_bytes = (int)round_up((size_t)(sp.cc + 1) * S2, 128);
+  sp.team_bytes = (int)(fixed + 2 * (size_t)sp.stage_bytes);
   sp.bytes = (size_t)sp.nteams * sp.team_bytes;
-  if (sp.bytes > kSmemBudget) sp.bytes = 0;
   return sp;
 }
 
@@ -533,10 +546,10 @@ __device__ __forceinline__ float lut_entry(uint32_t tab, uint32_t z, int mm) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t ldg_nc1(const void* p) {
-  uint32_t r;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
 }
 
 __device__ __forceinline__ void team_sync(int team, int threads) {
@@ -552,13 +565,14 @@ __device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) 
 }
 
 // A team of tw warps owns whole units (team k takes the CTA's units k,
-// k + nteams, ...).  Per unit the team's first warp writes the pair tables
-// and the screened coordinates into one of the team's two buffers; then
-// thread tt reads WPT 4-byte code words (16 channels each) of every screened
-// coordinate record straight into registers, a batch of kU pairs ahead of
-// the one being summed, two coordinates per table read.  The team's warps
-// meet once per unit (named barrier); a warp publishes a unit once the next
-// one is computed, so the fence finds the stores long done.
+// k + nteams, ...).  Per unit the team's first warp writes the pair tables,
+// the screened coordinates and the expert id into one of two unit buffers.
+// The unit's coordinate records are copied into shared memory in chunks of
+// cc positions with asynchronous 16-byte copies, chunk j + 1 in flight while
+// chunk j is summed.  Thread tt owns WPT 4-byte code words of every record
+// (16 channels each) and sums them in registers, two coordinates per table
+// read.  A warp publishes a unit once the next one is computed, so the
+// fence finds the stores long done.
 template <int WPT>
 __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int tt) {
   const Dims& d = P.d;
@@ -567,9 +581,10 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   const int TT = 32 * sp.tw, R16 = d.I / 16, W4 = 2 * R16;
   const int units = P.B * d.topk * d.nb, nctas = gridDim.x;
   const uint32_t S2 = 2u * (uint32_t)d.S;
-  const int np = (d.c + 1) >> 1;
-  constexpr int kU = WPT == 1 ? 6 : (WPT == 2 ? 2 : 1);   // pairs per load batch
+  const int P16 = (int)(S2 / 16);                // 16-byte pieces per record
   volatile int* flag = reinterpret_cast<volatile int*>(tsm);   // [0] ok, [2 + n % 2] expert id
+  unsigned char* ubuf = tsm + 128;                              // [2][buf_bytes]
+  unsigned char* stage = ubuf + 2 * (size_t)sp.buf_bytes;       // [2][stage_bytes]
   uint32_t off[WPT];
   int gv[WPT], jw[WPT];
   bool has[WPT];
@@ -581,10 +596,11 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     jw[x] = has[x] ? w % R16 : 0;
     off[x] = (uint32_t)(gv[x] * d.S + jw[x] * 4);
   }
-  if (blockIdx.x + team * nctas >= units) return;   // no unit for this team
+  auto unit_of = [&](int n) { return blockIdx.x + (team + n * sp.nteams) * nctas; };
+  if (unit_of(0) >= units) return;               // no unit for this team
   if (tt == 0)
     flag[0] = wait_at_least(P.sync + kSyncRot, (uint32_t)(P.B * d.nb), P.sync + kSyncAbort, P.err);
-  // the first warp keeps the next unit's list in registers
+  // the first warp keeps a unit's list in registers until it writes its buffer
   uint32_t cl = 0;
   float4 rs = make_float4(0.f, 0.f, 0.f, 0.f);
   int enext = 0;
@@ -595,88 +611,129 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     rs = __ldcg(reinterpret_cast<const float4*>(P.rsel) + row);
     enext = __ldcg(P.ids_ws + ts);
   };
-  team_sync(team, TT);
-  if (!flag[0]) return;
-  if (tw_i == 0) load_list(blockIdx.x + team * nctas);
-  int pend = -1;
-  for (int ul = team, n = 0;; ul += sp.nteams, ++n) {
-    const int u = blockIdx.x + ul * nctas;
-    if (u >= units) break;
-    unsigned char* buf = tsm + 128 + (size_t)(n & 1) * sp.buf_bytes;
-    if (tw_i == 0) {
-      // pair tables: lane l holds list positions 4l .. 4l+3, i.e. pairs 2l, 2l+1
-      const float rv[4] = {rs.x, rs.y, rs.z, rs.w};
+  auto write_unit = [&](int n) {   // first warp: unit n's tables, coordinates and expert
+    unsigned char* buf = ubuf + (size_t)(n & 1) * sp.buf_bytes;
+    const float rv[4] = {rs.x, rs.y, rs.z, rs.w};
+    // pair tables: lane l holds list positions 4l .. 4l+3, i.e. pairs 2l, 2l+1
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int p = 4 * lane + 2 * h;
-        if (p < d.c) {
-          const float r0 = rv[2 * h], r1 = p + 1 < d.c ? rv[2 * h + 1] : 0.f;
-          float4* tab = reinterpret_cast<float4*>(buf) + (p >> 1) * 4;
+    for (int h = 0; h < 2; ++h) {
+      const int p = 4 * lane + 2 * h;
+      if (p < d.c) {
+        const float r0 = rv[2 * h], r1 = p + 1 < d.c ? rv[2 * h + 1] : 0.f;
+        float4* tab = reinterpret_cast<float4*>(buf) + (p >> 1) * 4;
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            const float t1 = g4 == 1 ? r1 : (g4 == 3 ? -r1 : 0.f);   // code of the odd position
-            tab[g4] = make_float4(t1, r0 + t1, t1, t1 - r0);         // even position 00 01 10 11
-          }
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const float t1 = g4 == 1 ? r1 : (g4 == 3 ? -r1 : 0.f);   // code of the odd position
+          tab[g4] = make_float4(t1, r0 + t1, t1, t1 - r0);         // even position 00 01 10 11
         }
       }
-      // coordinates; an odd count's spare position repeats the last one
-      uint32_t c4 = cl;
-      if ((d.c & 1) && (d.c >> 2) == lane) {
-        const int v = d.c & 3;
-        const uint32_t lastc = (c4 >> (8 * (v - 1))) & 0xffu;
-        c4 = (c4 & ~(0xffu << (8 * v))) | (lastc << (8 * v));
+    }
+    reinterpret_cast<uint32_t*>(buf + sp.coord_off)[lane] = cl;
+    if (lane == 0) {
+      int e = enext;
+      flag[2 + (n & 1)] = (e < 0 || e >= d.E) ? 0 : e;
+    }
+  };
+  // asynchronous copies of chunk j (unit j / nch, chunk j % nch) into stage j % 2
+  auto issue = [&](int j) {
+    const int n = j / sp.nch, ch = j % sp.nch;
+    const int u = unit_of(n);
+    if (u < units) {
+      const unsigned char* buf = ubuf + (size_t)(n & 1) * sp.buf_bytes;
+      const uint8_t* coords = buf + sp.coord_off;
+      const int b = u % d.nb, e = flag[2 + (n & 1)];
+      const uint8_t* rec = P.codes + ((size_t)e * d.nb + b) * kBlock * S2;
+      const int p0 = ch * sp.cc, npos = min(sp.cc, d.c - p0);
+      const uint32_t dst0 = smem_addr(stage + (size_t)(j & 1) * sp.stage_bytes);
+      const int pieces = npos * P16;
+      int p = tt / P16, o = tt % P16;
+      const int dp = TT / P16, dq = TT % P16;
+      for (int q = tt; q < pieces; q += TT) {
+        const uint8_t* src = rec + (size_t)coords[p0 + p] * S2 + 16 * o;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + (uint32_t)p * S2 + 16u * o),
+                     "l"(src)
+                     : "memory");
+        p += dp;
+        o += dq;
+        if (o >= P16) {
+          o -= P16;
+          ++p;
+        }
       }
-      reinterpret_cast<uint32_t*>(buf + sp.coord_off)[lane] = c4;
-      if (lane == 0) flag[2 + (n & 1)] = enext;
-      const int un = u + sp.nteams * nctas;
-      if (un < units) load_list(un);   // in flight while this unit is summed
     }
-    team_sync(team, TT);
-    int e = flag[2 + (n & 1)];
-    if (e < 0 || e >= d.E) e = 0;
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  team_sync(team, TT);
+  if (!flag[0]) return;
+  if (tw_i == 0) {
+    load_list(unit_of(0));
+    write_unit(0);
+    if (unit_of(1) < units) load_list(unit_of(1));
+  }
+  team_sync(team, TT);
+  issue(0);
+  float acc[WPT][16];
+  uint4 al[WPT][2];
+  int pend = -1;
+  for (int j = 0;; ++j) {
+    const int n = j / sp.nch, ch = j % sp.nch;
+    const int u = unit_of(n);
+    if (u >= units) break;
+    team_sync(team, TT);   // chunk j - 1 is summed by everyone: its stage and unit buffer are free
+    if (ch == 0 && tw_i == 0 && unit_of(n + 1) < units) {
+      write_unit(n + 1);
+      if (unit_of(n + 2) < units) load_list(unit_of(n + 2));   // in flight while unit n is summed
+    }
+    if (ch == 0) team_sync(team, TT);   // unit n + 1's buffer is written
+    issue(j + 1);
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    team_sync(team, TT);   // every thread's copies of chunk j have landed
+    const int e = flag[2 + (n & 1)];
     const int ts = u / d.nb, b = u % d.nb;
-    const uint8_t* rec = P.codes + ((size_t)e * d.nb + b) * kBlock * S2;
-    const uint32_t lut0 = smem_addr(buf);
-    const uint16_t* cpair = reinterpret_cast<const uint16_t*>(buf + sp.coord_off);
-    // alpha of the thread's channels, requested now, used at the end
-    uint4 al[WPT][2];
+    // alpha of the thread's channels: requested with the first chunk when
+    // registers allow, else after the last
+    constexpr bool kAlphaEarly = WPT < 3;
+    auto load_alpha = [&]() {
 #pragma unroll
-    for (int x = 0; x < WPT; ++x) {
-      const uint4* a4 = reinterpret_cast<const uint4*>(
-          P.scales + (((size_t)e * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
-      al[x][0] = has[x] ? ldg_nc4(a4) : make_uint4(0u, 0u, 0u, 0u);
-      al[x][1] = has[x] ? ldg_nc4(a4 + 1) : make_uint4(0u, 0u, 0u, 0u);
+      for (int x = 0; x < WPT; ++x) {
+        const uint4* a4 = reinterpret_cast<const uint4*>(
+            P.scales + (((size_t)e * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
+        al[x][0] = has[x] ? ldg_nc4(a4) : make_uint4(0u, 0u, 0u, 0u);
+        al[x][1] = has[x] ? ldg_nc4(a4 + 1) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    if (ch == 0) {
+#pragma unroll
+      for (int x = 0; x < WPT; ++x)
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[x][q] = 0.f;
+      if (kAlphaEarly) load_alpha();
     }
-    float acc[WPT][16];
-#pragma unroll
-    for (int x = 0; x < WPT; ++x)
-#pragma unroll
-      for (int q = 0; q < 16; ++q) acc[x][q] = 0.f;
-    uint32_t wa[2][kU][WPT], wb[2][kU][WPT];
-    auto issue = [&](int pp0, uint32_t (&ra)[kU][WPT], uint32_t (&rb)[kU][WPT]) {
+    const uint32_t stg = smem_addr(stage + (size_t)(j & 1) * sp.stage_bytes);
+    const uint32_t lut0 = smem_addr(ubuf + (size_t)(n & 1) * sp.buf_bytes) + 64u * (uint32_t)(ch * sp.cc / 2);
+    const int npos = min(sp.cc, d.c - ch * sp.cc), np = (npos + 1) >> 1;
+    constexpr int kU = WPT == 3 ? 1 : 4;   // pairs per shared-memory load batch
+    for (int pp0 = 0; pp0 < np; pp0 += kU) {
+      uint32_t wa[kU][WPT], wb[kU][WPT];
 #pragma unroll
       for (int v = 0; v < kU; ++v) {
         const int pp = pp0 + v;
-        const uint32_t cp = pp < np ? cpair[pp] : 0u;
-        const uint8_t* ra_p = rec + (size_t)(cp & 0xffu) * S2;
-        const uint8_t* rb_p = rec + (size_t)(cp >> 8) * S2;
 #pragma unroll
         for (int x = 0; x < WPT; ++x) {
+          // an odd count's last pair reads a spare record slot (its table ignores it)
           const bool in = pp < np && has[x];
-          ra[v][x] = in ? ldg_nc1(ra_p + off[x]) : 0u;
-          rb[v][x] = in ? ldg_nc1(rb_p + off[x]) : 0u;
+          wa[v][x] = in ? lds_u32(stg + (uint32_t)(2 * pp) * S2 + off[x]) : 0u;
+          wb[v][x] = in ? lds_u32(stg + (uint32_t)(2 * pp + 1) * S2 + off[x]) : 0u;
         }
       }
-    };
-    auto sum = [&](int pp0, const uint32_t (&ra)[kU][WPT], const uint32_t (&rb)[kU][WPT]) {
 #pragma unroll
       for (int v = 0; v < kU; ++v) {
         const uint32_t lb = lut0 + 64u * (uint32_t)min(pp0 + v, np - 1);   // index 0 of a table is 0
 #pragma unroll
         for (int x = 0; x < WPT; ++x) {
           // nibble mm: (even-position code) | (odd-position code) << 2 of channel 2mm / 2mm+1
-          const uint32_t ze = (ra[v][x] & 0x33333333u) | ((rb[v][x] << 2) & 0xCCCCCCCCu);
-          const uint32_t zo = ((ra[v][x] >> 2) & 0x33333333u) | (rb[v][x] & 0xCCCCCCCCu);
+          const uint32_t ze = (wa[v][x] & 0x33333333u) | ((wb[v][x] << 2) & 0xCCCCCCCCu);
+          const uint32_t zo = ((wa[v][x] >> 2) & 0x33333333u) | (wb[v][x] & 0xCCCCCCCCu);
 #pragma unroll
           for (int mm = 0; mm < 8; ++mm) {
             acc[x][2 * mm] += lut_entry(lb, ze, mm);
@@ -684,15 +741,9 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
           }
         }
       }
-    };
-    issue(0, wa[0], wb[0]);
-    for (int pp0 = 0; pp0 < np; pp0 += 2 * kU) {
-      if (pp0 + kU < np) issue(pp0 + kU, wa[1], wb[1]);
-      sum(pp0, wa[0], wb[0]);
-      if (pp0 + kU >= np) break;
-      if (pp0 + 2 * kU < np) issue(pp0 + 2 * kU, wa[0], wb[0]);
-      sum(pp0 + kU, wa[1], wb[1]);
     }
+    if (ch != sp.nch - 1) continue;
+    if (!kAlphaEarly) load_alpha();
     if (pend >= 0) publish_unit(P, pend, lane);
 #pragma unroll
     for (int x = 0; x < WPT; ++x) {
@@ -713,6 +764,7 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     }
     pend = ts;
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
   if (pend >= 0) publish_unit(P, pend, lane);
 }
 
