@@ -147,6 +147,13 @@ def max_over_ranks(value, world):
     return float(t.item())
 
 
+def job_throughput(tokens_per_step, steps, elapsed_ms, world):
+    """Whole-job rate of N independent replicas: every rank decodes the same
+    fixed work, the job ends when the slowest rank does (max over ranks)."""
+    slowest_ms = max_over_ranks(elapsed_ms, world)
+    return tokens_per_step * steps * world / (slowest_ms / 1000.0), slowest_ms
+
+
 # ---------------------------------------------------------------------------
 # the oracle on host cores (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
@@ -382,9 +389,8 @@ def run_ours(args, wl, world, rank, local):
     elapsed_ms = t_start.elapsed_time(t_end)
     per_b_ms = {B: sum(per_b_events[i][bi][0].elapsed_time(per_b_events[i][bi][1])
                        for i in range(args.steps)) for bi, B in enumerate(batches)}
-    elapsed_ms = max_over_ranks(elapsed_ms, world)
     tokens_per_step = L * sum(batches)
-    value = tokens_per_step * args.steps * world / (elapsed_ms / 1000.0)
+    value, elapsed_ms = job_throughput(tokens_per_step, args.steps, elapsed_ms, world)
 
     # -- per-phase device time (profiling events inside fresh graphs of set 0)
     for rd in readers:
