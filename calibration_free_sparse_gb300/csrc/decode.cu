@@ -135,16 +135,10 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-// L2 eviction policies: streamed-once weights go first, the kept transposed
-// down rows (read again by the output phase) stay.
+// L2 eviction policy for rows read once: they go first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t pol;
-  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 __device__ __forceinline__ uint4 ldg_nc4_hint(const void* p, uint64_t pol) {
@@ -160,12 +154,6 @@ __device__ __forceinline__ uint4 ldcg4_hint(const void* p, uint64_t pol) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p), "l"(pol));
   return r;
-}
-// whole-row L2 prefetch (16-byte aligned address, size a multiple of 16)
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes, uint64_t pol) {
-  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes),
-               "l"(pol)
-               : "memory");
 }
 
 __device__ __forceinline__ uint4 ldg_nc4(const void* p) {
@@ -848,9 +836,6 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane) {
   const int slot = n / d.I, i = n % d.I;
   const int e = __ldcg(P.ids_ws + t * d.topk + slot);
   const size_t row = (size_t)e * d.I + i;
-  // the output phase reads this channel's transposed down row in 32-byte
-  // pieces from many CTAs: bring the whole row into L2 now, to stay there
-  if (lane == 0) bulk_prefetch_l2(P.Dt + row * d.H, 2u * (uint32_t)d.H, policy_evict_last());
   const uint64_t pol = policy_evict_first();
   const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
   const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
