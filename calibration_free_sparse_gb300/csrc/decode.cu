@@ -633,19 +633,30 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
       const uint8_t* rec = P.codes + ((size_t)e * d.nb + b) * kBlock * S2;
       const int p0 = ch * sp.cc, npos = min(sp.cc, d.c - p0);
       const uint32_t dst0 = smem_addr(stage + (size_t)(j & 1) * sp.stage_bytes);
-      const int pieces = npos * P16;
-      int p = tt / P16, o = tt % P16;
-      const int dp = TT / P16, dq = TT % P16;
-      for (int q = tt; q < pieces; q += TT) {
-        const uint8_t* src = rec + (size_t)coords[p0 + p] * S2 + 16 * o;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + (uint32_t)p * S2 + 16u * o),
-                     "l"(src)
-                     : "memory");
-        p += dp;
-        o += dq;
-        if (o >= P16) {
-          o -= P16;
-          ++p;
+      if (TT % P16 == 0) {
+        // every thread keeps one 16-byte piece offset: records tt / P16, + TT / P16, ...
+        const int o = tt % P16, dp = TT / P16;
+        const uint32_t dst_o = dst0 + 16u * (uint32_t)o;
+        const uint8_t* src_o = rec + 16 * o;
+        for (int p = tt / P16; p < npos; p += dp)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_o + (uint32_t)p * S2),
+                       "l"(src_o + (size_t)coords[p0 + p] * S2)
+                       : "memory");
+      } else {
+        const int pieces = npos * P16;
+        int p = tt / P16, o = tt % P16;
+        const int dp = TT / P16, dq = TT % P16;
+        for (int q = tt; q < pieces; q += TT) {
+          const uint8_t* src = rec + (size_t)coords[p0 + p] * S2 + 16 * o;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + (uint32_t)p * S2 + 16u * o),
+                       "l"(src)
+                       : "memory");
+          p += dp;
+          o += dq;
+          if (o >= P16) {
+            o -= P16;
+            ++p;
+          }
         }
       }
     }
