@@ -67,9 +67,9 @@ struct Allocs {
 void free_handle_memory(moe_reader* h) {
   if (!h) return;
   if (h->p.codes) cudaFree(h->p.codes);   // start of the prepared block
-  if (h->ws.rsel) cudaFree(h->ws.rsel);   // start of the workspace block
+  if (h->ws.mask) cudaFree(h->ws.mask);   // start of the workspace block
   h->p.codes = nullptr;
-  h->ws.rsel = nullptr;
+  h->ws.mask = nullptr;
 }
 
 int cuda_status(cudaError_t e) {
@@ -228,8 +228,6 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   // ---- decode workspace ----
   const size_t Bm = (size_t)d.Bmax;
   Arena wa;
-  const size_t w_rsel = wa.take(Bm * d.Hp * 4);
-  const size_t w_clist = wa.take(Bm * d.Hp);
   const size_t w_mask = wa.take(Bm * d.nb * 16);
   const size_t w_ids = wa.take(Bm * d.topk * 4);
   const size_t w_w = wa.take(Bm * d.topk * 4);
@@ -263,8 +261,6 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
     return MOE_READER_ENOMEM;
   }
   char* wb = static_cast<char*>(wbase);
-  h->ws.rsel = reinterpret_cast<float*>(wb + w_rsel);
-  h->ws.clist = reinterpret_cast<uint8_t*>(wb + w_clist);
   h->ws.mask = reinterpret_cast<uint32_t*>(wb + w_mask);
   h->ws.ids = reinterpret_cast<int32_t*>(wb + w_ids);
   h->ws.w = reinterpret_cast<float*>(wb + w_w);

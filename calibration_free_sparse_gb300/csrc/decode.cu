@@ -38,7 +38,8 @@ struct ScreenPlan {
   int wpt;           // 4-byte code words per thread (16 channels each)
   int tw;            // warps per team
   int nteams;        // teams side by side (at most 15: one named barrier each)
-  int coord_off;     // within a unit buffer: the coordinates after the pair tables
+  int coord_off;     // within a unit buffer: the coordinates [128] u8 after the pair
+                     // tables, then the screened Rx values [128] fp32
   int buf_bytes;     // one unit buffer
   int cc;            // list positions per copy chunk (even unless one chunk holds the list)
   int nch;           // chunks per unit
@@ -67,7 +68,7 @@ ScreenPlan screen_plan(const Dims& d) {
   }
   if (best == 0.0) return sp;
   sp.coord_off = (int)round_up(64 * (size_t)((d.c + 1) / 2), 128);
-  sp.buf_bytes = sp.coord_off + 128;
+  sp.buf_bytes = sp.coord_off + 128 + 4 * kBlock;   // + the screened Rx values in list order
   const size_t S2 = 2 * (size_t)d.S;
   const size_t per_team = kSmemBudget / sp.nteams / 128 * 128;
   const size_t fixed = 128 + 2 * (size_t)sp.buf_bytes;
@@ -118,8 +119,6 @@ struct Params {
   unsigned long long* stamps;   // [grid][5] phase timestamps, or null
   uint32_t* sync;
   uint32_t* err;
-  uint8_t* clist;               // [Bmax][nb][128] screened coordinates, ascending
-  float* rsel;                  // [Bmax][nb][128] their fp32 Rx values, same order
   ScreenPlan sp;
 };
 
@@ -194,31 +193,16 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   o.total = o.out + d.Bmax * ((d.H + 255) / 256);
   return o;
 }
-constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2, kSyncRot = 3;
+constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2;
 
 // ------------------------------- phase 0 -----------------------------------
-__device__ void rotate_item(const Params& P, int t, int b, int lane) {
+// Rotation and screen selection of one (token, 128-block) by one warp: lane
+// l ends with Rx of coordinates l + 32 s (s < 4) in u[s] and with word[s] =
+// the selection bits of coordinates 32 s .. 32 s + 31 (the c largest |Rx|,
+// ties to the lower coordinate).  rotate_load reads sigma x (true: x held a
+// NaN or an infinity); rotate_select_loaded does the rest.
+__device__ __forceinline__ bool rotate_load(const Params& P, int t, int b, int lane, float (&u)[4]) {
   const Dims& d = P.d;
-  uint32_t* err = P.err;
-  if (b == 0) {
-    for (int s = lane; s < d.topk; s += 32) {
-      int e = P.ids_in[t * d.topk + s];
-      const float wv = P.w_in[t * d.topk + s];
-      uint32_t bits = 0;
-      if (e < 0 || e >= d.E) {
-        bits |= kErrExpertRange;
-        e = 0;
-      }
-      for (int s2 = 0; s2 < s; ++s2)
-        if (P.ids_in[t * d.topk + s2] == P.ids_in[t * d.topk + s]) bits |= kErrExpertDup;
-      if (!(wv >= 0.f) || !isfinite(wv)) bits |= kErrWeight;
-      if (bits) atomicOr(err, bits);
-      P.ids_ws[t * d.topk + s] = e;
-      P.w_ws[t * d.topk + s] = wv;
-    }
-    for (int j = lane; j < d.r; j += 32) P.cvec[(size_t)t * d.r + j] = 0.f;
-  }
-  float u[4];
   bool bad = false;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
@@ -227,7 +211,12 @@ __device__ void rotate_item(const Params& P, int t, int b, int lane) {
     bad |= !isfinite(xv);
     u[s] = P.sigma[col] < 0 ? -xv : xv;
   }
-  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrXNonFinite);
+  return bad;
+}
+
+// u[s] = sigma x of coordinate lane + 32 s on entry (from rotate_load), Rx on exit.
+__device__ void rotate_select_loaded(const Params& P, int lane, float (&u)[4], uint32_t (&word)[4]) {
+  const Dims& d = P.d;
   // Sylvester butterfly, strides 1, 2, ..., 64; pair (i, i+h) -> (a + b, a - b) in fp32
 #pragma unroll
   for (int h = 1; h < 32; h <<= 1) {
@@ -264,28 +253,16 @@ __device__ void rotate_item(const Params& P, int t, int b, int lane) {
   const uint32_t below = (1u << lane) - 1u;
   int before = 0;
   const float inv = 0.08838834764831845f;   // 1/sqrt(128) rounded to fp32
-  // the screened list in ascending coordinate order, with its Rx values
-  const size_t row = ((size_t)t * d.nb + b) * kBlock;
-  int listed = 0;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const uint32_t eqb = __ballot_sync(0xffffffffu, m[s] == T);
     const bool sel = m[s] > T || (m[s] == T && before + __popc(eqb & below) < need);
     before += __popc(eqb);
-    const uint32_t word = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) P.mask[((size_t)t * d.nb + b) * 4 + s] = word;
-    const int pos = listed + __popc(word & below);
-    if (sel && pos < kBlock) {
-      P.clist[row + pos] = (uint8_t)(lane + 32 * s);
-      P.rsel[row + pos] = u[s] * inv;
-    }
-    listed += __popc(word);
+    word[s] = __ballot_sync(0xffffffffu, sel);
+    u[s] *= inv;
   }
-  __syncwarp();
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) atomicAdd(P.sync + kSyncRot, 1u);
 }
+
 
 // ------------------------------- top-k -------------------------------------
 // k-th largest key among the entries keyfn accepts; per-warp histograms.
@@ -570,7 +547,7 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   const int units = P.B * d.topk * d.nb, nctas = gridDim.x;
   const uint32_t S2 = 2u * (uint32_t)d.S;
   const int P16 = (int)(S2 / 16);                // 16-byte pieces per record
-  volatile int* flag = reinterpret_cast<volatile int*>(tsm);   // [0] ok, [2 + n % 2] expert id
+  volatile int* flag = reinterpret_cast<volatile int*>(tsm);   // [2 + n % 2] expert id of unit n
   unsigned char* ubuf = tsm + 128;                              // [2][buf_bytes]
   unsigned char* stage = ubuf + 2 * (size_t)sp.buf_bytes;       // [2][stage_bytes]
   uint32_t off[WPT];
@@ -586,22 +563,69 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   }
   auto unit_of = [&](int n) { return blockIdx.x + (team + n * sp.nteams) * nctas; };
   if (unit_of(0) >= units) return;               // no unit for this team
-  if (tt == 0)
-    flag[0] = wait_at_least(P.sync + kSyncRot, (uint32_t)(P.B * d.nb), P.sync + kSyncAbort, P.err);
-  // the first warp keeps a unit's list in registers until it writes its buffer
-  uint32_t cl = 0;
-  float4 rs = make_float4(0.f, 0.f, 0.f, 0.f);
+  // The first warp rotates and screens the unit's (token, block) itself, so
+  // the team waits on no other CTA; it keeps the next unit's sigma x (and the
+  // expert id) in registers until it writes that unit's buffer.
+  float xu[4] = {0.f, 0.f, 0.f, 0.f};
   int enext = 0;
+  bool xbad = false;
   auto load_list = [&](int uu) {
     const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
-    const size_t row = ((size_t)t * d.nb + b) * 32 + lane;
-    cl = __ldcg(reinterpret_cast<const uint32_t*>(P.clist) + row);
-    rs = __ldcg(reinterpret_cast<const float4*>(P.rsel) + row);
-    enext = __ldcg(P.ids_ws + ts);
+    xbad = rotate_load(P, t, b, lane, xu);
+    enext = P.ids_in[ts];
   };
   auto write_unit = [&](int n) {   // first warp: unit n's tables, coordinates and expert
     unsigned char* buf = ubuf + (size_t)(n & 1) * sp.buf_bytes;
-    const float rv[4] = {rs.x, rs.y, rs.z, rs.w};
+    uint8_t* cbuf = buf + sp.coord_off;
+    float* rbuf = reinterpret_cast<float*>(cbuf + 128);
+    const int uu = unit_of(n), b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk, slot = ts % d.topk;
+    uint32_t word[4];
+    rotate_select_loaded(P, lane, xu, word);
+    // the unit's side outputs: the block's screened set (the same from every
+    // slot), the input checks, and at block 0 the slot's sanitised expert id
+    // and weight (and, for slot 0, the token's zeroed recovery vector); the
+    // warp's unit publication orders them before every later reader
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4)
+      if (lane == s4) P.mask[((size_t)t * d.nb + b) * 4 + s4] = word[s4];
+    if (slot == 0 && __any_sync(0xffffffffu, xbad) && lane == 0) atomicOr(P.err, kErrXNonFinite);
+    if (b == 0) {
+      if (lane == 0) {
+        int e = P.ids_in[ts];
+        const float wv = P.w_in[ts];
+        uint32_t bits = 0;
+        if (e < 0 || e >= d.E) {
+          bits |= kErrExpertRange;
+          e = 0;
+        }
+        for (int s2 = 0; s2 < slot; ++s2)
+          if (P.ids_in[t * d.topk + s2] == P.ids_in[ts]) bits |= kErrExpertDup;
+        if (!(wv >= 0.f) || !isfinite(wv)) bits |= kErrWeight;
+        if (bits) atomicOr(P.err, bits);
+        P.ids_ws[ts] = e;
+        P.w_ws[ts] = wv;
+      }
+      if (slot == 0)
+        for (int j = lane; j < d.r; j += 32) P.cvec[(size_t)t * d.r + j] = 0.f;
+    }
+    // the screened list in ascending coordinate order; an odd count's spare
+    // position repeats the last coordinate
+    const uint32_t below = (1u << lane) - 1u;
+    int listed = 0;
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+      if ((word[s4] >> lane) & 1u) {
+        const int pos = listed + __popc(word[s4] & below);
+        cbuf[pos] = (uint8_t)(lane + 32 * s4);
+        rbuf[pos] = xu[s4];
+        if (pos == d.c - 1 && (d.c & 1)) cbuf[d.c] = (uint8_t)(lane + 32 * s4);
+      }
+      listed += __popc(word[s4]);
+    }
+    __syncwarp();
+    float rv[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) rv[v] = 4 * lane + v < d.c ? rbuf[4 * lane + v] : 0.f;
     // pair tables: lane l holds list positions 4l .. 4l+3, i.e. pairs 2l, 2l+1
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -616,7 +640,6 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
         }
       }
     }
-    reinterpret_cast<uint32_t*>(buf + sp.coord_off)[lane] = cl;
     if (lane == 0) {
       int e = enext;
       flag[2 + (n & 1)] = (e < 0 || e >= d.E) ? 0 : e;
@@ -662,8 +685,6 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  team_sync(team, TT);
-  if (!flag[0]) return;
   if (tw_i == 0) {
     load_list(unit_of(0));
     write_unit(0);
@@ -1105,19 +1126,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   unsigned long long* stamp = P.stamps ? P.stamps + (size_t)blockIdx.x * 5 : nullptr;
   if (stamp && threadIdx.x == 0) stamp[0] = globaltimer();
 
-  // phase 0: rotations, one warp per (token, block), spread over CTAs first
-  {
-    const int items = P.B * d.nb;
-    for (int it = blockIdx.x + nctas * warp; it < items; it += nctas * kWarps)
-      rotate_item(P, it / d.nb, it % d.nb, lane);
-  }
-  if (stamp) {
-    __syncthreads();
-    if (threadIdx.x == 0) stamp[1] = globaltimer();
-  }
-  // phase 1a: screen units, computed by teams of warps
+  // phase 1a: screen units (rotation, selection and sketch sums), computed by teams of warps
   screen_compute(P, smem, warp);
   __syncthreads();
+  if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
   // phase 1b: scoring tasks, then 1c: top-k tasks, spread over the CTAs
   {
     int* flag = reinterpret_cast<int*>(smem);
@@ -1201,7 +1213,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     }
     if (threadIdx.x == 0) {
       P.sync[kSyncExact] = 0u;
-      P.sync[kSyncRot] = 0u;
       P.sync[kSyncDone] = 0u;
     }
   }
@@ -1275,8 +1286,6 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
   P.bco = h.p.b;
   P.ids_ws = ws.ids;
   P.w_ws = ws.w;
-  P.clist = ws.clist;
-  P.rsel = ws.rsel;
   P.mask = ws.mask;
   P.partial = ws.partial;
   P.ghat = ws.ghat;

@@ -36,8 +36,6 @@ struct Dims {
 
 // Decode workspace (device), sized for Bmax tokens.
 struct Workspace {
-  float* rsel;          // [Bmax][nb][128] fp32 Rx of the screened coordinates, ascending order
-  uint8_t* clist;       // [Bmax][nb][128] the screened coordinates, ascending
   uint32_t* mask;       // [Bmax][nb][4]  screened coordinates
   int32_t* ids;         // [Bmax][topk]   sanitized expert ids
   float* w;             // [Bmax][topk]   routing weights

@@ -29,7 +29,7 @@ EXPORTED_SYMBOLS = (
     "moe_reader_get_info", "moe_reader_destroy", "moe_reader_strerror", "moe_reader_abi_version",
     "moe_reader_set_profiling", "moe_reader_read_profile", "moe_reader_topk_noalloc",
 )
-PHASES = ("decode", "rotate", "screen_topk", "exact", "out")
+PHASES = ("decode", "screen", "score_topk", "exact", "out")
 
 
 class ReaderError(RuntimeError):

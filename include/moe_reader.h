@@ -213,8 +213,8 @@ int moe_reader_get_info(moe_reader_t* h, moe_reader_info* out);
  * inside a captured CUDA graph), and its phases from globaltimer stamps every
  * CTA writes at the end of each phase.  Phase slots, in order:
  *   0 the whole kernel (events)
- *   1 rotation of x and coordinate selection   (to the last CTA's end)
- *   2 sketch screen, scores and global top-k   (from the end of slot 1)
+ *   1 rotation of x, coordinate selection and sketch screen  (to the last CTA's end)
+ *   2 scores and global top-k                  (from the end of slot 1)
  *   3 exact kept channels and recovery vector  (from the end of slot 2)
  *   4 output                                   (from the end of slot 3)  */
 #define MOE_READER_PHASES 5
