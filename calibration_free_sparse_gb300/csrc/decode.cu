@@ -182,18 +182,19 @@ __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* a
 
 // Offsets (in uint32) of the synchronisation area, fixed per handle.
 struct SyncOff {
-  int slot, tok, flag, out, total;
+  int slot, tok, flag, exact, out, total;
 };
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
   o.slot = 16;
   o.tok = o.slot + d.Bmax * d.topk;
   o.flag = o.tok + d.Bmax;
-  o.out = o.flag + d.Bmax;
+  o.exact = o.flag + d.Bmax;
+  o.out = o.exact + d.Bmax;
   o.total = o.out + d.Bmax * ((d.H + 255) / 256);
   return o;
 }
-constexpr int kSyncDone = 0, kSyncExact = 1, kSyncAbort = 2;
+constexpr int kSyncDone = 0, kSyncAbort = 2;
 
 // ------------------------------- phase 0 -----------------------------------
 // Rotation and screen selection of one (token, 128-block) by one warp: lane
@@ -862,11 +863,35 @@ __device__ __forceinline__ void dot8(const uint4& q, const float4& xa, const flo
 }
 
 
-__device__ void kept_item(const Params& P, int t, int qi, int lane) {
+// Count `count` finished phase-2 items of token pt (pt < 0: none): the items'
+// stores, then the token's counter.  Called right after the next item's first
+// loads are issued, so the fence mostly waits for loads needed anyway.
+__device__ __forceinline__ void publish_item(const Params& P, int pt, int count, int lane) {
+  if (pt < 0) return;
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicAdd(P.sync + sync_offsets(P.d).exact + pt, (uint32_t)count);
+}
+
+// Slot s's sanitised expert id / weight of token t, lane-distributed (topk <= 64).
+__device__ __forceinline__ int slot_expert(int e0, int e1, int slot) {
+  const int a = __shfl_sync(0xffffffffu, e0, slot & 31);
+  const int b = __shfl_sync(0xffffffffu, e1, slot & 31);
+  return slot < 32 ? a : b;
+}
+
+__device__ void kept_item(const Params& P, int t, int qi, int lane, int pend_t, int pend_n) {
   const Dims& d = P.d;
   const int n = __ldcg(P.kept + (size_t)t * d.N + qi);
+  // the token's expert ids, requested beside the kept index
+  const int e0 = lane < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane) : 0;
+  const int e1 = lane + 32 < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane + 32) : 0;
+  const float w0 = lane < d.topk ? __ldcg(P.w_ws + t * d.topk + lane) : 0.f;
+  const float w1 = lane + 32 < d.topk ? __ldcg(P.w_ws + t * d.topk + lane + 32) : 0.f;
+  publish_item(P, pend_t, pend_n, lane);
   const int slot = n / d.I, i = n % d.I;
-  const int e = __ldcg(P.ids_ws + t * d.topk + slot);
+  const int e = slot_expert(e0, e1, slot);
+  const float wslot = __int_as_float(slot_expert(__float_as_int(w0), __float_as_int(w1), slot));
   const size_t row = (size_t)e * d.I + i;
   const uint64_t pol = policy_evict_first();
   const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
@@ -899,12 +924,12 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane) {
   sg = warp_sum(sg);
   sv = warp_sum(sv);
   if (lane == 0) {
-    P.wa[(size_t)t * d.N + qi] = __ldcg(P.w_ws + t * d.topk + slot) * silu_f(sg) * sv;
+    P.wa[(size_t)t * d.N + qi] = wslot * silu_f(sg) * sv;
     P.rowoff[(size_t)t * d.N + qi] = (int32_t)row;
   }
 }
 
-__device__ void recovery_item(const Params& P, int t, int ch, int lane) {
+__device__ void recovery_item(const Params& P, int t, int ch, int lane, int pend_t, int pend_n) {
   // 64 channels: lane l takes channels l and l + 32 (full b rows), then the
   // warp transposes and sums the 32 lane vectors; lane j ends with component j
   const Dims& d = P.d;
@@ -917,6 +942,7 @@ __device__ void recovery_item(const Params& P, int t, int ch, int lane) {
   const bool s0 = !((kb0 >> lane) & 1u), s1 = !((kb1 >> lane) & 1u);
   const float c0 = s0 ? wv * __ldcg(P.p + (size_t)t * d.N + n0 + lane) : 0.f;
   const float c1 = s1 ? wv * __ldcg(P.p + (size_t)t * d.N + n0 + 32 + lane) : 0.f;
+  publish_item(P, pend_t, pend_n, lane);
   const __half* b0 = P.bco + ((size_t)e * d.I + (n0 % d.I) + lane) * d.r;
   const __half* b1 = b0 + (size_t)32 * d.r;
   for (int j0 = 0; j0 < d.r; j0 += 32) {
@@ -1153,49 +1179,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   {
     const long long wtot = (long long)nctas * kWarps;
     const long long gw = (long long)blockIdx.x * kWarps + warp;
-    int cur_t = -1;
-    for (long long q = gw; q < M; q += wtot) {
+    // contiguous runs of items per warp: a warp meets one or two tokens, and
+    // counts its items of a token once it leaves that token
+    const long long ipw = (M + wtot - 1) / wtot;
+    const long long q0 = gw * ipw, q1 = min(M, q0 + ipw);
+    int cur_t = -1, pend_t = -1, pend_n = 0;
+    bool ok = true;
+    for (long long q = q0; q < q1; ++q) {
       const int t = (int)(q / per_tok), local = (int)(q % per_tok);
       if (t != cur_t) {
         int w_ok = 1;
         if (lane == 0) w_ok = wait_at_least(P.sync + so.flag + t, 1u, abort_flag, P.err);
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) break;
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
         __syncwarp();
         cur_t = t;
       }
+      const bool flush = pend_t >= 0 && pend_t != t;   // leaving token pend_t
       if (local < P.k)
-        kept_item(P, t, local, lane);
+        kept_item(P, t, local, lane, flush ? pend_t : -1, pend_n);
       else
-        recovery_item(P, t, local - P.k, lane);
+        recovery_item(P, t, local - P.k, lane, flush ? pend_t : -1, pend_n);
+      if (flush) pend_n = 0;
+      pend_t = t;
+      ++pend_n;
     }
+    if (ok) publish_item(P, pend_t, pend_n, lane);
   }
-  __syncthreads();
-  if (stamp && threadIdx.x == 0) stamp[3] = globaltimer();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    int ok = ld_acquire(abort_flag) == 0u;
-    if (ok) {
-      long long mine = 0;
-      const long long wtot = (long long)nctas * kWarps;
-      for (int w = 0; w < kWarps; ++w) {
-        const long long gw = (long long)blockIdx.x * kWarps + w;
-        if (gw < M) mine += (M - 1 - gw) / wtot + 1;
-      }
-      atomicAdd(P.sync + kSyncExact, (uint32_t)mine);
-      ok = wait_at_least(P.sync + kSyncExact, (uint32_t)M, abort_flag, P.err);
-    }
-    ctl[1] = ok;
+  if (stamp) {
+    __syncthreads();
+    if (threadIdx.x == 0) stamp[3] = globaltimer();
   }
-  __syncthreads();
-  if (!ctl[1]) return;
-  // phase 3: output warp items (token, 256-column block, row chunk)
+  // phase 3: output warp items (token, 256-column block, row chunk); a token's
+  // items start once all of its phase-2 items are counted
   {
     const int nwarps = nctas * kWarps;
     const OutPlan op = out_plan(P, nwarps);
     const int items = P.B * op.ncb * op.NR;
-    for (int it = blockIdx.x + nctas * warp; it < items; it += nwarps)
-      out_chunk(P, op, it / (op.ncb * op.NR), (it / op.NR) % op.ncb, it % op.NR, lane);
+    int ready_t = -1;
+    for (int it = blockIdx.x + nctas * warp; it < items; it += nwarps) {
+      const int t = it / (op.ncb * op.NR);
+      if (t != ready_t) {
+        int w_ok = 1;
+        if (lane == 0)
+          w_ok = wait_at_least(P.sync + so.exact + t, (uint32_t)per_tok, abort_flag, P.err);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
+        __syncwarp();
+        ready_t = t;
+      }
+      out_chunk(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane);
+    }
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
   // the last CTA out resets the synchronisation area for the next call
@@ -1210,9 +1246,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     for (int i = threadIdx.x; i < P.B; i += kThreads) {
       P.sync[so.tok + i] = 0u;
       P.sync[so.flag + i] = 0u;
+      P.sync[so.exact + i] = 0u;
     }
     if (threadIdx.x == 0) {
-      P.sync[kSyncExact] = 0u;
       P.sync[kSyncDone] = 0u;
     }
   }
