@@ -804,8 +804,10 @@ __device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
 }
 
 // Score the channels of one (token, slot) once all its blocks are in: sum
-// the block partials in block order, s = w ||d|| |phi(ghat) vhat|.
-__device__ bool score_task(const Params& P, int ts, int* flag) {
+// the block partials in block order, s = w ||d|| |phi(ghat) vhat|.  Returns
+// -1 on abort, 1 when this was the token's last slot to be scored (the CTA
+// then runs the token's top-k), else 0.
+__device__ int score_task(const Params& P, int ts, int* flag) {
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int t = ts / d.topk, slot = ts % d.topk, I = d.I;
@@ -813,45 +815,70 @@ __device__ bool score_task(const Params& P, int ts, int* flag) {
     *flag = wait_at_least(P.sync + so.slot + ts, (uint32_t)(d.nb * P.sp.tw), P.sync + kSyncAbort,
                           P.err);
   __syncthreads();
-  if (!*flag) return false;
+  if (!*flag) return -1;
   int e = P.ids_in[ts];
   if (e < 0 || e >= d.E) e = 0;
   const float wv = P.w_in[ts];
-  for (int i = threadIdx.x; i < I; i += kThreads) {
-    const float* pg = P.partial + ((size_t)ts * d.nb) * 2 * I + i;
-    float g = 0.f, v = 0.f;
+  const float* pg0 = P.partial + ((size_t)ts * d.nb) * 2 * I;
+  // channels i and i + kThreads together: all their block loads first, then
+  // the sums in block order
+  for (int i = threadIdx.x; i < I; i += 2 * kThreads) {
+    const int i2 = i + kThreads;
+    const bool two = i2 < I;
+    const float dn[2] = {__ldg(P.dnorm + (size_t)e * I + i),
+                         two ? __ldg(P.dnorm + (size_t)e * I + i2) : 0.f};
+    float g[2] = {0.f, 0.f}, v[2] = {0.f, 0.f};
     int bb = 0;
-    for (; bb + 16 <= d.nb; bb += 16) {   // loads first, then the sums in block order
-      float gg[16], vv[16];
+    for (; bb + 16 <= d.nb; bb += 16) {
+      float gg[2][16], vv[2][16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        gg[u] = __ldcg(pg + (size_t)(bb + u) * 2 * I);
-        vv[u] = __ldcg(pg + (size_t)(bb + u) * 2 * I + I);
+        const float* pb = pg0 + (size_t)(bb + u) * 2 * I;
+        gg[0][u] = __ldcg(pb + i);
+        vv[0][u] = __ldcg(pb + I + i);
+        gg[1][u] = two ? __ldcg(pb + i2) : 0.f;
+        vv[1][u] = two ? __ldcg(pb + I + i2) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        g += gg[u];
-        v += vv[u];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          g[h] += gg[h][u];
+          v[h] += vv[h][u];
+        }
       }
     }
     for (; bb < d.nb; ++bb) {
-      g += __ldcg(pg + (size_t)bb * 2 * I);
-      v += __ldcg(pg + (size_t)bb * 2 * I + I);
+      const float* pb = pg0 + (size_t)bb * 2 * I;
+      g[0] += __ldcg(pb + i);
+      v[0] += __ldcg(pb + I + i);
+      if (two) {
+        g[1] += __ldcg(pb + i2);
+        v[1] += __ldcg(pb + I + i2);
+      }
     }
-    const float pv = silu_f(g) * v;
-    const float s = wv * __ldg(P.dnorm + (size_t)e * I + i) * fabsf(pv);
-    const size_t o = (size_t)t * d.N + (size_t)slot * I + i;
-    P.ghat[o] = g;
-    P.vhat[o] = v;
-    P.p[o] = pv;
-    P.score[o] = s;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (h == 1 && !two) break;
+      const int ii = h ? i2 : i;
+      const float pv = silu_f(g[h]) * v[h];
+      const float sc = wv * dn[h] * fabsf(pv);
+      const size_t o = (size_t)t * d.N + (size_t)slot * I + ii;
+      P.ghat[o] = g[h];
+      P.vhat[o] = v[h];
+      P.p[o] = pv;
+      P.score[o] = sc;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    atomicAdd(P.sync + so.tok + t, 1u);
+    const uint32_t prev = atomicAdd(P.sync + so.tok + t, 1u);
+    *flag = prev == (uint32_t)(d.topk - 1);
+    if (*flag) __threadfence();   // every slot's scores are in: read them after this
   }
-  return true;
+  __syncthreads();
+  return *flag ? 1 : 0;
 }
 
 // ------------------------------- phase 2 -----------------------------------
@@ -1156,19 +1183,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   screen_compute(P, smem, warp);
   __syncthreads();
   if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
-  // phase 1b: scoring tasks, then 1c: top-k tasks, spread over the CTAs
+  // phase 1b: scoring tasks spread over the CTAs; the CTA that scores a
+  // token's last slot runs the token's top-k (1c) at once
   {
-    int* flag = reinterpret_cast<int*>(smem);
+    int* flag = &ctl[1];   // static shared memory: the top-k's working area starts at smem
     for (int ts = blockIdx.x; ts < P.B * d.topk; ts += nctas) {
-      if (!score_task(P, ts, flag)) return;
-      __syncthreads();
-    }
-    for (int t = blockIdx.x; t < P.B; t += nctas) {
-      if (threadIdx.x == 0)
-        ctl[1] = wait_at_least(P.sync + so.tok + t, (uint32_t)d.topk, abort_flag, P.err);
-      __syncthreads();
-      if (!ctl[1]) return;
-      topk_token(P, t, smem);
+      const int r = score_task(P, ts, flag);
+      if (r < 0) return;
+      if (r > 0) topk_token(P, ts / d.topk, smem);
       __syncthreads();
     }
   }
