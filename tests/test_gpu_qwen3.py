@@ -63,3 +63,23 @@ def test_decode_parity(pair, B):
     frac = sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")) / st["dense"]
     if B == 1:
         assert abs(frac - 0.187) < 2e-3
+
+
+@pytest.mark.parametrize("zero_slots,k", [(1, 5500), (2, 5000)])
+def test_threshold_inside_tied_scores(pair, zero_slots, k):
+    """Routing weights of 0 give whole slots of equal (zero) scores.  With k
+    inside that group the kept set is decided by the tie rule (lower global id
+    first): 768 tied candidates take the exact candidate ranking, 1536 the
+    radix fallback of the top-k."""
+    B = 2
+    x, ids, w = pair.tokens(B, 300 + zero_slots)
+    w = w.copy()
+    w[:, :zero_slots] = 0.0
+    y = pair.decode_gpu(x, ids, w, k)
+    assert pair.reader.status() == (0, 0)
+    res = R.decode(pair.layer, x, ids, w, k)
+    kept = pair.reader.kept(B, k)
+    for t in range(B):
+        # equal scores leave no near-tie band: the set must be exact
+        assert set(kept[t].tolist()) == set(res[t].kept.tolist())
+        C.assert_y_close(y[t], res[t].y)
