@@ -33,7 +33,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
 // Shared-memory plan of the screen (host-computed, passed to the kernel).
-constexpr size_t kSmemBudget = 226 * 1024 - 128;   // dynamic shared memory: 227 KB less static, slack
+constexpr size_t kSmemBudget = 226 * 1024 - 256;   // dynamic shared memory: 227 KB less static, slack
 struct ScreenPlan {
   int wpt;           // 4-byte code words per thread (16 channels each)
   int tw;            // warps per team
@@ -44,7 +44,7 @@ struct ScreenPlan {
   int cc;            // list positions per copy chunk (even unless one chunk holds the list)
   int nch;           // chunks per unit
   int stage_bytes;   // one chunk stage: cc + 1 records (the spare slot of an odd count)
-  int team_bytes;    // 128-byte flag area, two unit buffers, two chunk stages
+  int team_bytes;    // 256-byte flag area, two unit buffers, two chunk stages
   size_t bytes;      // shared memory of the screen; 0: the shape does not fit
 };
 
@@ -67,19 +67,21 @@ ScreenPlan screen_plan(const Dims& d) {
     }
   }
   if (best == 0.0) return sp;
-  sp.coord_off = (int)round_up(64 * (size_t)((d.c + 1) / 2), 128);
-  sp.buf_bytes = sp.coord_off + 128 + 4 * kBlock;   // + the screened Rx values in list order
+  // everything 256-byte aligned: four 64-byte pair tables share one 256-byte
+  // block, whose base the table reads assemble byte-wise
+  sp.coord_off = (int)round_up(64 * (size_t)((d.c + 1) / 2), 256);
+  sp.buf_bytes = (int)round_up((size_t)sp.coord_off + 128 + 4 * kBlock, 256);   // + Rx in list order
   const size_t S2 = 2 * (size_t)d.S;
-  const size_t per_team = kSmemBudget / sp.nteams / 128 * 128;
-  const size_t fixed = 128 + 2 * (size_t)sp.buf_bytes;
+  const size_t per_team = kSmemBudget / sp.nteams / 256 * 256;
+  const size_t fixed = 256 + 2 * (size_t)sp.buf_bytes;
   for (int nch = 1; nch <= d.c && !sp.cc; ++nch) {
     int c1 = (d.c + nch - 1) / nch;
     if (nch > 1) c1 += c1 & 1;                  // chunks hold whole pairs
-    if (fixed + 2 * round_up((size_t)(c1 + 1) * S2, 128) <= per_team) sp.cc = c1;
+    if (fixed + 2 * round_up((size_t)(c1 + 1) * S2, 256) <= per_team) sp.cc = c1;
   }
   if (!sp.cc) return sp;
   sp.nch = (d.c + sp.cc - 1) / sp.cc;
-  sp.stage_bytes = (int)round_up((size_t)(sp.cc + 1) * S2, 128);
+  sp.stage_bytes = (int)round_up((size_t)(sp.cc + 1) * S2, 256);
   sp.team_bytes = (int)(fixed + 2 * (size_t)sp.stage_bytes);
   sp.bytes = (size_t)sp.nteams * sp.team_bytes;
   return sp;
@@ -503,12 +505,9 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Entry of a 64-byte aligned pair table at shared address `tab` indexed by
-// nibble mm of z (byte offset = nibble * 4, or-ed into the aligned base).
-__device__ __forceinline__ float lut_entry(uint32_t tab, uint32_t z, int mm) {
-  const uint32_t off = mm == 0 ? (z << 2) & 0x3Cu : (z >> (4 * mm - 2)) & 0x3Cu;
+__device__ __forceinline__ float lds_f32(uint32_t a) {
   float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(tab | off));
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
   return v;
 }
 
@@ -549,7 +548,7 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   const uint32_t S2 = 2u * (uint32_t)d.S;
   const int P16 = (int)(S2 / 16);                // 16-byte pieces per record
   volatile int* flag = reinterpret_cast<volatile int*>(tsm);   // [2 + n % 2] expert id of unit n
-  unsigned char* ubuf = tsm + 128;                              // [2][buf_bytes]
+  unsigned char* ubuf = tsm + 256;                              // [2][buf_bytes]
   unsigned char* stage = ubuf + 2 * (size_t)sp.buf_bytes;       // [2][stage_bytes]
   uint32_t off[WPT];
   int gv[WPT], jw[WPT];
@@ -731,7 +730,8 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
       if (kAlphaEarly) load_alpha();
     }
     const uint32_t stg = smem_addr(stage + (size_t)(j & 1) * sp.stage_bytes);
-    const uint32_t lut0 = smem_addr(ubuf + (size_t)(n & 1) * sp.buf_bytes) + 64u * (uint32_t)(ch * sp.cc / 2);
+    const uint32_t lut_base = smem_addr(ubuf + (size_t)(n & 1) * sp.buf_bytes);   // 256-aligned
+    const int pbase = ch * sp.cc / 2;   // the chunk's first pair in the unit's list
     const int npos = min(sp.cc, d.c - ch * sp.cc), np = (npos + 1) >> 1;
     constexpr int kU = WPT == 3 ? 1 : 4;   // pairs per shared-memory load batch
     for (int pp0 = 0; pp0 < np; pp0 += kU) {
@@ -749,16 +749,28 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
       }
 #pragma unroll
       for (int v = 0; v < kU; ++v) {
-        const uint32_t lb = lut0 + 64u * (uint32_t)min(pp0 + v, np - 1);   // index 0 of a table is 0
+        // table of pair pg: 256-byte block pg / 4 (bytes 1-3 of the address),
+        // 64 (pg % 4) + 4 index in the low byte; index 0 of a table is 0
+        const int pg = pbase + min(pp0 + v, np - 1);
+        const uint32_t blk = lut_base + 256u * (uint32_t)(pg >> 2);
+        const uint32_t sub = (uint32_t)(pg & 3) * 0x40404040u;
 #pragma unroll
         for (int x = 0; x < WPT; ++x) {
           // nibble mm: (even-position code) | (odd-position code) << 2 of channel 2mm / 2mm+1
           const uint32_t ze = (wa[v][x] & 0x33333333u) | ((wb[v][x] << 2) & 0xCCCCCCCCu);
           const uint32_t zo = ((wa[v][x] >> 2) & 0x33333333u) | (wb[v][x] & 0xCCCCCCCCu);
+          // byte k: 4 x (nibble 2k or 2k+1) + 64 (pg % 4), i.e. the address's low byte
+          const uint32_t bee = ((ze << 2) & 0x3C3C3C3Cu) | sub;   // channels 4k
+          const uint32_t beo = ((ze >> 2) & 0x3C3C3C3Cu) | sub;   // channels 4k + 2
+          const uint32_t boe = ((zo << 2) & 0x3C3C3C3Cu) | sub;   // channels 4k + 1
+          const uint32_t boo = ((zo >> 2) & 0x3C3C3C3Cu) | sub;   // channels 4k + 3
 #pragma unroll
-          for (int mm = 0; mm < 8; ++mm) {
-            acc[x][2 * mm] += lut_entry(lb, ze, mm);
-            acc[x][2 * mm + 1] += lut_entry(lb, zo, mm);
+          for (int kb = 0; kb < 4; ++kb) {
+            const uint32_t sel = 0x7650u + kb;   // low byte from the index word, the rest from blk
+            acc[x][4 * kb] += lds_f32(__byte_perm(bee, blk, sel));
+            acc[x][4 * kb + 1] += lds_f32(__byte_perm(boe, blk, sel));
+            acc[x][4 * kb + 2] += lds_f32(__byte_perm(beo, blk, sel));
+            acc[x][4 * kb + 3] += lds_f32(__byte_perm(boo, blk, sel));
           }
         }
       }
@@ -1165,10 +1177,10 @@ __device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
 
 // ------------------------------- the kernel --------------------------------
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  // the pair tables are addressed by or-ing offsets into 64-byte aligned
-  // bases: align the working area to 128 bytes whatever the window offset
-  unsigned char* const smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  extern __shared__ __align__(256) unsigned char smem_raw[];
+  // the pair tables are addressed by assembling a 256-byte aligned block base
+  // with a low byte: align the working area to 256 bytes whatever the window offset
+  unsigned char* const smem = smem_raw + ((256u - (smem_addr(smem_raw) & 255u)) & 255u);
   __shared__ int ctl[2];
   if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
@@ -1280,7 +1292,7 @@ size_t decode_smem_bytes(const Dims& d) {
   const size_t screen = screen_plan(d).bytes;
   const size_t topk = topk_smem_bytes(d.N);
   const size_t m = screen > topk ? screen : topk;
-  return m + 128;   // + alignment slack of the working area
+  return m + 256;   // + alignment slack of the working area
 }
 
 }  // namespace
