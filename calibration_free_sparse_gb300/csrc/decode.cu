@@ -165,6 +165,22 @@ __device__ __forceinline__ uint4 ldg_nc4(const void* p) {
   return r;
 }
 
+// Hand-off primitives at GPU scope.  A block (or warp) barrier before a
+// single thread's release makes the whole block's (warp's) earlier writes
+// part of the release; an acquire-release add also orders the caller's
+// later reads after every release it follows.
+__device__ __forceinline__ void red_add_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Wait (one thread) until *flag >= target.  false: timed out or aborted.
 __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* abort_flag,
                               uint32_t* err) {
@@ -488,10 +504,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     pos += __popc(bal);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicExch(&P.sync[sync_offsets(d).flag + t], 1u);
-  }
+  if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], 1u);
 }
 
 // ------------------------------- phase 1 -----------------------------------
@@ -521,12 +534,11 @@ __device__ __forceinline__ void team_sync(int team, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(threads) : "memory");
 }
 
-// Publish a stored unit: the warp's partial stores, then its share of the
-// (token, slot) counter (complete at nb * tw).
+// Publish a stored unit: the warp's partial stores, then (release add) its
+// share of the (token, slot) counter (complete at nb * tw).
 __device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) {
-  __threadfence();
   __syncwarp();
-  if (lane == 0) atomicAdd(P.sync + sync_offsets(P.d).slot + ts, 1u);
+  if (lane == 0) red_add_release(P.sync + sync_offsets(P.d).slot + ts, 1u);
 }
 
 // A team of tw warps owns whole units (team k takes the CTA's units k,
@@ -537,7 +549,7 @@ __device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) 
 // chunk j is summed.  Thread tt owns WPT 4-byte code words of every record
 // (16 channels each) and sums them in registers, two coordinates per table
 // read.  A warp publishes a unit once the next one is computed, so the
-// fence finds the stores long done.
+// release finds the stores long done.
 template <int WPT>
 __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int tt) {
   const Dims& d = P.d;
@@ -884,10 +896,9 @@ __device__ int score_task(const Params& P, int ts, int* flag) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(P.sync + so.tok + t, 1u);
+    // releases this slot's scores; the last slot in also acquires the others'
+    const uint32_t prev = atom_add_acq_rel(P.sync + so.tok + t, 1u);
     *flag = prev == (uint32_t)(d.topk - 1);
-    if (*flag) __threadfence();   // every slot's scores are in: read them after this
   }
   __syncthreads();
   return *flag ? 1 : 0;
@@ -902,14 +913,13 @@ __device__ __forceinline__ void dot8(const uint4& q, const float4& xa, const flo
 }
 
 
-// Count `count` finished phase-2 items of token pt (pt < 0: none): the items'
-// stores, then the token's counter.  Called right after the next item's first
-// loads are issued, so the fence mostly waits for loads needed anyway.
+// Count `count` finished phase-2 items of token pt (pt < 0: none): a release
+// add after the warp's barrier, so the items' stores come first.  Called
+// right after the next item's first loads are issued.
 __device__ __forceinline__ void publish_item(const Params& P, int pt, int count, int lane) {
   if (pt < 0) return;
-  __threadfence();
   __syncwarp();
-  if (lane == 0) atomicAdd(P.sync + sync_offsets(P.d).exact + pt, (uint32_t)count);
+  if (lane == 0) red_add_release(P.sync + sync_offsets(P.d).exact + pt, (uint32_t)count);
 }
 
 // Slot s's sanitised expert id / weight of token t, lane-distributed (topk <= 64).
@@ -1139,15 +1149,13 @@ __device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
   float4* part = reinterpret_cast<float4*>(P.ypart + (blk + rc) * kOutCols + lane * 8);
   part[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   part[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  __threadfence();
   __syncwarp();
   uint32_t* cnt = P.sync + sync_offsets(d).out + t * op.ncb + cb;
   uint32_t prev = 0;
-  if (lane == 0) prev = atomicAdd(cnt, 1u);
+  if (lane == 0) prev = atom_add_acq_rel(cnt, 1u);
   prev = __shfl_sync(0xffffffffu, prev, 0);
   if (prev != (uint32_t)(op.NR - 1)) return;
   // the last chunk in: sum the chunks in order
-  __threadfence();
   float y8[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) y8[u] = 0.f;
