@@ -242,7 +242,6 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_ro = wa.take(Bm * d.N * 4);
   const size_t w_sync = wa.take(mr::sync_words(d) * 4);
   const size_t w_cp = wa.take(Bm * d.r * 4);
-  const size_t w_yp = wa.take(Bm * (size_t)((d.H + 255) / 256) * 32 * 256 * 4);
   const size_t w_xs = wa.take(Bm * d.H * 4);
   const size_t w_ys = wa.take(Bm * d.H * 4);
   const size_t w_is = wa.take(Bm * d.topk * 4);
@@ -275,7 +274,6 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.rowoff = reinterpret_cast<int32_t*>(wb + w_ro);
   h->ws.sync = reinterpret_cast<uint32_t*>(wb + w_sync);
   h->ws.cpart = reinterpret_cast<float*>(wb + w_cp);
-  h->ws.ypart = reinterpret_cast<float*>(wb + w_yp);
   h->ws.x_stage = reinterpret_cast<float*>(wb + w_xs);
   h->ws.y_stage = reinterpret_cast<float*>(wb + w_ys);
   h->ws.ids_stage = reinterpret_cast<int32_t*>(wb + w_is);

@@ -117,7 +117,6 @@ struct Params {
   int32_t* rowoff;
   float* wa;
   float* cvec;                  // [Bmax][r] recovery vectors, accumulated atomically
-  float* ypart;                 // [Bmax][ncb][kOutChunksMax][kOutCols] output partials
   unsigned long long* stamps;   // [grid][5] phase timestamps, or null
   uint32_t* sync;
   uint32_t* err;
@@ -200,7 +199,7 @@ __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* a
 
 // Offsets (in uint32) of the synchronisation area, fixed per handle.
 struct SyncOff {
-  int slot, tok, flag, exact, out, total;
+  int slot, tok, flag, exact, total;
 };
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
@@ -208,8 +207,7 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   o.tok = o.slot + d.Bmax * d.topk;
   o.flag = o.tok + d.Bmax;
   o.exact = o.flag + d.Bmax;
-  o.out = o.exact + d.Bmax;
-  o.total = o.out + d.Bmax * ((d.H + 255) / 256);
+  o.total = o.exact + d.Bmax;
   return o;
 }
 constexpr int kSyncDone = 0, kSyncAbort = 2;
@@ -503,6 +501,8 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     if (lane == 0) P.keptbits[(size_t)t * words + wd] = bal;
     pos += __popc(bal);
   }
+  // the output phase adds its chunks into y[t]: start it from zero
+  for (int h = threadIdx.x; h < d.H; h += kThreads) P.y[(size_t)t * d.H + h] = 0.f;
   __syncthreads();
   if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], 1u);
 }
@@ -1053,7 +1053,6 @@ __device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
 }
 
 constexpr int kOutCols = 256;        // columns of an output block: 8 per lane
-constexpr int kOutChunksMax = 32;    // row chunks per (token, output block)
 constexpr int kOutBatch = 12;        // kept rows whose loads a warp issues together
 
 struct OutPlan {
@@ -1069,8 +1068,8 @@ __device__ __forceinline__ OutPlan out_plan(const Params& P, int nwarps) {
   op.ncb = (P.d.H + kOutCols - 1) / kOutCols;
   const int per = P.B * op.ncb;
   const int rec = P.k < P.d.N ? 1 : 0;
-  int R = nwarps / per - rec;                 // one round of warp items
-  R = min(R, kOutChunksMax - 1);
+  int R = nwarps / per - rec;                 // one round of warp items,
+  R = min(R, (P.k + kOutBatch - 1) / kOutBatch);   // each at least one full load batch
   R = max(1, min(R, P.k));
   op.RC = (P.k + R - 1) / R;
   op.R = op.RC > 0 ? (P.k + op.RC - 1) / op.RC : 1;
@@ -1091,8 +1090,7 @@ __device__ __forceinline__ void axpy8h(float c, const uint4& v, float* acc) {
 // One warp item: columns cb*256 + 8 lane .. +7 of token t over kept rows
 // [rc RC, (rc+1) RC) of Dt, each row read as one coalesced 512-byte piece, or
 // for rc = R the recovery U c as the r rows of U^T weighted by c.  The
-// partial goes to ypart; the warp that completes a (token, block) sums its
-// chunks in chunk order and writes y.
+// partial is added into y with fp32 atomics.
 __device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int rc, int lane) {
   const Dims& d = P.d;
   const int c0 = cb * kOutCols + lane * 8;
@@ -1145,42 +1143,12 @@ __device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
       for (int u = 0; u < kOutBatch; ++u) axpy8(c[u], v[u], acc);
     }
   }
-  const size_t blk = ((size_t)t * op.ncb + cb) * kOutChunksMax;
-  float4* part = reinterpret_cast<float4*>(P.ypart + (blk + rc) * kOutCols + lane * 8);
-  part[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  part[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  __syncwarp();
-  uint32_t* cnt = P.sync + sync_offsets(d).out + t * op.ncb + cb;
-  uint32_t prev = 0;
-  if (lane == 0) prev = atom_add_acq_rel(cnt, 1u);
-  prev = __shfl_sync(0xffffffffu, prev, 0);
-  if (prev != (uint32_t)(op.NR - 1)) return;
-  // the last chunk in: sum the chunks in order
-  float y8[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) y8[u] = 0.f;
-  for (int r0 = 0; r0 < op.NR; r0 += 8) {   // loads in groups of 8 chunks, sums in order
-    float4 a[8], b[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4* pp = reinterpret_cast<const float4*>(P.ypart + (blk + r0 + u) * kOutCols + lane * 8);
-      a[u] = r0 + u < op.NR ? __ldcg(pp) : make_float4(0.f, 0.f, 0.f, 0.f);
-      b[u] = r0 + u < op.NR ? __ldcg(pp + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (r0 + u < op.NR) {
-        y8[0] += a[u].x; y8[1] += a[u].y; y8[2] += a[u].z; y8[3] += a[u].w;
-        y8[4] += b[u].x; y8[5] += b[u].y; y8[6] += b[u].z; y8[7] += b[u].w;
-      }
-    }
-  }
+  // y was zeroed by the token's top-k; the chunks add in any order (fp32)
   if (on) {
     float4* yo = reinterpret_cast<float4*>(P.y + (size_t)t * d.H + c0);
-    yo[0] = make_float4(y8[0], y8[1], y8[2], y8[3]);
-    yo[1] = make_float4(y8[4], y8[5], y8[6], y8[7]);
+    atomicAdd(yo, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    atomicAdd(yo + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
   }
-  if (lane == 0) *cnt = 0u;   // every chunk of this block is in: ready for the next call
 }
 
 // ------------------------------- the kernel --------------------------------
@@ -1375,7 +1343,6 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
   P.rowoff = ws.rowoff;
   P.wa = ws.wa;
   P.cvec = ws.cpart;
-  P.ypart = ws.ypart;
   P.stamps = stamps;
   P.sync = ws.sync;
   P.err = ws.err;

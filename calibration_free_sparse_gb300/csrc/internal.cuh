@@ -49,7 +49,6 @@ struct Workspace {
   float* wa;            // [Bmax][N]      w * a for kept list entries
   int32_t* rowoff;      // [Bmax][N]      e*I + i of kept list entries
   float* cpart;         // [Bmax][r] recovery vector c = sum_S w_j p_j b_j
-  float* ypart;         // [Bmax][ceil(H/256)][32][256] output partials per row chunk
   // host-ABI staging
   float* x_stage;       // [Bmax][H]
   float* y_stage;       // [Bmax][H]
