@@ -239,7 +239,6 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_kb = wa.take(Bm * (d.N / 32) * 4);
   const size_t w_kept = wa.take(Bm * d.N * 4);
   const size_t w_wa = wa.take(Bm * d.N * 4);
-  const size_t w_ro = wa.take(Bm * d.N * 4);
   const size_t w_sync = wa.take(mr::sync_words(d) * 4);
   const size_t w_cp = wa.take(Bm * d.r * 4);
   const size_t w_xs = wa.take(Bm * d.H * 4);
@@ -271,7 +270,6 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.keptbits = reinterpret_cast<uint32_t*>(wb + w_kb);
   h->ws.kept = reinterpret_cast<int32_t*>(wb + w_kept);
   h->ws.wa = reinterpret_cast<float*>(wb + w_wa);
-  h->ws.rowoff = reinterpret_cast<int32_t*>(wb + w_ro);
   h->ws.sync = reinterpret_cast<uint32_t*>(wb + w_sync);
   h->ws.cpart = reinterpret_cast<float*>(wb + w_cp);
   h->ws.x_stage = reinterpret_cast<float*>(wb + w_xs);

@@ -114,7 +114,6 @@ struct Params {
   float* score;
   uint32_t* keptbits;
   int32_t* kept;
-  int32_t* rowoff;
   float* wa;
   float* cvec;                  // [Bmax][r] recovery vectors, accumulated atomically
   unsigned long long* stamps;   // [grid][5] phase timestamps, or null
@@ -974,7 +973,6 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane, int pend_t, 
   sv = warp_sum(sv);
   if (lane == 0) {
     P.wa[(size_t)t * d.N + qi] = wslot * silu_f(sg) * sv;
-    P.rowoff[(size_t)t * d.N + qi] = (int32_t)row;
   }
 }
 
@@ -1091,18 +1089,58 @@ __device__ __forceinline__ void axpy8h(float c, const uint4& v, float* acc) {
 // [rc RC, (rc+1) RC) of Dt, each row read as one coalesced 512-byte piece, or
 // for rc = R the recovery U c as the r rows of U^T weighted by c.  The
 // partial is added into y with fp32 atomics.
-__device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int rc, int lane) {
+// The token's sanitised expert ids and weights, lane-distributed (topk <= 64).
+struct TokenSlots {
+  int e0, e1;
+  float w0, w1;
+};
+
+__device__ __forceinline__ TokenSlots load_token_slots(const Params& P, int t, int lane) {
   const Dims& d = P.d;
+  TokenSlots ts;
+  ts.e0 = lane < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane) : 0;
+  ts.e1 = lane + 32 < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane + 32) : 0;
+  ts.w0 = lane < d.topk ? __ldcg(P.w_ws + t * d.topk + lane) : 0.f;
+  ts.w1 = lane + 32 < d.topk ? __ldcg(P.w_ws + t * d.topk + lane + 32) : 0.f;
+  return ts;
+}
+
+// Wait state of a warp's output items: the token whose top-k it has seen
+// (rows known) and the token whose phase-2 items it has seen counted (kept
+// weights and the recovery vector known).
+struct OutWait {
+  int flag_t = -1, count_t = -1;
+  TokenSlots sl{};
+};
+
+__device__ bool out_wait(const Params& P, const uint32_t* word, uint32_t target, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = wait_at_least(word, target, P.sync + kSyncAbort, P.err);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+__device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int rc, int lane,
+                          int per_tok, OutWait& ow) {
+  const Dims& d = P.d;
+  const SyncOff so = sync_offsets(d);
   const int c0 = cb * kOutCols + lane * 8;
   const bool on = c0 < d.H;                  // H is a multiple of 8
   const int qb0 = rc * op.RC, qe = min(P.k, qb0 + op.RC);
   const uint64_t pol = policy_evict_first();  // the last read of these rows
-  const int32_t* ro_t = P.rowoff + (size_t)t * d.N;
   const float* wa_t = P.wa + (size_t)t * d.N;
+  auto counted = [&]() {
+    if (ow.count_t == t) return true;
+    if (!out_wait(P, P.sync + so.exact + t, (uint32_t)per_tok, lane)) return false;
+    ow.count_t = t;
+    return true;
+  };
   float acc[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) acc[u] = 0.f;
   if (rc == op.R) {   // recovery chunk
+    if (!counted()) return false;
     const float* c_t = P.cvec + (size_t)t * d.r;
     for (int jb = 0; jb < d.r; jb += 32) {
       const int nj = min(32, d.r - jb);
@@ -1122,25 +1160,50 @@ __device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
         for (int u = 0; u < kOutBatch; ++u) axpy8h(c[u], v[u], acc);
       }
     }
-  }
-  for (int qb = qb0; qb < qe; qb += 32) {
-    const int nq = min(32, qe - qb);
-    const int32_t ro_l = lane < nq ? __ldcg(ro_t + qb + lane) : 0;
-    const float cw_l = lane < nq ? __ldcg(wa_t + qb + lane) : 0.f;
-    for (int i0 = 0; i0 < nq; i0 += kOutBatch) {
-      uint4 v[kOutBatch];
-      float c[kOutBatch];
-#pragma unroll
-      for (int u = 0; u < kOutBatch; ++u) {
-        const int i = i0 + u;
-        const int ro = __shfl_sync(0xffffffffu, ro_l, i & 31);
-        const float cw = __shfl_sync(0xffffffffu, cw_l, i & 31);
-        const bool use = i < nq && on;
-        c[u] = i < nq ? cw : 0.f;
-        v[u] = use ? ldcg4_hint(P.Dt + (size_t)ro * d.H + c0, pol) : make_uint4(0u, 0u, 0u, 0u);
+  } else {
+    // the rows come from the kept list and the expert ids alone (known at the
+    // top-k): their loads go out before the token's phase-2 items are counted
+    if (ow.flag_t != t) {
+      if (!out_wait(P, P.sync + so.flag + t, 1u, lane)) return false;
+      ow.flag_t = t;
+      ow.sl = load_token_slots(P, t, lane);
+    }
+    for (int qb = qb0; qb < qe; qb += 32) {
+      const int nq = min(32, qe - qb);
+      int slot_l = 0, i_l = 0;
+      if (lane < nq) {
+        const int n = __ldcg(P.kept + (size_t)t * d.N + qb + lane);
+        slot_l = n / d.I;
+        i_l = n - slot_l * d.I;
       }
+      const int e_l = slot_expert(ow.sl.e0, ow.sl.e1, slot_l);   // every lane takes part
+      const int row_l = e_l * d.I + i_l;
+      float cw_l = 0.f;
+      bool have_w = false;
+      for (int i0 = 0; i0 < nq; i0 += kOutBatch) {
+        uint4 v[kOutBatch];
+        float c[kOutBatch];
 #pragma unroll
-      for (int u = 0; u < kOutBatch; ++u) axpy8(c[u], v[u], acc);
+        for (int u = 0; u < kOutBatch; ++u) {
+          const int i = i0 + u;
+          const int ro = __shfl_sync(0xffffffffu, row_l, i & 31);
+          v[u] = i < nq && on ? ldcg4_hint(P.Dt + (size_t)ro * d.H + c0, pol)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (!have_w) {   // with the first rows in flight
+          if (!counted()) return false;
+          cw_l = lane < nq ? __ldcg(wa_t + qb + lane) : 0.f;
+          have_w = true;
+        }
+#pragma unroll
+        for (int u = 0; u < kOutBatch; ++u) {
+          const int i = i0 + u;
+          const float cw = __shfl_sync(0xffffffffu, cw_l, i & 31);
+          c[u] = i < nq ? cw : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kOutBatch; ++u) axpy8(c[u], v[u], acc);
+      }
     }
   }
   // y was zeroed by the token's top-k; the chunks add in any order (fp32)
@@ -1149,6 +1212,7 @@ __device__ void out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
     atomicAdd(yo, make_float4(acc[0], acc[1], acc[2], acc[3]));
     atomicAdd(yo + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
   }
+  return true;
 }
 
 // ------------------------------- the kernel --------------------------------
@@ -1223,24 +1287,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     __syncthreads();
     if (threadIdx.x == 0) stamp[3] = globaltimer();
   }
-  // phase 3: output warp items (token, 256-column block, row chunk); a token's
-  // items start once all of its phase-2 items are counted
+  // phase 3: output warp items (token, 256-column block, row chunk), dealt
+  // from the last warp down so that warps without phase-2 work take them
+  // first; an item loads its rows once the token's top-k is in and weighs
+  // them once the token's phase-2 items are counted
   {
     const int nwarps = nctas * kWarps;
     const OutPlan op = out_plan(P, nwarps);
     const int items = P.B * op.ncb * op.NR;
-    int ready_t = -1;
-    for (int it = blockIdx.x + nctas * warp; it < items; it += nwarps) {
+    const int gw = blockIdx.x * kWarps + warp;
+    OutWait ow;
+    for (int it = nwarps - 1 - gw; it < items; it += nwarps) {
       const int t = it / (op.ncb * op.NR);
-      if (t != ready_t) {
-        int w_ok = 1;
-        if (lane == 0)
-          w_ok = wait_at_least(P.sync + so.exact + t, (uint32_t)per_tok, abort_flag, P.err);
-        if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
-        __syncwarp();
-        ready_t = t;
-      }
-      out_chunk(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane);
+      if (!out_chunk(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane, per_tok, ow)) break;
     }
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
@@ -1340,7 +1399,6 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
   P.score = ws.score;
   P.keptbits = ws.keptbits;
   P.kept = ws.kept;
-  P.rowoff = ws.rowoff;
   P.wa = ws.wa;
   P.cvec = ws.cpart;
   P.stamps = stamps;

@@ -47,7 +47,6 @@ struct Workspace {
   uint32_t* keptbits;   // [Bmax][N/32]   1 = kept
   int32_t* kept;        // [Bmax][N]      kept n = slot*I + i, ascending n (first k used)
   float* wa;            // [Bmax][N]      w * a for kept list entries
-  int32_t* rowoff;      // [Bmax][N]      e*I + i of kept list entries
   float* cpart;         // [Bmax][r] recovery vector c = sum_S w_j p_j b_j
   // host-ABI staging
   float* x_stage;       // [Bmax][H]
