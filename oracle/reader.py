@@ -461,3 +461,34 @@ def decode(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int):
     """Batch decode: every token independently (selection is per token; the
     batch-shared selection of [CN] §未来方向 is future work)."""
     return [decode_token(layer, x[t], ids[t], w[t], k) for t in range(x.shape[0])]
+
+
+# --------------------------------------------------------------------------
+# stacked layers
+# --------------------------------------------------------------------------
+RMS_EPS = 1e-6   # keeps a zero residual finite, as RMS normalisation layers do
+
+
+def rms_normalise(h: np.ndarray) -> np.ndarray:
+    """x = h / sqrt(mean(h^2) + eps) per token, in float64.  The stack's layer
+    input: the pages state only that the residual stream is carried from layer
+    to layer ([CN] §局限与改进 and §独立分析的弱点 (1) on per-layer fixed costs);
+    each layer reading the normalised residual is the plain reading of a
+    pre-normalised decoder block."""
+    h = np.asarray(h, dtype=np.float64)
+    return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + RMS_EPS)
+
+
+def decode_stack(layers, h_in: np.ndarray, ids, w, k: int):
+    """L stacked layers: x_l = rms_normalise(h_l) handed to the layer as fp32
+    (the layer input precision), y_l = decode(layer_l, x_l), h_{l+1} = h_l + y_l
+    in float64.  ids, w: [L][B][topk].  Returns (per-layer decode results,
+    h_L)."""
+    h = np.asarray(h_in, dtype=np.float64)
+    results = []
+    for l, layer in enumerate(layers):
+        x = rms_normalise(h).astype(np.float32)
+        res = decode(layer, x, ids[l], w[l], k)
+        results.append(res)
+        h = h + np.stack([r.y for r in res])
+    return results, h
