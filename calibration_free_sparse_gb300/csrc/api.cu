@@ -243,6 +243,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_cp = wa.take(Bm * d.r * 4);
   const size_t w_xs = wa.take(Bm * d.H * 4);
   const size_t w_ys = wa.take(Bm * d.H * 4);
+  const size_t w_hs = wa.take(Bm * d.H * 4);
   const size_t w_is = wa.take(Bm * d.topk * 4);
   const size_t w_ws = wa.take(Bm * d.topk * 4);
   const size_t w_bmc = wa.take((size_t)d.E * d.nb * 16);
@@ -274,6 +275,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.cpart = reinterpret_cast<float*>(wb + w_cp);
   h->ws.x_stage = reinterpret_cast<float*>(wb + w_xs);
   h->ws.y_stage = reinterpret_cast<float*>(wb + w_ys);
+  h->ws.h_stage = reinterpret_cast<float*>(wb + w_hs);
   h->ws.ids_stage = reinterpret_cast<int32_t*>(wb + w_is);
   h->ws.w_stage = reinterpret_cast<float*>(wb + w_ws);
   h->ws.bm_codes = reinterpret_cast<uint32_t*>(wb + w_bmc);
@@ -376,6 +378,50 @@ int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
     return MOE_READER_ETIMEOUT;
   }
   if (bits) return MOE_READER_EDEVICE;
+  return MOE_READER_OK;
+}
+
+int moe_reader_decode_stack(moe_reader_t* const* layers, int32_t L, const float* h_in, int32_t B,
+                            const int32_t* expert_ids, const float* expert_w, int32_t k,
+                            float* h_out, float* y_layers, void* stream) {
+  if (!layers || L < 1) return MOE_READER_EINVAL;
+  for (int l = 0; l < L; ++l) {
+    const moe_reader* h = layers[l];
+    if (!h) return MOE_READER_EINVAL;
+    const mr::Dims& a = h->d;
+    const mr::Dims& b = layers[0]->d;
+    if (a.H != b.H || a.E != b.E || a.topk != b.topk || a.I != b.I || a.c != b.c || a.r != b.r ||
+        h->device != layers[0]->device || h->grid != layers[0]->grid)
+      return MOE_READER_EINVAL;
+    if (B < 0 || B > a.Bmax) return MOE_READER_EINVAL;
+    for (int m = 0; m < l; ++m)
+      if (layers[m] == h) return MOE_READER_EINVAL;   // each layer needs its own counters
+  }
+  if (k < 0 || k > layers[0]->d.N) return MOE_READER_EINVAL;
+  if (B == 0) return MOE_READER_OK;
+  if (!h_in || !expert_ids || !expert_w || !h_out) return MOE_READER_EINVAL;
+  if (!aligned(h_in, 16) || !aligned(expert_ids, 16) || !aligned(expert_w, 16) ||
+      !aligned(h_out, 16) || !aligned(y_layers, 16))
+    return MOE_READER_EINVAL;
+  const size_t act = (size_t)B * layers[0]->d.H * 4;
+  auto overlap = [](const void* p, size_t pn, const void* q, size_t qn) {
+    const char* a = static_cast<const char*>(p);
+    const char* b = static_cast<const char*>(q);
+    return a < b + qn && b < a + pn;
+  };
+  if (overlap(h_in, act, h_out, act)) return MOE_READER_EINVAL;
+  if (y_layers && (overlap(y_layers, act * L, h_in, act) || overlap(y_layers, act * L, h_out, act)))
+    return MOE_READER_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t ce =
+      mr::launch_decode_stack(layers, L, h_in, B, expert_ids, expert_w, k, h_out, y_layers, s);
+  if (ce != cudaSuccess) return cuda_status(ce);
+  for (int l = 0; l < L; ++l) {
+    layers[l]->has_decode = 1;
+    layers[l]->last_B = B;
+    layers[l]->last_k = k;
+    layers[l]->last_stream = s;
+  }
   return MOE_READER_OK;
 }
 

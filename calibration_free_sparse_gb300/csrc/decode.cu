@@ -120,6 +120,17 @@ struct Params {
   uint32_t* sync;
   uint32_t* err;
   ScreenPlan sp;
+  // a layer of a stack: x is released per token on xwait (null: ready at
+  // launch); the token's last output item writes the residual hnext = hres + y
+  // and the next layer's input xnext = hnext / RMS(hnext) (null: last layer),
+  // then releases xnext_ready.  hnext null: a lone layer, no residual.
+  const uint32_t* xwait;
+  const float* hres;
+  float* hnext;
+  float* xnext;
+  uint32_t* xnext_ready;
+  uint32_t* next_abort;   // the next layer's abort flag and error word: an
+  uint32_t* next_err;     // aborted layer aborts the next one too
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -198,7 +209,7 @@ __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* a
 
 // Offsets (in uint32) of the synchronisation area, fixed per handle.
 struct SyncOff {
-  int slot, tok, flag, exact, total;
+  int slot, tok, flag, exact, outdone, xready, total;
 };
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
@@ -206,7 +217,9 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   o.tok = o.slot + d.Bmax * d.topk;
   o.flag = o.tok + d.Bmax;
   o.exact = o.flag + d.Bmax;
-  o.total = o.exact + d.Bmax;
+  o.outdone = o.exact + d.Bmax;
+  o.xready = o.outdone + d.Bmax;
+  o.total = o.xready + d.Bmax;
   return o;
 }
 constexpr int kSyncDone = 0, kSyncAbort = 2;
@@ -223,7 +236,7 @@ __device__ __forceinline__ bool rotate_load(const Params& P, int t, int b, int l
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int col = b * kBlock + lane + 32 * s;
-    const float xv = col < d.H ? P.x[(size_t)t * d.H + col] : 0.f;
+    const float xv = col < d.H ? __ldcg(P.x + (size_t)t * d.H + col) : 0.f;
     bad |= !isfinite(xv);
     u[s] = P.sigma[col] < 0 ? -xv : xv;
   }
@@ -582,6 +595,12 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   bool xbad = false;
   auto load_list = [&](int uu) {
     const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
+    if (P.xwait) {   // a stacked layer: token t's input comes from the layer before
+      int ok = 1;
+      if (lane == 0) ok = wait_at_least(P.xwait + t, 1u, P.sync + kSyncAbort, P.err);
+      __shfl_sync(0xffffffffu, ok, 0);   // on a timeout the abort flag ends the launch
+      __syncwarp();
+    }
     xbad = rotate_load(P, t, b, lane, xu);
     enext = P.ids_in[ts];
   };
@@ -958,14 +977,14 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane, int pend_t, 
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const float4 xa = __ldg(x4 + 2 * (h8 + 32 * u)), xb = __ldg(x4 + 2 * (h8 + 32 * u) + 1);
+      const float4 xa = x4[2 * (h8 + 32 * u)], xb = x4[2 * (h8 + 32 * u) + 1];
       dot8(gq[u], xa, xb, sg);
       dot8(vq[u], xa, xb, sv);
     }
   }
   for (; h8 < n8; h8 += 32) {
     const uint4 gq = ldg_nc4_hint(g4 + h8, pol), vq = ldg_nc4_hint(v4 + h8, pol);
-    const float4 xa = __ldg(x4 + 2 * h8), xb = __ldg(x4 + 2 * h8 + 1);
+    const float4 xa = x4[2 * h8], xb = x4[2 * h8 + 1];
     dot8(gq, xa, xb, sg);
     dot8(vq, xa, xb, sv);
   }
@@ -1108,6 +1127,57 @@ __device__ __forceinline__ TokenSlots load_token_slots(const Params& P, int t, i
 // Wait state of a warp's output items: the token whose top-k it has seen
 // (rows known) and the token whose phase-2 items it has seen counted (kept
 // weights and the recovery vector known).
+// ------------------------------ stack hand-off ------------------------------
+// One warp: 1 / RMS(v) = 1 / sqrt(mean(v^2) + 1e-6), the mean and the root in
+// fp64 so that the factor does not depend on the summation order beyond fp64
+// rounding.
+__device__ __forceinline__ float inv_rms(double ss, int H) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  return (float)(1.0 / sqrt(ss / H + 1e-6));
+}
+
+// hn = h + y (fp32) and, unless xn is null, xn = hn / RMS(hn); then release
+// the token on ready (if not null).
+__device__ void carry_residual(const float* h, const float* y, float* hn, float* xn,
+                               uint32_t* ready, int H, int lane) {
+  double ss = 0.0;
+  for (int c = 4 * lane; c < H; c += 128) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(h + c));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(y + c));
+    const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    *reinterpret_cast<float4*>(hn + c) = v;
+    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
+  }
+  if (xn) {
+    const float f = inv_rms(ss, H);
+    for (int c = 4 * lane; c < H; c += 128) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(h + c));
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(y + c));
+      *reinterpret_cast<float4*>(xn + c) =
+          make_float4((a.x + b.x) * f, (a.y + b.y) * f, (a.z + b.z) * f, (a.w + b.w) * f);
+    }
+  }
+  __syncwarp();
+  if (lane == 0 && ready) st_release(ready, 1u);
+}
+
+// xn = h / RMS(h) for the first layer of a stack; then release the token.
+__device__ __forceinline__ void normalise_input(const float* h, float* xn, uint32_t* ready, int H, int lane) {
+  double ss = 0.0;
+  for (int c = 4 * lane; c < H; c += 128) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(h + c));
+    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
+  }
+  const float f = inv_rms(ss, H);
+  for (int c = 4 * lane; c < H; c += 128) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(h + c));
+    *reinterpret_cast<float4*>(xn + c) = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
+  }
+  __syncwarp();
+  if (lane == 0) st_release(ready, 1u);
+}
+
 struct OutWait {
   int flag_t = -1, count_t = -1;
   TokenSlots sl{};
@@ -1216,12 +1286,8 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
 }
 
 // ------------------------------- the kernel --------------------------------
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
-  extern __shared__ __align__(256) unsigned char smem_raw[];
-  // the pair tables are addressed by assembling a 256-byte aligned block base
-  // with a low byte: align the working area to 256 bytes whatever the window offset
-  unsigned char* const smem = smem_raw + ((256u - (smem_addr(smem_raw) & 255u)) & 255u);
-  __shared__ int ctl[2];
+// One layer's decode by every CTA of the grid.  false: the launch is aborting.
+__device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* smem, int* ctl) {
   if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
@@ -1241,7 +1307,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     int* flag = &ctl[1];   // static shared memory: the top-k's working area starts at smem
     for (int ts = blockIdx.x; ts < P.B * d.topk; ts += nctas) {
       const int r = score_task(P, ts, flag);
-      if (r < 0) return;
+      if (r < 0) return false;
       if (r > 0) topk_token(P, ts / d.topk, smem);
       __syncthreads();
     }
@@ -1300,6 +1366,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
     for (int it = nwarps - 1 - gw; it < items; it += nwarps) {
       const int t = it / (op.ncb * op.NR);
       if (!out_chunk(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane, per_tok, ow)) break;
+      if (P.hnext) {   // a layer of a stack: the token's last item carries the residual
+        __syncwarp();
+        uint32_t prev = 0;
+        if (lane == 0) prev = atom_add_acq_rel(P.sync + so.outdone + t, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == (uint32_t)(op.ncb * op.NR - 1))
+          carry_residual(P.hres + (size_t)t * d.H, P.y + (size_t)t * d.H,
+                         P.hnext + (size_t)t * d.H, P.xnext ? P.xnext + (size_t)t * d.H : nullptr,
+                         P.xnext_ready ? P.xnext_ready + t : nullptr, d.H, lane);
+      }
     }
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
@@ -1317,10 +1393,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
       P.sync[so.flag + i] = 0u;
       P.sync[so.exact + i] = 0u;
     }
+    for (int i = threadIdx.x; i < P.B; i += kThreads) {
+      P.sync[so.outdone + i] = 0u;
+      P.sync[so.xready + i] = 0u;
+    }
     if (threadIdx.x == 0) {
       P.sync[kSyncDone] = 0u;
     }
   }
+  __syncthreads();   // ctl is reused by the next layer
+  return true;
+}
+
+// the pair tables are addressed by assembling a 256-byte aligned block base
+// with a low byte: align the working area to 256 bytes whatever the window offset
+__device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
+  return raw + ((256u - (smem_addr(raw) & 255u)) & 255u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
+  extern __shared__ __align__(256) unsigned char smem_raw[];
+  __shared__ int ctl[2];
+  // a launch queued behind this one with programmatic serialization (the next
+  // layer of a stack) may take each SM as soon as this grid's CTA leaves it
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  decode_layer(P, aligned_smem(smem_raw), ctl);
+  if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
+    // the next layer would wait for inputs that never come
+    atomicOr(P.next_err, kErrTimeout);
+    atomicExch(P.next_abort, 1u);
+  }
+  // the layer before (when this grid overlapped it) finishes before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 size_t decode_smem_bytes(const Dims& d) {
@@ -1356,21 +1460,10 @@ int decode_grid(const Dims& d) {
   return per_sm >= 1 ? sms : 0;   // one CTA per SM, all co-resident
 }
 
-cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
-                          const float* w, int k, float* y, cudaStream_t s, const cudaEvent_t* ev,
-                          unsigned long long* stamps) {
+static Params make_params(const moe_reader& h, const float* x, int B, const int32_t* ids, const float* w,
+                   int k, float* y, unsigned long long* stamps) {
   const Dims& d = h.d;
   const Workspace& ws = h.ws;
-  cudaError_t err;
-  unsigned int rec_flags = cudaEventRecordDefault;
-  if (ev) {
-    // inside stream capture a plain record is only a dependency marker; the
-    // External flag makes it an event-record node of the graph
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if ((err = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return err;
-    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
-    if ((err = cudaEventRecordWithFlags(ev[0], s, rec_flags)) != cudaSuccess) return err;
-  }
   Params P;
   P.d = d;
   P.B = B;
@@ -1405,19 +1498,91 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
   P.sync = ws.sync;
   P.err = ws.err;
   P.sp = screen_plan(d);
+  P.xwait = nullptr;
+  P.hres = nullptr;
+  P.hnext = nullptr;
+  P.xnext = nullptr;
+  P.xnext_ready = nullptr;
+  P.next_abort = nullptr;
+  P.next_err = nullptr;
+  return P;
+}
 
+// The first layer's input x_0 = h_0 / RMS(h_0), one warp per token, each
+// token released on `ready` for the decode that follows.
+__global__ void __launch_bounds__(kThreads) stack_input_kernel(const float* h, float* x,
+                                                             uint32_t* ready, int B, int H) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t < B) normalise_input(h + (size_t)t * H, x + (size_t)t * H, ready + t, H, threadIdx.x & 31);
+}
+
+static cudaError_t launch_params(const moe_reader& h, const Params& P, bool programmatic,
+                                 cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h.grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes(d);
+  cfg.dynamicSmemBytes = decode_smem_bytes(h.d);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (programmatic) {
+    // overlaps the grid before; every wait across the two grids is a
+    // bounded flag wait, and the grid before never waits on this one
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if ((err = cudaLaunchKernelEx(&cfg, decode_kernel, P)) != cudaSuccess) return err;
+  return cudaLaunchKernelEx(&cfg, decode_kernel, P);
+}
+
+cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
+                          const float* w, int k, float* y, cudaStream_t s, const cudaEvent_t* ev,
+                          unsigned long long* stamps) {
+  cudaError_t err;
+  unsigned int rec_flags = cudaEventRecordDefault;
+  if (ev) {
+    // inside stream capture a plain record is only a dependency marker; the
+    // External flag makes it an event-record node of the graph
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((err = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return err;
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+    if ((err = cudaEventRecordWithFlags(ev[0], s, rec_flags)) != cudaSuccess) return err;
+  }
+  const Params P = make_params(h, x, B, ids, w, k, y, stamps);
+  if ((err = launch_params(h, P, false, s)) != cudaSuccess) return err;
   if (ev && (err = cudaEventRecordWithFlags(ev[1], s, rec_flags)) != cudaSuccess) return err;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_stack(moe_reader* const* hs, int L, const float* h_in, int B,
+                                const int32_t* ids, const float* w, int k, float* h_out,
+                                float* y_layers, cudaStream_t s) {
+  if (L < 1) return cudaErrorInvalidValue;
+  const Dims& d = hs[0]->d;
+  const size_t tok = (size_t)B * d.topk, act = (size_t)B * d.H;
+  stack_input_kernel<<<(B + kWarps - 1) / kWarps, kThreads, 0, s>>>(
+      h_in, hs[0]->ws.x_stage, hs[0]->ws.sync + sync_offsets(d).xready, B, d.H);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  for (int l = 0; l < L; ++l) {
+    const moe_reader& h = *hs[l];
+    float* yl = y_layers ? y_layers + l * act : h.ws.y_stage;
+    Params P = make_params(h, h.ws.x_stage, B, ids + l * tok, w + l * tok, k, yl, nullptr);
+    P.xwait = h.ws.sync + sync_offsets(h.d).xready;
+    P.hres = l == 0 ? h_in : h.ws.h_stage;
+    P.hnext = l + 1 < L ? hs[l + 1]->ws.h_stage : h_out;
+    P.xnext = l + 1 < L ? hs[l + 1]->ws.x_stage : nullptr;
+    P.xnext_ready = l + 1 < L ? hs[l + 1]->ws.sync + sync_offsets(hs[l + 1]->d).xready : nullptr;
+    P.next_abort = l + 1 < L ? hs[l + 1]->ws.sync + kSyncAbort : nullptr;
+    P.next_err = l + 1 < L ? hs[l + 1]->ws.err : nullptr;
+    // the input kernel waits for everything before it on the stream; each
+    // layer overlaps the grid before, token by token
+    if ((err = launch_params(h, P, true, s)) != cudaSuccess) return err;
+  }
   return cudaSuccess;
 }
 

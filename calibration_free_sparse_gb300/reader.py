@@ -28,6 +28,7 @@ EXPORTED_SYMBOLS = (
     "moe_reader_get_stats", "moe_reader_get_kept", "moe_reader_export_size", "moe_reader_export",
     "moe_reader_get_info", "moe_reader_destroy", "moe_reader_strerror", "moe_reader_abi_version",
     "moe_reader_set_profiling", "moe_reader_read_profile", "moe_reader_topk_noalloc",
+    "moe_reader_decode_stack",
 )
 PHASES = ("decode", "screen", "score_topk", "exact", "out")
 
@@ -77,6 +78,8 @@ def _lib():
         lib.moe_reader_decode.restype = ctypes.c_int
         lib.moe_reader_decode_host.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp]
         lib.moe_reader_decode_host.restype = ctypes.c_int
+        lib.moe_reader_decode_stack.argtypes = [vp, i32, vp, i32, vp, vp, i32, vp, vp, vp]
+        lib.moe_reader_decode_stack.restype = ctypes.c_int
         lib.moe_reader_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.moe_reader_status.restype = ctypes.c_int
         lib.moe_reader_get_stats.argtypes = [vp, ctypes.POINTER(Stats)]
@@ -155,6 +158,20 @@ def topk_noalloc(scores, k, kept, ids=None, stream=None):
     code = _lib().moe_reader_topk_noalloc(_ptr(scores), _ptr(ids), rows, cols, int(k),
                                           _ptr(kept), _stream(stream))
     _check(code, "moe_reader_topk_noalloc")
+
+
+def decode_stack(readers, h_in, ids, w, k, h_out, y_layers=None, stream=None):
+    """Enqueue one decode of B = h_in.shape[0] tokens through the stacked
+    layers `readers` (distinct MoeReader objects of one shape) in a single
+    launch: layer l decodes h_l / RMS(h_l) and h_{l+1} = h_l + y_l; h_out
+    receives h_L.  ids, w: device [L][B][topk]; y_layers: device [L][B][H]
+    or None."""
+    L = len(readers)
+    arr = (ctypes.c_void_p * L)(*[r.handle for r in readers])
+    code = _lib().moe_reader_decode_stack(arr, L, _ptr(h_in), int(h_in.shape[0]), _ptr(ids),
+                                          _ptr(w), int(k), _ptr(h_out), _ptr(y_layers),
+                                          _stream(stream))
+    _check(code, "moe_reader_decode_stack")
 
 
 class MoeReader:

@@ -167,6 +167,50 @@ int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
                            const int32_t* ids_host, const float* w_host, int32_t k,
                            float* y_host, void* stream);
 
+/*
+ * moe_reader_decode_stack -- one decode step of B tokens through L stacked
+ * layers with the residual stream carried on the device (Chinese summary
+ * page, 局限与改进 (1) and 独立分析的弱点 (1): fixed per-launch costs dominate
+ * small batches).  Asynchronous on `stream`.  With h_0 = h_in:
+ *
+ *   x_l     = h_l / sqrt(mean_c h_l[c]^2 + 1e-6)   (mean and root in fp64)
+ *   y_l     = moe_reader_decode(layers[l], x_l, ...)
+ *   h_{l+1} = h_l + y_l                             (fp32)
+ *   h_out   = h_L
+ *
+ * One small input kernel and one decode grid per layer are enqueued, each
+ * grid allowed to start while the one before it runs (programmatic stream
+ * serialization): layer l+1 takes each SM as layer l leaves it and starts a
+ * token as soon as layer l has released that token's x_{l+1}.  The input
+ * kernel waits for earlier work on `stream` as any kernel does; work enqueued
+ * after the call waits for all L layers.
+ *
+ *   layers      host array of L >= 1 distinct handles prepared with
+ *               the same H, E, topk, I, c and r on the same device; a handle
+ *               may not appear twice (each layer owns its counters).
+ *   h_in        dev, fp32 [B][H]: the residual stream entering layer 0.
+ *   B           0 <= B <= every handle's max_batch (B = 0 enqueues nothing).
+ *   expert_ids  dev, int32 [L][B][topk]: layer l's routed experts.
+ *   expert_w    dev, fp32 [L][B][topk]: layer l's routing weights.
+ *   k           exact channels per token, the same in every layer.
+ *   h_out       dev, fp32 [B][H]: overwritten with h_L.
+ *   y_layers    dev, fp32 [L][B][H] or NULL: receives each y_l (NULL: the
+ *               handles' own scratch holds them).
+ *
+ * Arrays must be 16-byte aligned; h_out may not overlap h_in, nor y_layers
+ * either of them.  EINVAL for argument errors (nothing is enqueued).
+ * Device-side errors land in the error word of the layer that met them;
+ * a timeout in layer l also marks every later layer with the timeout bit,
+ * so moe_reader_status() on each handle reports and clears it.
+ * moe_reader_get_kept / get_stats / export on layers[l] then describe layer
+ * l of this step.  Per-phase profiling covers moe_reader_decode only.
+ * Each layer's y_l is as deterministic as moe_reader_decode's (fp32 atomic
+ * adds of output chunks); h_{l+1} adds it to h_l once, in fp32.
+ */
+int moe_reader_decode_stack(moe_reader_t* const* layers, int32_t L, const float* h_in, int32_t B,
+                            const int32_t* expert_ids, const float* expert_w, int32_t k,
+                            float* h_out, float* y_layers, void* stream);
+
 /* moe_reader_status -- synchronize the stream of the last decode, read and
  * clear the device error word.  *bits (host, may be NULL) receives the
  * MOE_READER_ERR_* bits.  Returns OK, EDEVICE (input check) or ETIMEOUT. */
