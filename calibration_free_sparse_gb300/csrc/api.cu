@@ -244,6 +244,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_xs = wa.take(Bm * d.H * 4);
   const size_t w_ys = wa.take(Bm * d.H * 4);
   const size_t w_hs = wa.take(Bm * d.H * 4);
+  const size_t w_xsc = wa.take(Bm * 4);
   const size_t w_is = wa.take(Bm * d.topk * 4);
   const size_t w_ws = wa.take(Bm * d.topk * 4);
   const size_t w_bmc = wa.take((size_t)d.E * d.nb * 16);
@@ -276,6 +277,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.x_stage = reinterpret_cast<float*>(wb + w_xs);
   h->ws.y_stage = reinterpret_cast<float*>(wb + w_ys);
   h->ws.h_stage = reinterpret_cast<float*>(wb + w_hs);
+  h->ws.xscale = reinterpret_cast<float*>(wb + w_xsc);
   h->ws.ids_stage = reinterpret_cast<int32_t*>(wb + w_is);
   h->ws.w_stage = reinterpret_cast<float*>(wb + w_ws);
   h->ws.bm_codes = reinterpret_cast<uint32_t*>(wb + w_bmc);

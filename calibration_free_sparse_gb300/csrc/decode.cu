@@ -120,14 +120,18 @@ struct Params {
   uint32_t* sync;
   uint32_t* err;
   ScreenPlan sp;
-  // a layer of a stack: x is released per token on xwait (null: ready at
-  // launch); the token's last output item writes the residual hnext = hres + y
-  // and the next layer's input xnext = hnext / RMS(hnext) (null: last layer),
-  // then releases xnext_ready.  hnext null: a lone layer, no residual.
+  // a layer of a stack (hnext null: a lone layer).  Token t's input is
+  // released on xwait[t] with its scale xscale[t] = 1 / RMS(hres[t]); the
+  // screen forms x = hres * xscale and writes it to xfill for the rest of the
+  // layer.  Each 256-column output block, once complete, writes hnext = hres
+  // + y; the token's last block sets xscale_next (null: last layer) from the
+  // blocks' fp64 sums of squares and releases xnext_ready.
   const uint32_t* xwait;
+  const float* xscale;
+  float* xfill;
   const float* hres;
   float* hnext;
-  float* xnext;
+  float* xscale_next;
   uint32_t* xnext_ready;
   uint32_t* next_abort;   // the next layer's abort flag and error word: an
   uint32_t* next_err;     // aborted layer aborts the next one too
@@ -142,6 +146,12 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -196,8 +206,9 @@ __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* a
   if (ld_acquire(flag) >= target) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    if (ld_acquire(flag) >= target) return true;
-    if (ld_acquire(abort_flag)) return false;
+    // poll without ordering; the acquire load orders what follows once it is met
+    if (ld_relaxed(flag) >= target && ld_acquire(flag) >= target) return true;
+    if (ld_relaxed(abort_flag)) return false;
     if (globaltimer() - t0 > kWaitNs) {
       atomicOr(err, kErrTimeout);
       atomicExch(abort_flag, 1u);
@@ -208,8 +219,10 @@ __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* a
 }
 
 // Offsets (in uint32) of the synchronisation area, fixed per handle.
+// slot .. exact: the decode's own hand-offs; cbdone .. ssum: the residual
+// hand-off of a stacked layer (ssum: fp64 [Bmax], 8-byte aligned).
 struct SyncOff {
-  int slot, tok, flag, exact, outdone, xready, total;
+  int slot, tok, flag, exact, cbdone, tokdone, xready, ssum, total;
 };
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
@@ -217,9 +230,11 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   o.tok = o.slot + d.Bmax * d.topk;
   o.flag = o.tok + d.Bmax;
   o.exact = o.flag + d.Bmax;
-  o.outdone = o.exact + d.Bmax;
-  o.xready = o.outdone + d.Bmax;
-  o.total = o.xready + d.Bmax;
+  o.cbdone = o.exact + d.Bmax;
+  o.tokdone = o.cbdone + d.Bmax * ((d.H + 255) / 256);
+  o.xready = o.tokdone + d.Bmax;
+  o.ssum = (o.xready + d.Bmax + 1) & ~1;
+  o.total = o.ssum + 2 * d.Bmax;
   return o;
 }
 constexpr int kSyncDone = 0, kSyncAbort = 2;
@@ -230,13 +245,27 @@ constexpr int kSyncDone = 0, kSyncAbort = 2;
 // the selection bits of coordinates 32 s .. 32 s + 31 (the c largest |Rx|,
 // ties to the lower coordinate).  rotate_load reads sigma x (true: x held a
 // NaN or an infinity); rotate_select_loaded does the rest.
-__device__ __forceinline__ bool rotate_load(const Params& P, int t, int b, int lane, float (&u)[4]) {
+__device__ __forceinline__ bool rotate_load(const Params& P, int t, int b, int slot, int lane,
+                                            float (&u)[4]) {
   const Dims& d = P.d;
   bool bad = false;
+  const size_t row = (size_t)t * d.H;
+  if (P.xscale) {   // a stacked layer: x = h / RMS(h), written out once per (token, block)
+    const float f = __ldcg(P.xscale + t);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int col = b * kBlock + lane + 32 * s;
+      const float xv = col < d.H ? __ldcg(P.hres + row + col) * f : 0.f;
+      if (slot == 0 && col < d.H) P.xfill[row + col] = xv;
+      bad |= !isfinite(xv);
+      u[s] = P.sigma[col] < 0 ? -xv : xv;
+    }
+    return bad;
+  }
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int col = b * kBlock + lane + 32 * s;
-    const float xv = col < d.H ? __ldcg(P.x + (size_t)t * d.H + col) : 0.f;
+    const float xv = col < d.H ? __ldcg(P.x + row + col) : 0.f;
     bad |= !isfinite(xv);
     u[s] = P.sigma[col] < 0 ? -xv : xv;
   }
@@ -601,7 +630,7 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
       __shfl_sync(0xffffffffu, ok, 0);   // on a timeout the abort flag ends the launch
       __syncwarp();
     }
-    xbad = rotate_load(P, t, b, lane, xu);
+    xbad = rotate_load(P, t, b, ts - t * d.topk, lane, xu);
     enext = P.ids_in[ts];
   };
   auto write_unit = [&](int n) {   // first warp: unit n's tables, coordinates and expert
@@ -1128,54 +1157,43 @@ __device__ __forceinline__ TokenSlots load_token_slots(const Params& P, int t, i
 // (rows known) and the token whose phase-2 items it has seen counted (kept
 // weights and the recovery vector known).
 // ------------------------------ stack hand-off ------------------------------
-// One warp: 1 / RMS(v) = 1 / sqrt(mean(v^2) + 1e-6), the mean and the root in
-// fp64 so that the factor does not depend on the summation order beyond fp64
-// rounding.
-__device__ __forceinline__ float inv_rms(double ss, int H) {
+// The warp that completes output block cb of token t: hnext = hres + y on the
+// block's 256 columns (fp32), and, when a next layer reads it, the block's sum
+// of squares (fp64) into the token's sum.  The token's last block sets the
+// next layer's input scale 1 / sqrt(sum / H + 1e-6) and releases the token.
+__device__ void carry_block(const Params& P, int t, int cb, int ncb, int lane) {
+  const Dims& d = P.d;
+  const SyncOff so = sync_offsets(d);
+  const size_t row = (size_t)t * d.H;
+  const int c0 = cb * kOutCols + lane * 8;
+  double ss = 0.0;
+  if (c0 < d.H) {
+    const float4* h4 = reinterpret_cast<const float4*>(P.hres + row + c0);
+    const float4* y4 = reinterpret_cast<const float4*>(P.y + row + c0);
+    const float4 a0 = __ldcg(h4), a1 = __ldcg(h4 + 1), b0 = __ldcg(y4), b1 = __ldcg(y4 + 1);
+    const float4 v0 = make_float4(a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w);
+    const float4 v1 = make_float4(a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w);
+    float4* o4 = reinterpret_cast<float4*>(P.hnext + row + c0);
+    o4[0] = v0;
+    o4[1] = v1;
+    ss = (double)v0.x * v0.x + (double)v0.y * v0.y + (double)v0.z * v0.z + (double)v0.w * v0.w +
+         (double)v1.x * v1.x + (double)v1.y * v1.y + (double)v1.z * v1.z + (double)v1.w * v1.w;
+  }
+  if (!P.xscale_next) return;   // the last layer: h_out only
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  return (float)(1.0 / sqrt(ss / H + 1e-6));
-}
-
-// hn = h + y (fp32) and, unless xn is null, xn = hn / RMS(hn); then release
-// the token on ready (if not null).
-__device__ void carry_residual(const float* h, const float* y, float* hn, float* xn,
-                               uint32_t* ready, int H, int lane) {
-  double ss = 0.0;
-  for (int c = 4 * lane; c < H; c += 128) {
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(h + c));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(y + c));
-    const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-    *reinterpret_cast<float4*>(hn + c) = v;
-    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
-  }
-  if (xn) {
-    const float f = inv_rms(ss, H);
-    for (int c = 4 * lane; c < H; c += 128) {
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(h + c));
-      const float4 b = __ldcg(reinterpret_cast<const float4*>(y + c));
-      *reinterpret_cast<float4*>(xn + c) =
-          make_float4((a.x + b.x) * f, (a.y + b.y) * f, (a.z + b.z) * f, (a.w + b.w) * f);
+  double* sum = reinterpret_cast<double*>(P.sync + so.ssum) + t;
+  __syncwarp();
+  uint32_t prev = 0;
+  if (lane == 0) {
+    atomicAdd(sum, ss);
+    prev = atom_add_acq_rel(P.sync + so.tokdone + t, 1u);
+    if (prev == (uint32_t)(ncb - 1)) {
+      const double tot = __ldcg(sum);
+      P.xscale_next[t] = (float)(1.0 / sqrt(tot / d.H + 1e-6));
+      st_release(P.xnext_ready + t, 1u);
     }
   }
-  __syncwarp();
-  if (lane == 0 && ready) st_release(ready, 1u);
-}
-
-// xn = h / RMS(h) for the first layer of a stack; then release the token.
-__device__ __forceinline__ void normalise_input(const float* h, float* xn, uint32_t* ready, int H, int lane) {
-  double ss = 0.0;
-  for (int c = 4 * lane; c < H; c += 128) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(h + c));
-    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
-  }
-  const float f = inv_rms(ss, H);
-  for (int c = 4 * lane; c < H; c += 128) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(h + c));
-    *reinterpret_cast<float4*>(xn + c) = make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
-  }
-  __syncwarp();
-  if (lane == 0) st_release(ready, 1u);
 }
 
 struct OutWait {
@@ -1366,15 +1384,13 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     for (int it = nwarps - 1 - gw; it < items; it += nwarps) {
       const int t = it / (op.ncb * op.NR);
       if (!out_chunk(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane, per_tok, ow)) break;
-      if (P.hnext) {   // a layer of a stack: the token's last item carries the residual
+      if (P.hnext) {   // a layer of a stack: the block's last item carries the residual
+        const int cb = (it / op.NR) % op.ncb;
         __syncwarp();
         uint32_t prev = 0;
-        if (lane == 0) prev = atom_add_acq_rel(P.sync + so.outdone + t, 1u);
+        if (lane == 0) prev = atom_add_acq_rel(P.sync + so.cbdone + t * op.ncb + cb, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == (uint32_t)(op.ncb * op.NR - 1))
-          carry_residual(P.hres + (size_t)t * d.H, P.y + (size_t)t * d.H,
-                         P.hnext + (size_t)t * d.H, P.xnext ? P.xnext + (size_t)t * d.H : nullptr,
-                         P.xnext_ready ? P.xnext_ready + t : nullptr, d.H, lane);
+        if (prev == (uint32_t)(op.NR - 1)) carry_block(P, t, cb, op.ncb, lane);
       }
     }
   }
@@ -1393,9 +1409,15 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       P.sync[so.flag + i] = 0u;
       P.sync[so.exact + i] = 0u;
     }
-    for (int i = threadIdx.x; i < P.B; i += kThreads) {
-      P.sync[so.outdone + i] = 0u;
-      P.sync[so.xready + i] = 0u;
+    if (P.hnext) {
+      const int ncb = (d.H + kOutCols - 1) / kOutCols;
+      for (int i = threadIdx.x; i < P.B * ncb; i += kThreads) P.sync[so.cbdone + i] = 0u;
+      for (int i = threadIdx.x; i < P.B; i += kThreads) {
+        P.sync[so.tokdone + i] = 0u;
+        P.sync[so.xready + i] = 0u;
+        P.sync[so.ssum + 2 * i] = 0u;
+        P.sync[so.ssum + 2 * i + 1] = 0u;
+      }
     }
     if (threadIdx.x == 0) {
       P.sync[kSyncDone] = 0u;
@@ -1414,17 +1436,12 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  // a launch queued behind this one with programmatic serialization (the next
-  // layer of a stack) may take each SM as soon as this grid's CTA leaves it
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   decode_layer(P, aligned_smem(smem_raw), ctl);
   if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
     // the next layer would wait for inputs that never come
     atomicOr(P.next_err, kErrTimeout);
     atomicExch(P.next_abort, 1u);
   }
-  // the layer before (when this grid overlapped it) finishes before this one
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 size_t decode_smem_bytes(const Dims& d) {
@@ -1499,41 +1516,49 @@ static Params make_params(const moe_reader& h, const float* x, int B, const int3
   P.err = ws.err;
   P.sp = screen_plan(d);
   P.xwait = nullptr;
+  P.xscale = nullptr;
+  P.xfill = nullptr;
   P.hres = nullptr;
   P.hnext = nullptr;
-  P.xnext = nullptr;
+  P.xscale_next = nullptr;
   P.xnext_ready = nullptr;
   P.next_abort = nullptr;
   P.next_err = nullptr;
   return P;
 }
 
-// The first layer's input x_0 = h_0 / RMS(h_0), one warp per token, each
-// token released on `ready` for the decode that follows.
-__global__ void __launch_bounds__(kThreads) stack_input_kernel(const float* h, float* x,
-                                                             uint32_t* ready, int B, int H) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (t < B) normalise_input(h + (size_t)t * H, x + (size_t)t * H, ready + t, H, threadIdx.x & 31);
+// The first layer's input scale 1 / RMS(h_0[t]), one CTA per token (fp64
+// sum of squares), each token released on `ready` for the decode that follows.
+__global__ void __launch_bounds__(kThreads) stack_input_kernel(const float* h, float* scale,
+                                                             uint32_t* ready, int H) {
+  __shared__ double part[kWarps];
+  const int t = blockIdx.x;
+  double ss = 0.0;
+  for (int c = 4 * threadIdx.x; c < H; c += 4 * kThreads) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(h + (size_t)t * H + c));
+    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < kWarps; ++w) tot += part[w];
+    scale[t] = (float)(1.0 / sqrt(tot / H + 1e-6));
+    st_release(ready + t, 1u);
+  }
 }
 
-static cudaError_t launch_params(const moe_reader& h, const Params& P, bool programmatic,
-                                 cudaStream_t s) {
+static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = decode_smem_bytes(h.d);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  if (programmatic) {
-    // overlaps the grid before; every wait across the two grids is a
-    // bounded flag wait, and the grid before never waits on this one
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-  } else {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-  }
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_kernel, P);
@@ -1553,7 +1578,7 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
     if ((err = cudaEventRecordWithFlags(ev[0], s, rec_flags)) != cudaSuccess) return err;
   }
   const Params P = make_params(h, x, B, ids, w, k, y, stamps);
-  if ((err = launch_params(h, P, false, s)) != cudaSuccess) return err;
+  if ((err = launch_params(h, P, s)) != cudaSuccess) return err;
   if (ev && (err = cudaEventRecordWithFlags(ev[1], s, rec_flags)) != cudaSuccess) return err;
   return cudaSuccess;
 }
@@ -1564,8 +1589,8 @@ cudaError_t launch_decode_stack(moe_reader* const* hs, int L, const float* h_in,
   if (L < 1) return cudaErrorInvalidValue;
   const Dims& d = hs[0]->d;
   const size_t tok = (size_t)B * d.topk, act = (size_t)B * d.H;
-  stack_input_kernel<<<(B + kWarps - 1) / kWarps, kThreads, 0, s>>>(
-      h_in, hs[0]->ws.x_stage, hs[0]->ws.sync + sync_offsets(d).xready, B, d.H);
+  stack_input_kernel<<<B, kThreads, 0, s>>>(h_in, hs[0]->ws.xscale,
+                                             hs[0]->ws.sync + sync_offsets(d).xready, d.H);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   for (int l = 0; l < L; ++l) {
@@ -1573,15 +1598,20 @@ cudaError_t launch_decode_stack(moe_reader* const* hs, int L, const float* h_in,
     float* yl = y_layers ? y_layers + l * act : h.ws.y_stage;
     Params P = make_params(h, h.ws.x_stage, B, ids + l * tok, w + l * tok, k, yl, nullptr);
     P.xwait = h.ws.sync + sync_offsets(h.d).xready;
+    P.xscale = h.ws.xscale;
+    P.xfill = h.ws.x_stage;
     P.hres = l == 0 ? h_in : h.ws.h_stage;
     P.hnext = l + 1 < L ? hs[l + 1]->ws.h_stage : h_out;
-    P.xnext = l + 1 < L ? hs[l + 1]->ws.x_stage : nullptr;
+    P.xscale_next = l + 1 < L ? hs[l + 1]->ws.xscale : nullptr;
     P.xnext_ready = l + 1 < L ? hs[l + 1]->ws.sync + sync_offsets(hs[l + 1]->d).xready : nullptr;
     P.next_abort = l + 1 < L ? hs[l + 1]->ws.sync + kSyncAbort : nullptr;
     P.next_err = l + 1 < L ? hs[l + 1]->ws.err : nullptr;
-    // the input kernel waits for everything before it on the stream; each
-    // layer overlaps the grid before, token by token
-    if ((err = launch_params(h, P, true, s)) != cudaSuccess) return err;
+    // stream order: a layer's grid starts once the grid before has finished
+    // (a grid allowed to start early, by programmatic serialization, parks
+    // CTAs that would take SMs the layer before still needs, and was
+    // measured slower); the per-token release on xwait keeps the hand-off
+    // valid under any launch order
+    if ((err = launch_params(h, P, s)) != cudaSuccess) return err;
   }
   return cudaSuccess;
 }

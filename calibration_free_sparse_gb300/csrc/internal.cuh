@@ -52,6 +52,7 @@ struct Workspace {
   float* x_stage;       // [Bmax][H]
   float* y_stage;       // [Bmax][H]
   float* h_stage;       // [Bmax][H]      residual stream entering this layer of a stack
+  float* xscale;        // [Bmax]         1 / RMS of that residual, per token
   int32_t* ids_stage;   // [Bmax][topk]
   float* w_stage;       // [Bmax][topk]
   // accounting scratch
@@ -123,10 +124,9 @@ cudaError_t launch_project_b(const Dims& d, const __nv_bfloat16* Dt, const __hal
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
                           const float* w, int k, float* y, cudaStream_t s,
                           const cudaEvent_t* ev, unsigned long long* stamps);
-// A stack of L layers (distinct handles of equal shape), one launch per layer
-// chained by programmatic serialization, with the residual stream h carried
-// on the device: h_0 = h_in, layer l decodes
-// x_l = h_l / RMS(h_l) (staged in handle l's x_stage), h_{l+1} = h_l + y_l
+// A stack of L layers (distinct handles of equal shape), one launch per layer,
+// with the residual stream h carried on the device: h_0 = h_in, layer l decodes
+// x_l = h_l / RMS(h_l) (formed by layer l's screen into handle l's x_stage), h_{l+1} = h_l + y_l
 // (handle l+1's h_stage; h_out for the last layer).  y_l goes to y_layers +
 // l B H, or to handle l's y_stage when y_layers is null.
 cudaError_t launch_decode_stack(moe_reader* const* hs, int L, const float* h_in, int B,

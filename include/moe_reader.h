@@ -173,17 +173,17 @@ int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
  * page, 局限与改进 (1) and 独立分析的弱点 (1): fixed per-launch costs dominate
  * small batches).  Asynchronous on `stream`.  With h_0 = h_in:
  *
- *   x_l     = h_l / sqrt(mean_c h_l[c]^2 + 1e-6)   (mean and root in fp64)
+ *   x_l     = h_l * f_l,  f_l = 1 / sqrt(mean_c h_l[c]^2 + 1e-6)
+ *             (mean and root in fp64, f_l and the product in fp32)
  *   y_l     = moe_reader_decode(layers[l], x_l, ...)
  *   h_{l+1} = h_l + y_l                             (fp32)
  *   h_out   = h_L
  *
- * One small input kernel and one decode grid per layer are enqueued, each
- * grid allowed to start while the one before it runs (programmatic stream
- * serialization): layer l+1 takes each SM as layer l leaves it and starts a
- * token as soon as layer l has released that token's x_{l+1}.  The input
- * kernel waits for earlier work on `stream` as any kernel does; work enqueued
- * after the call waits for all L layers.
+ * One small input kernel (the per-token scale of h_0) and one decode grid
+ * per layer are enqueued in stream order.  Each layer's output blocks write
+ * h_{l+1} and the next layer's input scale as they complete; the next layer
+ * forms x_{l+1} in its screen.  No host work or separate residual kernel
+ * sits between the layers.
  *
  *   layers      host array of L >= 1 distinct handles prepared with
  *               the same H, E, topk, I, c and r on the same device; a handle
