@@ -6,7 +6,9 @@ distinct prepared Qwen3-30B-A3B-shaped layers (H 2048, E 128, top-8, I 768,
 k 756 = the 17.8% read budget, c 80, r 32).  Cycling the layers keeps the
 data a step touches (hundreds of MB) far above the 129 MB L2, so no decode
 finds its weights in L2.  Every step is one CUDA-graph replay per batch size;
-timing uses CUDA events on the replay stream.
+timing uses CUDA events on the replay stream.  The same layers are also run
+as one residual-carrying stack per call (the 48-layer stack workload at the
+17.8% and 12.8% budgets, batch 1 and 8), reported beside the headline.
 
 Prints ONE JSON line (rank 0).  --impl reference times the fp64 oracle on
 the host cores instead (the reference arm: there is no runnable reference
@@ -40,7 +42,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--batches", default="1,4,8,16")
     ap.add_argument("--input-sets", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -445,21 +447,24 @@ def run_ours(args, wl, world, rank, local):
     if not args.no_stack:
         from calibration_free_sparse_gb300.reader import decode_stack
 
-        stack = {"layers": L, "per_batch": {}}
-        for B in batches:
+        stack = {"layers": L, "per_budget": {}}
+        k_low = S.QWEN3_30B_LOW.k if wl.name == S.QWEN3_30B.name else None
+        budgets = [("17.8%", wl.k)] + ([("12.8%", k_low)] if k_low is not None else [])
+        stack_batches = [B for B in batches if B in (1, 8)] or batches
+        for (bname, kk), B in [(bk, B) for bk in budgets for B in stack_batches]:
             h_in = inputs[(0, B, 0)][0]
             ids = torch.stack([inputs[(0, B, l)][1] for l in range(L)]).contiguous()
             w = torch.stack([inputs[(0, B, l)][2] for l in range(L)]).contiguous()
             h_out = torch.empty_like(h_in)
             with torch.cuda.stream(stream):
-                decode_stack(readers, h_in, ids, w, wl.k, h_out)
+                decode_stack(readers, h_in, ids, w, kk, h_out)
             for rd in readers:
                 code, bits = rd.status()
                 if code != 0:
                     raise RuntimeError(f"stack: device status {code} bits {bits}")
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
-                decode_stack(readers, h_in, ids, w, wl.k, h_out)
+                decode_stack(readers, h_in, ids, w, kk, h_out)
             with torch.cuda.stream(stream):
                 for _ in range(max(3, args.warmup)):
                     graph.replay()
@@ -472,9 +477,11 @@ def run_ours(args, wl, world, rank, local):
                 ev1.record(stream)
             torch.cuda.synchronize()
             us_layer = 1000.0 * ev0.elapsed_time(ev1) / (args.steps * L)
-            stack["per_batch"][str(B)] = {
-                "us_per_layer": us_layer, "tokens_per_s": B / (us_layer / 1e6),
-                "vs_independent_decodes": per_batch[str(B)]["us_per_decode"] / us_layer}
+            row = {"k": kk, "us_per_layer": us_layer, "tokens_per_s": B / (us_layer / 1e6),
+                   "us_per_stack_step": us_layer * L}
+            if kk == wl.k:
+                row["vs_independent_decodes"] = per_batch[str(B)]["us_per_decode"] / us_layer
+            stack["per_budget"].setdefault(bname, {})[str(B)] = row
         stack["note"] = ("moe_reader_decode_stack over the %d prepared layers, one call per "
                          "step captured in a CUDA graph: an input-scale kernel plus one decode "
                          "grid per layer, residual and next input carried on the device; "
