@@ -976,18 +976,33 @@ __device__ __forceinline__ int slot_expert(int e0, int e1, int slot) {
   return slot < 32 ? a : b;
 }
 
-__device__ void kept_item(const Params& P, int t, int qi, int lane, int pend_t, int pend_n) {
+struct TokenSlots {
+  int e0, e1;
+  float w0, w1;
+};
+
+__device__ __forceinline__ TokenSlots load_token_slots(const Params& P, int t, int lane) {
   const Dims& d = P.d;
-  const int n = __ldcg(P.kept + (size_t)t * d.N + qi);
-  // the token's expert ids, requested beside the kept index
-  const int e0 = lane < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane) : 0;
-  const int e1 = lane + 32 < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane + 32) : 0;
-  const float w0 = lane < d.topk ? __ldcg(P.w_ws + t * d.topk + lane) : 0.f;
-  const float w1 = lane + 32 < d.topk ? __ldcg(P.w_ws + t * d.topk + lane + 32) : 0.f;
+  TokenSlots ts;
+  ts.e0 = lane < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane) : 0;
+  ts.e1 = lane + 32 < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane + 32) : 0;
+  ts.w0 = lane < d.topk ? __ldcg(P.w_ws + t * d.topk + lane) : 0.f;
+  ts.w1 = lane + 32 < d.topk ? __ldcg(P.w_ws + t * d.topk + lane + 32) : 0.f;
+  return ts;
+}
+
+// Kept channel n (list position qi) of token t: a = phi(g^T x)(v^T x) from the
+// native rows, stored as w a.  The kept index and the token's slots were read
+// ahead by the caller, so the row loads are the item's only round trip.
+__device__ void kept_item(const Params& P, int t, int qi, int n, const TokenSlots& sl, int lane,
+                          int pend_t, int pend_n) {
+  const Dims& d = P.d;
   publish_item(P, pend_t, pend_n, lane);
+
   const int slot = n / d.I, i = n % d.I;
-  const int e = slot_expert(e0, e1, slot);
-  const float wslot = __int_as_float(slot_expert(__float_as_int(w0), __float_as_int(w1), slot));
+  const int e = slot_expert(sl.e0, sl.e1, slot);
+  const float wslot =
+      __int_as_float(slot_expert(__float_as_int(sl.w0), __float_as_int(sl.w1), slot));
   const size_t row = (size_t)e * d.I + i;
   const uint64_t pol = policy_evict_first();
   const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
@@ -1004,6 +1019,7 @@ __device__ void kept_item(const Params& P, int t, int qi, int lane, int pend_t, 
       gq[u] = ldg_nc4_hint(g4 + h8 + 32 * u, pol);
       vq[u] = ldg_nc4_hint(v4 + h8 + 32 * u, pol);
     }
+
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const float4 xa = x4[2 * (h8 + 32 * u)], xb = x4[2 * (h8 + 32 * u) + 1];
@@ -1105,7 +1121,7 @@ struct OutPlan {
   int ncb;   // output blocks
   int R;     // kept-row chunks per (token, block)
   int RC;    // kept rows per chunk
-  int NR;    // chunks per (token, block): R, plus the recovery chunk U c when k < N
+  int NR;    // chunks per (token, block): R, plus the recovery chunks of U c when k < N
 };
 
 // Enough (token, block, chunk) warp items to occupy every warp once.
@@ -1113,7 +1129,8 @@ __device__ __forceinline__ OutPlan out_plan(const Params& P, int nwarps) {
   OutPlan op;
   op.ncb = (P.d.H + kOutCols - 1) / kOutCols;
   const int per = P.B * op.ncb;
-  const int rec = P.k < P.d.N ? 1 : 0;
+  // the recovery U c comes in chunks of kOutBatch rank components
+  const int rec = P.k < P.d.N ? (P.d.r + kOutBatch - 1) / kOutBatch : 0;
   int R = nwarps / per - rec;                 // one round of warp items,
   R = min(R, (P.k + kOutBatch - 1) / kOutBatch);   // each at least one full load batch
   R = max(1, min(R, P.k));
@@ -1138,24 +1155,6 @@ __device__ __forceinline__ void axpy8h(float c, const uint4& v, float* acc) {
 // for rc = R the recovery U c as the r rows of U^T weighted by c.  The
 // partial is added into y with fp32 atomics.
 // The token's sanitised expert ids and weights, lane-distributed (topk <= 64).
-struct TokenSlots {
-  int e0, e1;
-  float w0, w1;
-};
-
-__device__ __forceinline__ TokenSlots load_token_slots(const Params& P, int t, int lane) {
-  const Dims& d = P.d;
-  TokenSlots ts;
-  ts.e0 = lane < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane) : 0;
-  ts.e1 = lane + 32 < d.topk ? __ldcg(P.ids_ws + t * d.topk + lane + 32) : 0;
-  ts.w0 = lane < d.topk ? __ldcg(P.w_ws + t * d.topk + lane) : 0.f;
-  ts.w1 = lane + 32 < d.topk ? __ldcg(P.w_ws + t * d.topk + lane + 32) : 0.f;
-  return ts;
-}
-
-// Wait state of a warp's output items: the token whose top-k it has seen
-// (rows known) and the token whose phase-2 items it has seen counted (kept
-// weights and the recovery vector known).
 // ------------------------------ stack hand-off ------------------------------
 // The warp that completes output block cb of token t: hnext = hres + y on the
 // block's 256 columns (fp32), and, when a next layer reads it, the block's sum
@@ -1196,6 +1195,9 @@ __device__ void carry_block(const Params& P, int t, int cb, int ncb, int lane) {
   }
 }
 
+// Wait state of a warp's output items: the token whose top-k it has seen
+// (rows known) and the token whose phase-2 items it has seen counted (kept
+// weights and the recovery vector known).
 struct OutWait {
   int flag_t = -1, count_t = -1;
   TokenSlots sl{};
@@ -1227,26 +1229,19 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
   float acc[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-  if (rc == op.R) {   // recovery chunk
+  if (rc >= op.R) {   // recovery chunk: rank components j0 .. j0 + nj - 1 of U c
+    const int j0 = (rc - op.R) * kOutBatch, nj = min(kOutBatch, d.r - j0);
+    uint4 v[kOutBatch];
+#pragma unroll
+    for (int u = 0; u < kOutBatch; ++u)   // U^T rows do not depend on the token: load first
+      v[u] = u < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(j0 + u) * d.H + c0))
+                          : make_uint4(0u, 0u, 0u, 0u);
     if (!counted()) return false;
-    const float* c_t = P.cvec + (size_t)t * d.r;
-    for (int jb = 0; jb < d.r; jb += 32) {
-      const int nj = min(32, d.r - jb);
-      const float cj_l = lane < nj ? __ldcg(c_t + jb + lane) : 0.f;
-      for (int i0 = 0; i0 < nj; i0 += kOutBatch) {
-        uint4 v[kOutBatch];
-        float c[kOutBatch];
+    const float cj_l = lane < nj ? __ldcg(P.cvec + (size_t)t * d.r + j0 + lane) : 0.f;
 #pragma unroll
-        for (int u = 0; u < kOutBatch; ++u) {
-          const int i = i0 + u;
-          const float cw = __shfl_sync(0xffffffffu, cj_l, i & 31);
-          c[u] = i < nj ? cw : 0.f;
-          v[u] = i < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(jb + i) * d.H + c0))
-                              : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < kOutBatch; ++u) axpy8h(c[u], v[u], acc);
-      }
+    for (int u = 0; u < kOutBatch; ++u) {
+      const float cw = __shfl_sync(0xffffffffu, cj_l, u);
+      axpy8h(u < nj ? cw : 0.f, v[u], acc);
     }
   } else {
     // the rows come from the kept list and the expert ids alone (known at the
@@ -1266,6 +1261,14 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
       }
       const int e_l = slot_expert(ow.sl.e0, ow.sl.e1, slot_l);   // every lane takes part
       const int row_l = e_l * d.I + i_l;
+      // rows past the first load batch head for L2 now (4 lines of a 512-byte piece each)
+      for (int p0 = kOutBatch * 4; p0 < nq * 4; p0 += 32) {
+        const int pl = p0 + lane, i = pl >> 2;
+        const int ro = __shfl_sync(0xffffffffu, row_l, i & 31);
+        const int col = cb * kOutCols + (pl & 3) * 64;
+        if (pl < nq * 4 && col < d.H)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(P.Dt + (size_t)ro * d.H + col));
+      }
       float cw_l = 0.f;
       bool have_w = false;
       for (int i0 = 0; i0 < nq; i0 += kOutBatch) {
@@ -1342,6 +1345,8 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     const long long ipw = (M + wtot - 1) / wtot;
     const long long q0 = gw * ipw, q1 = min(M, q0 + ipw);
     int cur_t = -1, pend_t = -1, pend_n = 0;
+    int kbase = 0, kn_l = 0;   // lane j: kept index at list position kbase + j
+    TokenSlots sl{};
     bool ok = true;
     for (long long q = q0; q < q1; ++q) {
       const int t = (int)(q / per_tok), local = (int)(q % per_tok);
@@ -1355,11 +1360,18 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
         }
         __syncwarp();
         cur_t = t;
+        sl = load_token_slots(P, t, lane);
+        kbase = -64;
       }
       const bool flush = pend_t >= 0 && pend_t != t;   // leaving token pend_t
-      if (local < P.k)
-        kept_item(P, t, local, lane, flush ? pend_t : -1, pend_n);
-      else
+      if (local < P.k) {
+        if (local - kbase >= 32) {   // the next 32 kept indices in one read
+          kbase = local;
+          kn_l = kbase + lane < P.k ? __ldcg(P.kept + (size_t)t * d.N + kbase + lane) : 0;
+        }
+        const int n = __shfl_sync(0xffffffffu, kn_l, local - kbase);
+        kept_item(P, t, local, n, sl, lane, flush ? pend_t : -1, pend_n);
+      } else
         recovery_item(P, t, local - P.k, lane, flush ? pend_t : -1, pend_n);
       if (flush) pend_n = 0;
       pend_t = t;
