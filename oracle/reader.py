@@ -387,18 +387,21 @@ def screen_estimates(layer: Layer, e: int, Rx: np.ndarray, mask: np.ndarray):
     return est[0], est[1]
 
 
-def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int) -> TokenResult:
-    """One token through the reader ([CN] §方法步骤详情, decode (1)-(4)).
+@dataclass
+class TokenScreen:
+    """Steps 1-2 of one token up to its scores (before any selection)."""
+    mask: np.ndarray         # bool [nb][128]
+    ghat: np.ndarray         # float64 [topk][I]
+    vhat: np.ndarray
+    p: np.ndarray            # phi(ghat) vhat
+    score: np.ndarray        # w ||d|| |p|
 
-    1. Rotate x once; partial screen of the c largest-|Rx| coordinates per block.
-    2. s_j = w_j ||d_j|| |phi(ghat_j) vhat_j| for every routed channel (the
-       placement of |.| follows [KR] §어떻게 쓰나; [CN] writes phi(ghat)|vhat|),
-       then the exact top-k over all routed experts' channels together; ties
-       go to the lower global channel id e*I + i.
-    3. Kept channels: native BF16 g_j, v_j with the original fp32 x,
-       a_j = phi(g_j^T x)(v_j^T x); y_exact = sum_K w_j a_j d_j.
-    4. Skipped channels: y_recovery = U sum_S w_j b_j p_j, p_j = phi(ghat_j) vhat_j.
-    """
+
+def screen_token(layer: Layer, x: np.ndarray, ids, w) -> TokenScreen:
+    """Rotate x once, partial screen of the c largest-|Rx| coordinates per
+    block, and the output-unit score s_j = w_j ||d_j|| |phi(ghat_j) vhat_j| of
+    every routed channel ([CN] §方法步骤详情, decode (1)-(2); the placement of
+    |.| follows [KR] §어떻게 쓰나, [CN] writes phi(ghat)|vhat|)."""
     sh = layer.shape
     x64 = np.asarray(x, dtype=np.float64)
     xpad = pad_hidden(x64, sh.Hp)
@@ -416,44 +419,64 @@ def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k:
     p = silu(ghat) * vhat
     wv = np.asarray(w, dtype=np.float64)
     score = wv[:, None] * dn * np.abs(p)
+    return TokenScreen(mask=mask, ghat=ghat, vhat=vhat, p=p, score=score)
 
+
+def exact_and_recovery(layer: Layer, x: np.ndarray, ids, w, p: np.ndarray, keep: np.ndarray):
+    """Steps 3-4 for one token given its kept channels (keep: bool [topk][I]):
+    kept channels from the native BF16 g_j, v_j with the original fp32 x,
+    a_j = phi(g_j^T x)(v_j^T x), y_exact = sum_K w_j a_j d_j; skipped ones
+    recovered as y_recovery = U sum_S w_j b_j p_j."""
+    sh = layer.shape
+    x64 = np.asarray(x, dtype=np.float64)
+    wv = np.asarray(w, dtype=np.float64)
+    y_exact = np.zeros(sh.H)
+    coef = np.zeros(sh.r)
+    any_skip = False
+    for s, e in enumerate(int(v) for v in ids):
+        rows = np.nonzero(keep[s])[0]
+        if rows.size:
+            g_rows = bf16_bits_to_f64(layer.G[e][rows])          # [n][H]
+            v_rows = bf16_bits_to_f64(layer.V[e][rows])
+            d_cols = bf16_bits_to_f64(layer.D[e][:, rows])        # [H][n]
+            a = silu(g_rows @ x64) * (v_rows @ x64)
+            y_exact += d_cols @ (wv[s] * a)
+        skip = np.nonzero(~keep[s])[0]
+        if skip.size:
+            any_skip = True
+            coef += (wv[s] * p[s, skip]) @ layer.b(e)[skip].astype(np.float64)
+    y_rec = layer.U.astype(np.float64) @ coef if any_skip else np.zeros(sh.H)
+    return y_exact, y_rec
+
+
+def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int) -> TokenResult:
+    """One token through the reader ([CN] §方法步骤详情, decode (1)-(4)).
+
+    1. Rotate x once; partial screen of the c largest-|Rx| coordinates per block.
+    2. s_j = w_j ||d_j|| |phi(ghat_j) vhat_j| for every routed channel, then the
+       exact top-k over all routed experts' channels together; ties go to the
+       lower global channel id e*I + i.
+    3. Kept channels: native BF16 g_j, v_j with the original fp32 x,
+       a_j = phi(g_j^T x)(v_j^T x); y_exact = sum_K w_j a_j d_j.
+    4. Skipped channels: y_recovery = U sum_S w_j b_j p_j, p_j = phi(ghat_j) vhat_j.
+    """
+    sh = layer.shape
+    sc = screen_token(layer, x, ids, w)
+    ids = [int(e) for e in ids]
     gid = np.array([[e * sh.I + i for i in range(sh.I)] for e in ids], dtype=np.int64)
-    flat_s = score.reshape(-1)
+    flat_s = sc.score.reshape(-1)
     flat_id = gid.reshape(-1)
     order = np.lexsort((flat_id, -flat_s))       # primary -s, secondary id
     kept_idx = order[:k]
-    skip_idx = order[k:]
     kth = float(flat_s[order[k - 1]]) if k > 0 else float("nan")
     nxt = float(flat_s[order[k]]) if k < flat_s.size else float("nan")
-
-    kept_slot, kept_i = np.divmod(kept_idx, sh.I)
-    skip_slot, skip_i = np.divmod(skip_idx, sh.I)
-
-    y_exact = np.zeros(sh.H)
-    for s, e in enumerate(ids):
-        rows = kept_i[kept_slot == s]
-        if rows.size == 0:
-            continue
-        g_rows = bf16_bits_to_f64(layer.G[e][rows])          # [n][H]
-        v_rows = bf16_bits_to_f64(layer.V[e][rows])
-        d_cols = bf16_bits_to_f64(layer.D[e][:, rows])        # [H][n]
-        a = silu(g_rows @ x64) * (v_rows @ x64)
-        y_exact += d_cols @ (wv[s] * a)
-
-    y_rec = np.zeros(sh.H)
-    if skip_idx.size:
-        coef = np.zeros(sh.r)
-        for s, e in enumerate(ids):
-            rows = skip_i[skip_slot == s]
-            if rows.size == 0:
-                continue
-            coef += (wv[s] * p[s, rows]) @ layer.b(e)[rows].astype(np.float64)
-        y_rec = layer.U.astype(np.float64) @ coef
-
+    keep = np.zeros(flat_s.size, bool)
+    keep[kept_idx] = True
+    y_exact, y_rec = exact_and_recovery(layer, x, ids, w, sc.p, keep.reshape(len(ids), sh.I))
     return TokenResult(
         y=y_exact + y_rec, y_exact=y_exact, y_recovery=y_rec,
         kept=np.sort(flat_id[kept_idx]), kept_order=flat_id[kept_idx],
-        score=score, p=p, ghat=ghat, vhat=vhat, mask=mask,
+        score=sc.score, p=sc.p, ghat=sc.ghat, vhat=sc.vhat, mask=sc.mask,
         kth_score=kth, next_score=nxt)
 
 
@@ -461,6 +484,77 @@ def decode(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int):
     """Batch decode: every token independently (selection is per token; the
     batch-shared selection of [CN] §未来方向 is future work)."""
     return [decode_token(layer, x[t], ids[t], w[t], k) for t in range(x.shape[0])]
+
+
+# --------------------------------------------------------------------------
+# batch-shared selection
+# --------------------------------------------------------------------------
+@dataclass
+class SharedResult:
+    """One batch through the reader with one kept set for the whole batch."""
+    tokens: list             # per token: TokenResult (kept = its share of K; kth/next: the batch's)
+    experts: np.ndarray      # ascending distinct routed experts of the batch
+    batch_score: np.ndarray  # float64 [len(experts)][I]
+    K: int                   # kept channels of the batch
+    kept: np.ndarray         # int64 sorted global ids e*I + i of K
+    kth_score: float
+    next_score: float
+
+
+def shared_kept_count(k: int, n_experts: int, topk: int) -> int:
+    """K_B = k * n_e / topk rounded half up: the per-token kept fraction k / N
+    applied to the batch's union of n_e * I routed channels."""
+    return (2 * k * n_experts + topk) // (2 * topk)
+
+
+def decode_shared(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int) -> SharedResult:
+    """Batch-shared selection: one kept set for the whole batch ([CN] §未来方向
+    (1) names it as the way to keep the gains at larger batches and gives no
+    formula; the reading taken here):
+
+    - every token is screened and scored as in decode_token (steps 1-2);
+    - the union U of the batch's routed channels: all I channels of every
+      expert some token routes to;
+    - batch score S(e, i) = sum of s_{t,(e,i)} over the tokens t routed to e,
+      in token order (the output-unit scores add up the tokens' output error);
+    - K = the top-K_B of S over U, K_B = shared_kept_count(k, |experts|, topk),
+      ties to the lower global id e*I + i;
+    - token t computes its channels in K exactly and recovers its routed
+      channels outside K with its own p (steps 3-4).
+
+    At batch 1, U is the token's N routed channels, K_B = k and S = s: the
+    per-token reader."""
+    sh = layer.shape
+    B = x.shape[0]
+    ids = np.asarray(ids)
+    screens = [screen_token(layer, x[t], ids[t], w[t]) for t in range(B)]
+    experts = np.array(sorted({int(e) for e in ids.reshape(-1)}), dtype=np.int64)
+    rank = {int(e): r for r, e in enumerate(experts)}
+    S = np.zeros((experts.size, sh.I))
+    for t in range(B):
+        for s_, e in enumerate(ids[t]):
+            S[rank[int(e)]] += screens[t].score[s_]
+    K = shared_kept_count(k, experts.size, sh.topk)
+    gid = (experts[:, None] * sh.I + np.arange(sh.I)[None, :]).reshape(-1)
+    flat = S.reshape(-1)
+    order = np.lexsort((gid, -flat))
+    kept = np.sort(gid[order[:K]])
+    kth = float(flat[order[K - 1]]) if K > 0 else float("nan")
+    nxt = float(flat[order[K]]) if K < flat.size else float("nan")
+    kept_set = set(int(g) for g in kept)
+    tokens = []
+    for t in range(B):
+        sc = screens[t]
+        tid = np.array([[int(e) * sh.I + i for i in range(sh.I)] for e in ids[t]], dtype=np.int64)
+        keep = np.vectorize(lambda g: int(g) in kept_set)(tid) if tid.size else np.zeros_like(tid, bool)
+        y_exact, y_rec = exact_and_recovery(layer, x[t], ids[t], w[t], sc.p, keep)
+        mine = np.sort(tid[keep])
+        tokens.append(TokenResult(
+            y=y_exact + y_rec, y_exact=y_exact, y_recovery=y_rec, kept=mine, kept_order=mine,
+            score=sc.score, p=sc.p, ghat=sc.ghat, vhat=sc.vhat, mask=sc.mask,
+            kth_score=kth, next_score=nxt))
+    return SharedResult(tokens=tokens, experts=experts, batch_score=S, K=K, kept=kept,
+                        kth_score=kth, next_score=nxt)
 
 
 # --------------------------------------------------------------------------
