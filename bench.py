@@ -49,6 +49,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
+    ap.add_argument("--no-shared", action="store_true")
+    ap.add_argument("--large-batch", action="store_true",
+                    help="also time the GPT-OSS-120B-shaped layer at batch 1-128, per-token "
+                         "against batch-shared selection")
     return ap.parse_args()
 
 
@@ -283,6 +287,63 @@ def traffic_for(kernel, batch):
     return ent.get("bytes_per_launch")
 
 
+def large_batch_stress(torch, dev, stream, args, nl=6, batches=(1, 16, 64, 128)):
+    """Per-token against batch-shared selection on nl GPT-OSS-120B-shaped
+    layers (17.8% budget): microseconds per layer decode and the read fraction
+    of the first layer, one CUDA graph per (mode, batch)."""
+    from calibration_free_sparse_gb300 import synthetic as S
+    from calibration_free_sparse_gb300.reader import MoeReader
+
+    wl = S.GPT_OSS_120B
+    readers, keep = [], []
+    for l in range(nl):
+        g, v, d = S.weights_device(300 + l, wl.E, wl.I, wl.H, dev)
+        readers.append(MoeReader(wl.H, wl.E, wl.topk, wl.I, g, v, d, S.signs(300 + l, wl.Hp),
+                                 screen_coords=wl.c, rank=wl.r, max_batch=max(batches)))
+        keep.append((g, v))
+        del d
+    out = {"workload": wl.name, "k": wl.k, "layers": nl, "per_batch": {}}
+    for B in batches:
+        x = torch.from_numpy(S.activations(5, B, wl.H)).to(dev)
+        ids, w = S.routing(5, B, wl.E, wl.topk)
+        ids, w = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
+        y = torch.empty_like(x)
+        row = {}
+        for mode in ("per_token", "shared"):
+            def run(mode=mode):
+                for rd in readers:
+                    (rd.decode_shared if mode == "shared" else rd.decode)(x, ids, w, wl.k, y)
+            with torch.cuda.stream(stream):
+                run()
+            st = readers[0].stats()
+            frac = sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")) / st["dense"]
+            for rd in readers:
+                code, bits = rd.status()
+                if code != 0:
+                    raise RuntimeError(f"large batch: device status {code} bits {bits}")
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                run()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    graph.replay()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            reps = max(3, min(args.steps, 10))
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                ev1.record(stream)
+            torch.cuda.synchronize()
+            us = 1000.0 * ev0.elapsed_time(ev1) / (reps * nl)
+            row[mode] = {"us_per_decode": us, "tokens_per_s": B / (us / 1e6), "read_fraction": frac}
+        out["per_batch"][str(B)] = row
+    for rd in readers:
+        rd.close()
+    return out
+
+
 def run_ours(args, wl, world, rank, local):
     import torch
 
@@ -441,6 +502,47 @@ def run_ours(args, wl, world, rank, local):
                 "launch_us": 1000.0 * dom_ms, "peak_kind": f"{peak_kind} copy bandwidth",
                 "share_of_step_time": 1.0}
 
+    # -- batch-shared selection (one kept set per batch) on the same layers and
+    # inputs: informational, the headline keeps per-token selection
+    shared = None
+    if not args.no_shared:
+        shared = {"per_batch": {}}
+        for B in batches:
+            def run_shared(B=B):
+                for l, rd in enumerate(readers):
+                    x, ids, w, y, _ = inputs[(0, B, l)]
+                    rd.decode_shared(x, ids, w, wl.k, y)
+            with torch.cuda.stream(stream):
+                run_shared()
+            rd0 = readers[0]
+            st = rd0.stats()
+            sb = 32 * sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U"))
+            for rd in readers:
+                code, bits = rd.status()
+                if code != 0:
+                    raise RuntimeError(f"shared: device status {code} bits {bits}")
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                run_shared()
+            with torch.cuda.stream(stream):
+                for _ in range(max(3, args.warmup)):
+                    graph.replay()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                for _ in range(args.steps):
+                    graph.replay()
+                ev1.record(stream)
+            torch.cuda.synchronize()
+            us = 1000.0 * ev0.elapsed_time(ev1) / (args.steps * L)
+            shared["per_batch"][str(B)] = {
+                "us_per_decode": us, "tokens_per_s": B / (us / 1e6),
+                "sector_bytes_per_decode_layer0": sb, "read_fraction_layer0": sb / (32 * st["dense"]),
+                "vs_per_token": per_batch[str(B)]["us_per_decode"] / us}
+        shared["note"] = ("moe_reader_decode_shared on the same %d layers and inputs, one CUDA "
+                          "graph per batch: one kept set per batch of k n_e / topk channels" % L)
+
     # -- the same layers as one stack per call (residual carried on the device):
     # informational, the headline above decodes the layers independently
     stack = None
@@ -487,6 +589,11 @@ def run_ours(args, wl, world, rank, local):
                          "grid per layer, residual and next input carried on the device; "
                          "vs_independent_decodes compares with the headline's unchained "
                          "per-layer decodes, which carry no residual" % L)
+
+    # -- large-batch stress: the GPT-OSS-120B-shaped layer, both selections
+    large = None
+    if args.large_batch and rank == 0:
+        large = large_batch_stress(torch, dev, stream, args)
 
     # -- end to end through the host-buffer C ABI (pinned host memory)
     e2e = None
@@ -566,6 +673,8 @@ def run_ours(args, wl, world, rank, local):
             "per_batch": per_batch,
             "roofline": roofline,
             "stack": stack,
+            "shared": shared,
+            "large_batch": large,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

@@ -138,11 +138,11 @@ int profile_slot(moe_reader* h) {
 }
 
 cudaError_t launch_profiled(moe_reader* h, const float* x, int B, const int32_t* ids,
-                            const float* w, int k, float* y, cudaStream_t s) {
+                            const float* w, int k, float* y, cudaStream_t s, bool shared = false) {
   const int slot = profile_slot(h);
-  if (slot < 0) return mr::launch_decode(*h, x, B, ids, w, k, y, s, nullptr, nullptr);
+  if (slot < 0) return mr::launch_decode(*h, x, B, ids, w, k, y, s, nullptr, nullptr, shared);
   return mr::launch_decode(*h, x, B, ids, w, k, y, s, h->prof_ev[slot],
-                           h->prof_stamps + (size_t)slot * h->grid * 5);
+                           h->prof_stamps + (size_t)slot * h->grid * 5, shared);
 }
 
 }  // namespace
@@ -245,6 +245,15 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_ys = wa.take(Bm * d.H * 4);
   const size_t w_hs = wa.take(Bm * d.H * 4);
   const size_t w_xsc = wa.take(Bm * 4);
+  const size_t EI = (size_t)d.E * d.I;
+  const size_t w_ssc = wa.take(EI * 4);
+  const size_t w_skp = wa.take(EI * 4);
+  const size_t w_sbt = wa.take(EI / 32 * 4);
+  const size_t w_est = wa.take(((size_t)d.E + 1) * 4);
+  const size_t w_els = wa.take(Bm * d.topk * 4);
+  const size_t w_kct = wa.take(Bm * 4);
+  const size_t w_sK = wa.take(4);
+  const size_t w_sinf = wa.take(EI * 4);
   const size_t w_is = wa.take(Bm * d.topk * 4);
   const size_t w_ws = wa.take(Bm * d.topk * 4);
   const size_t w_bmc = wa.take((size_t)d.E * d.nb * 16);
@@ -278,6 +287,14 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.y_stage = reinterpret_cast<float*>(wb + w_ys);
   h->ws.h_stage = reinterpret_cast<float*>(wb + w_hs);
   h->ws.xscale = reinterpret_cast<float*>(wb + w_xsc);
+  h->ws.sscore = reinterpret_cast<float*>(wb + w_ssc);
+  h->ws.skept = reinterpret_cast<int32_t*>(wb + w_skp);
+  h->ws.sbits = reinterpret_cast<uint32_t*>(wb + w_sbt);
+  h->ws.estart = reinterpret_cast<int32_t*>(wb + w_est);
+  h->ws.elist = reinterpret_cast<int32_t*>(wb + w_els);
+  h->ws.kcount = reinterpret_cast<int32_t*>(wb + w_kct);
+  h->ws.sK = reinterpret_cast<int32_t*>(wb + w_sK);
+  h->ws.sinfo = reinterpret_cast<int32_t*>(wb + w_sinf);
   h->ws.ids_stage = reinterpret_cast<int32_t*>(wb + w_is);
   h->ws.w_stage = reinterpret_cast<float*>(wb + w_ws);
   h->ws.bm_codes = reinterpret_cast<uint32_t*>(wb + w_bmc);
@@ -338,7 +355,46 @@ int moe_reader_decode(moe_reader_t* h, const float* x, int32_t B, const int32_t*
   h->has_decode = 1;
   h->last_B = B;
   h->last_k = k;
+  h->last_shared = 0;
   h->last_stream = s;
+  return MOE_READER_OK;
+}
+
+int moe_reader_decode_shared(moe_reader_t* h, const float* x, int32_t B, const int32_t* expert_ids,
+                             const float* expert_w, int32_t k, float* y, void* stream) {
+  int st = check_decode_args(h, x, B, expert_ids, expert_w, k, y);
+  if (st != MOE_READER_OK) return st;
+  if (B == 0) return MOE_READER_OK;
+  if (!aligned(x, 16) || !aligned(expert_ids, 16) || !aligned(expert_w, 16) || !aligned(y, 16))
+    return MOE_READER_EINVAL;
+  if ((const void*)x == (const void*)y) return MOE_READER_EINVAL;
+  if (!mr::shared_supported(h->d, B)) return MOE_READER_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t ce = launch_profiled(h, x, B, expert_ids, expert_w, k, y, s, true);
+  if (ce != cudaSuccess) return cuda_status(ce);
+  h->has_decode = 1;
+  h->last_B = B;
+  h->last_k = k;
+  h->last_shared = 1;
+  h->last_stream = s;
+  return MOE_READER_OK;
+}
+
+int moe_reader_get_kept_shared(moe_reader_t* h, int32_t* kept_host, int64_t capacity,
+                               int32_t* count_out) {
+  if (!h || (!kept_host && capacity > 0)) return MOE_READER_EINVAL;
+  if (!h->has_decode || !h->last_shared) return MOE_READER_ESTATE;
+  cudaStream_t s = h->last_stream;
+  cudaError_t ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return cuda_status(ce);
+  int32_t K = 0;
+  if ((ce = cudaMemcpy(&K, h->ws.sK, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_status(ce);
+  if (count_out) *count_out = K;
+  if (capacity < K) return MOE_READER_EINVAL;
+  if (K > 0 && (ce = cudaMemcpy(kept_host, h->ws.skept, (size_t)K * 4, cudaMemcpyDeviceToHost)) !=
+                   cudaSuccess)
+    return cuda_status(ce);
   return MOE_READER_OK;
 }
 
@@ -366,6 +422,7 @@ int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
   h->has_decode = 1;
   h->last_B = B;
   h->last_k = k;
+  h->last_shared = 0;
   h->last_stream = s;
   if ((ce = cudaMemcpyAsync(y_host, h->ws.y_stage, (size_t)B * d.H * 4, cudaMemcpyDeviceToHost, s)) !=
       cudaSuccess)
@@ -422,6 +479,7 @@ int moe_reader_decode_stack(moe_reader_t* const* layers, int32_t L, const float*
     layers[l]->has_decode = 1;
     layers[l]->last_B = B;
     layers[l]->last_k = k;
+    layers[l]->last_shared = 0;
     layers[l]->last_stream = s;
   }
   return MOE_READER_OK;
@@ -478,7 +536,7 @@ int moe_reader_get_stats(moe_reader_t* h, moe_reader_stats* out) {
 
 int moe_reader_get_kept(moe_reader_t* h, int32_t* kept_host, int64_t capacity) {
   if (!h || (!kept_host && capacity > 0)) return MOE_READER_EINVAL;
-  if (!h->has_decode) return MOE_READER_ESTATE;
+  if (!h->has_decode || h->last_shared) return MOE_READER_ESTATE;
   const int B = h->last_B, k = h->last_k;
   const int64_t n = (int64_t)B * k;
   if (capacity < n) return MOE_READER_EINVAL;

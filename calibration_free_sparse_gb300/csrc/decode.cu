@@ -135,6 +135,18 @@ struct Params {
   uint32_t* xnext_ready;
   uint32_t* next_abort;   // the next layer's abort flag and error word: an
   uint32_t* next_err;     // aborted layer aborts the next one too
+  // batch-shared selection (the shared kernel only)
+  float* sscore;          // [E][I]        batch scores of the routed experts
+  int32_t* skept;         // [E * I]       the batch's kept global ids e*I + i, ascending
+  uint32_t* sbits;        // [E][I / 32]   the batch's kept set (routed experts only)
+  int32_t* estart;        // [E + 1]       per expert: its first entry in elist
+  int32_t* elist;         // [Bmax*topk]   token slots routed to each expert, ascending
+  int32_t* kcount;        // [Bmax]        kept channels of each token
+  int32_t* sK;            // [1]           the batch's kept count
+  int32_t* sinfo;         // [E * I]       per kept channel: its expert's first elist entry
+                          //               * 16384 + the expert's token-slot count
+  uint32_t* ecount;       // [E]           per expert: score tasks in (synchronisation)
+  int smem_bytes;         // dynamic shared memory of a CTA (after alignment)
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -222,7 +234,7 @@ __device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* a
 // slot .. exact: the decode's own hand-offs; cbdone .. ssum: the residual
 // hand-off of a stacked layer (ssum: fp64 [Bmax], 8-byte aligned).
 struct SyncOff {
-  int slot, tok, flag, exact, cbdone, tokdone, xready, ssum, total;
+  int slot, tok, flag, exact, cbdone, tokdone, xready, ssum, ecount, total;
 };
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
@@ -234,10 +246,14 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   o.tokdone = o.cbdone + d.Bmax * ((d.H + 255) / 256);
   o.xready = o.tokdone + d.Bmax;
   o.ssum = (o.xready + d.Bmax + 1) & ~1;
-  o.total = o.ssum + 2 * d.Bmax;
+  o.ecount = o.ssum + 2 * d.Bmax;   // the shared kernel: score tasks in, per expert
+  o.total = o.ecount + d.E;
   return o;
 }
 constexpr int kSyncDone = 0, kSyncAbort = 2;
+// the shared kernel's batch-wide hand-offs: routed experts scored, the
+// batch's kept set released, shared kept items done
+constexpr int kSyncBatch = 5, kSyncReady = 6, kSyncSdone = 7;
 
 // ------------------------------- phase 0 -----------------------------------
 // Rotation and screen selection of one (token, 128-block) by one warp: lane
@@ -476,18 +492,17 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
         }
       }
       __syncthreads();
-      // every (ci, cj) pair once, spread over the threads
-      const int pairs = m * m;
-      int* rk = hist;               // reuse: rank counters [m]
-      for (int c = threadIdx.x; c < m; c += kThreads) rk[c] = 0;
-      __syncthreads();
-      for (int q = threadIdx.x; q < pairs; q += kThreads) {
-        const int ci = q / m, cj = q - ci * m;
-        const uint32_t ki = ckey[ci], kj = ckey[cj];
-        if (kj > ki || (kj == ki && cgid[cj] < cgid[ci])) atomicAdd(&rk[ci], 1);
+      // a warp per candidate: its lanes count the candidates ahead of it
+      for (int ci = wid; ci < m; ci += kWarps) {
+        const uint32_t ki = ckey[ci], gi = cgid[ci];
+        int ahead = 0;
+        for (int cj = lane; cj < m; cj += 32) {
+          const uint32_t kj = ckey[cj];
+          ahead += kj > ki || (kj == ki && cgid[cj] < gi);
+        }
+        ahead = warp_sum_i(ahead);
+        if (lane == 0) keep[crank[ci]] = ahead < need;
       }
-      __syncthreads();
-      for (int c = threadIdx.x; c < m; c += kThreads) keep[crank[c]] = rk[c] < need;
     } else {
       // degenerate spread (too many keys in one digit): full radix select
       int need2 = 0;
@@ -544,6 +559,440 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   }
   // the output phase adds its chunks into y[t]: start it from zero
   for (int h = threadIdx.x; h < d.H; h += kThreads) P.y[(size_t)t * d.H + h] = 0.f;
+  __syncthreads();
+  if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], 1u);
+}
+
+// ------------------------- batch-shared selection ---------------------------
+// One kept set for the whole batch: the union of the routed experts' channels
+// is ranked by the batch score (the routed tokens' scores summed in token
+// order) and the top K = k n_e / topk (rounded half up, n_e routed experts)
+// are kept; each token computes its share exactly and recovers the rest.
+
+// In-place exclusive prefix sum of a[0..n) by the whole CTA (each thread a
+// contiguous segment); returns the total.  wsum: [kWarps] scratch.
+__device__ int block_exclusive_scan(int* a, int n, int* wsum) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int per = (n + kThreads - 1) / kThreads;
+  const int b0 = min(n, (int)threadIdx.x * per), b1 = min(n, b0 + per);
+  int mine = 0;
+  for (int q = b0; q < b1; ++q) mine += a[q];
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  int before = incl - mine, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    before += w < wid ? wsum[w] : 0;
+    total += wsum[w];
+  }
+  __syncthreads();   // every thread has read wsum
+  for (int q = b0; q < b1; ++q) {
+    const int v = a[q];
+    a[q] = before;
+    before += v;
+  }
+  __syncthreads();
+  return total;
+}
+
+// The digit of a kBins histogram (counted from the top) holding the K-th
+// largest key: sh[3] = digit, sh[4] = its keys to keep, sh[5] = its keys.
+__device__ void digit_search(const int* hist, int K, int* wsum, int* sh) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  constexpr int kPer = kBins / kThreads;
+  int c8[kPer], tot = 0;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    c8[q] = hist[kBins - 1 - (threadIdx.x * kPer + q)];
+    tot += c8[q];
+  }
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  int before = incl - tot;
+  for (int w = 0; w < wid; ++w) before += wsum[w];
+  if (before < K && before + tot >= K) {
+    int above = before;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      if (above + c8[q] >= K) {
+        sh[3] = kBins - 1 - (threadIdx.x * kPer + q);
+        sh[4] = K - above;
+        sh[5] = c8[q];
+        break;
+      }
+      above += c8[q];
+    }
+  }
+  __syncthreads();
+}
+
+// Shared-memory bytes of shared_select for a shape (0 if it does not fit the
+// decode's dynamic shared memory).
+__host__ __device__ inline size_t shared_select_bytes(const Dims& d) {
+  return (size_t)(kWarps + 1) * 256 * 4 + (size_t)(3 * d.E + 2) * 4 + 64 + kWarps * 4 +
+         (size_t)kCandMax * 12 + (size_t)d.E * (d.I / 32) * 4 + 256;
+}
+
+// The batch's kept set, by the CTA that completed the last batch-score task.
+__device__ void shared_select(const Params& P, unsigned char* smem) {
+  const Dims& d = P.d;
+  const int BT = P.B * d.topk, E = d.E, I = d.I, IW = d.I / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t below = (1u << lane) - 1u;
+  int* hist = reinterpret_cast<int*>(smem);            // [(kWarps + 1) * 256]
+  int* cnt = hist + (kWarps + 1) * 256;                 // [E + 1] counts, then starts
+  int* cur = cnt + (E + 1);                             // [E + 1] fill cursors
+  int* uexp = cur + (E + 1);                            // [E] routed experts, ascending
+  int* sh = uexp + E;                                   // [16]
+  int* wsum = sh + 16;                                  // [kWarps]
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(wsum + kWarps);   // [kCandMax]
+  uint32_t* cgid = ckey + kCandMax;                     // [kCandMax]
+  int* cu = reinterpret_cast<int*>(cgid + kCandMax);    // [kCandMax]
+  uint32_t* bits = reinterpret_cast<uint32_t*>(cu + kCandMax);   // [n_e][IW]
+  uint32_t* kc = bits + (size_t)E * IW;   // the union's keys when they fit, else unused
+  for (int e = threadIdx.x; e <= E; e += kThreads) cnt[e] = 0;
+  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+  if (threadIdx.x == 0) sh[2] = 0;
+  __syncthreads();
+  for (int ts = threadIdx.x; ts < BT; ts += kThreads) atomicAdd(&cnt[__ldcg(P.ids_ws + ts)], 1);
+  __syncthreads();
+  // routed-expert ranks (cur as scratch), then the starts of each expert's slots
+  for (int e = threadIdx.x; e < E; e += kThreads) cur[e] = cnt[e] ? 1 : 0;
+  __syncthreads();
+  const int ne = block_exclusive_scan(cur, E, wsum);
+  for (int e = threadIdx.x; e < E; e += kThreads)
+    if (cnt[e]) uexp[cur[e]] = e;
+  __syncthreads();
+  block_exclusive_scan(cnt, E + 1, wsum);   // cnt[E] was 0: it becomes the total
+  for (int e = threadIdx.x; e <= E; e += kThreads) {
+    cur[e] = cnt[e];
+    P.estart[e] = cnt[e];
+  }
+  const int K = (2 * P.k * ne + d.topk) / (2 * d.topk), U = ne * I;
+  if (threadIdx.x == 0) *P.sK = K;
+  __syncthreads();
+  // the union's keys stay in shared memory when they fit; else their digits
+  // (the second pass then reads only the threshold digit's keys again)
+  const size_t room = (size_t)P.smem_bytes - (size_t)(reinterpret_cast<unsigned char*>(kc) - smem);
+  const bool cached = (size_t)U * 4 <= room;
+  const bool dcached = !cached && (size_t)U * 2 <= room;
+  uint16_t* dc = reinterpret_cast<uint16_t*>(kc);
+  // each expert's token slots in ascending order: one warp, 32 slots a step
+  if (wid == 0) {
+    for (int base = 0; base < BT; base += 32) {
+      const int ts = base + lane;
+      const int e = ts < BT ? __ldcg(P.ids_ws + ts) : -1 - lane;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int at = ts < BT ? cur[e] + __popc(same & below) : 0;
+      __syncwarp();
+      if (ts < BT) {
+        P.elist[at] = ts;
+        if ((same & below) == 0) cur[e] += __popc(same);
+      }
+      __syncwarp();
+    }
+  }
+  // 1. histogram of the batch scores' 12-bit digit over the union (the keys
+  //    stay in shared memory when they fit)
+  {
+    constexpr int kV = 4;   // float4 loads in flight per thread
+    const int U4 = U / 4;   // I is a multiple of 64: whole float4 groups of one expert
+    for (int f0 = threadIdx.x; f0 < U4; f0 += kThreads * kV) {
+      float4 kv[kV];
+#pragma unroll
+      for (int v = 0; v < kV; ++v) {
+        const int f = f0 + v * kThreads;
+        const int u = 4 * f, r = u / I;
+        kv[v] = f < U4 ? __ldcg(reinterpret_cast<const float4*>(P.sscore + (size_t)uexp[r] * I +
+                                                                 (u - r * I)))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int v = 0; v < kV; ++v) {
+        const int f = f0 + v * kThreads;
+        if (f >= U4) break;
+        const uint32_t k4[4] = {__float_as_uint(kv[v].x), __float_as_uint(kv[v].y),
+                                __float_as_uint(kv[v].z), __float_as_uint(kv[v].w)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (cached) kc[4 * f + c] = k4[c];
+          if (dcached) dc[4 * f + c] = (uint16_t)key_digit(k4[c]);
+          atomicAdd(&hist[key_digit(k4[c])], 1);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  auto keyof = [&](int u) {
+    if (cached) return kc[u];
+    const int r = u / I, i = u - r * I;
+    return __float_as_uint(__ldcg(P.sscore + (size_t)uexp[r] * I + i));
+  };
+  const bool all = K >= U, none = K <= 0;
+  int D = -1, need = 0, m = 0;
+  if (!all && !none) {
+    // 2. the digit holding the K-th largest batch score
+    digit_search(hist, K, wsum, sh);
+    D = sh[3];
+    need = sh[4];
+    m = sh[5];
+  }
+  // the digit's members (u) when they fit the list after the key cache
+  constexpr int kDl = 8192;
+  const size_t used = cached ? (size_t)U * 4 : (dcached ? (size_t)U * 2 : 0);
+  int* dl = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(kc) + ((used + 15) & ~(size_t)15));
+  const bool listed = m > kCandMax && m <= kDl && ((used + 15) & ~(size_t)15) + (size_t)kDl * 4 <= room;
+  // 3. kept bits above the digit (a ballot per 32 channels of one expert) and
+  //    the digit's candidates
+  for (int base = 32 * wid; base < U; base += kThreads) {
+    const int u = base + lane, r = u / I, i = u - r * I;
+    const int dg = dcached ? (int)dc[u] : key_digit(keyof(u));
+    const unsigned keep = __ballot_sync(0xffffffffu, all || (!none && dg > D));
+    if (lane == 0) bits[base >> 5] = keep;
+    if (!all && !none && dg == D && m <= kCandMax) {
+      const int c = atomicAdd(&sh[2], 1);
+      cgid[c] = (uint32_t)(uexp[r] * I + i);
+      cu[c] = u;
+    } else if (listed && dg == D) {
+      dl[atomicAdd(&sh[2], 1)] = u;
+    }
+  }
+  __syncthreads();
+  if (!all && !none && m <= kCandMax)   // the candidates' keys, all loads in flight together
+    for (int c = threadIdx.x; c < m; c += kThreads) ckey[c] = keyof(cu[c]);
+  __syncthreads();
+  int mode = 0;   // 1: rank the candidates; 2: full radix select
+  if (!all && !none) mode = m <= kCandMax ? 1 : 2;
+  if (listed) {
+    // a second 12-bit digit (key bits 18..7) inside digit D
+    for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for (int c = threadIdx.x; c < m; c += kThreads) atomicAdd(&hist[(keyof(dl[c]) >> 7) & (kBins - 1)], 1);
+    __syncthreads();
+    digit_search(hist, need, wsum, sh);
+    const int D2 = sh[3], need2 = sh[4], m2 = sh[5];
+    if (threadIdx.x == 0) sh[2] = 0;
+    __syncthreads();
+    for (int c = threadIdx.x; c < m; c += kThreads) {
+      const int u = dl[c];
+      const uint32_t key = keyof(u);
+      const int d2 = (int)((key >> 7) & (kBins - 1));
+      if (d2 > D2) atomicOr(&bits[u >> 5], 1u << (u & 31));
+      if (d2 == D2 && m2 <= kCandMax) {
+        const int q = atomicAdd(&sh[2], 1);
+        const int r = u / I;
+        ckey[q] = key;
+        cgid[q] = (uint32_t)(uexp[r] * I + (u - r * I));
+        cu[q] = u;
+      }
+    }
+    __syncthreads();
+    if (m2 <= kCandMax) {   // D2's members ranked exactly
+      m = m2;
+      need = need2;
+      mode = 1;
+    }
+  }
+  {
+    if (mode == 1) {
+      // the candidates ranked exactly: larger score, then lower global id (a
+      // warp per candidate)
+      for (int ci = wid; ci < m; ci += kWarps) {
+        const uint32_t ki = ckey[ci], gi = cgid[ci];
+        int ahead = 0;
+        for (int cj = lane; cj < m; cj += 32) {
+          const uint32_t kj = ckey[cj];
+          ahead += kj > ki || (kj == ki && cgid[cj] < gi);
+        }
+        ahead = warp_sum_i(ahead);
+        if (lane == 0 && ahead < need) atomicOr(&bits[cu[ci] >> 5], 1u << (cu[ci] & 31));
+      }
+    } else if (mode == 2) {
+      // degenerate spread: full radix select over the union, ties by id
+      auto gidof = [&](int u) {
+        const int r = u / I;
+        return (uint32_t)(uexp[r] * I + (u - r * I));
+      };
+      int need2 = 0;
+      const uint32_t T = cta_radix_select(
+          U, K, [&](int u, uint32_t& key) { key = keyof(u); return true; }, hist, sh + 8, &need2);
+      int eq = 0;
+      for (int u = threadIdx.x; u < U; u += kThreads) eq += keyof(u) == T;
+      eq = warp_sum_i(eq);
+      if (lane == 0) wsum[wid] = eq;
+      __syncthreads();
+      int eq_total = 0;
+      for (int w = 0; w < kWarps; ++w) eq_total += wsum[w];
+      __syncthreads();
+      uint32_t T2 = 0;
+      if (need2 < eq_total) {
+        int dummy = 0;
+        T2 = cta_radix_select(
+            U, need2,
+            [&](int u, uint32_t& key) {
+              if (keyof(u) != T) return false;
+              key = 0xffffffffu - gidof(u);
+              return true;
+            },
+            hist, sh + 8, &dummy);
+      }
+      for (int base = 32 * wid; base < U; base += kThreads) {
+        const int u = base + lane;
+        const uint32_t a = keyof(u);
+        const bool kp = a > T || (a == T && 0xffffffffu - gidof(u) >= T2);
+        const unsigned keep = __ballot_sync(0xffffffffu, kp);
+        if (lane == 0) bits[base >> 5] = keep;
+      }
+    }
+  }
+  __syncthreads();
+  // 4. the set per expert, and the kept global ids in ascending order
+  const int words = ne * IW;
+  for (int q = threadIdx.x; q < words; q += kThreads)
+    P.sbits[(size_t)uexp[q / IW] * IW + q % IW] = bits[q];
+  const int wper = (words + kWarps - 1) / kWarps;
+  const int w0 = wid * wper, w1 = min(words, w0 + wper);
+  int mine = 0;
+  for (int wd = w0; wd < w1; ++wd) mine += __popc(bits[wd]);
+  if (lane == 0) wsum[wid] = mine;
+  __syncthreads();
+  int pos = 0;
+  for (int w = 0; w < wid; ++w) pos += wsum[w];
+  {
+    int r = w0 / IW, wr = w0 - r * IW;   // expert rank and word within it, advanced together
+    for (int wd = w0; wd < w1; ++wd) {
+      const uint32_t bw = bits[wd];
+      if (bw) {
+        if ((bw >> lane) & 1u) {
+          const int e = uexp[r], at = pos + __popc(bw & below);
+          P.skept[at] = e * I + wr * 32 + lane;
+          P.sinfo[at] = cnt[e] * 16384 + (cnt[e + 1] - cnt[e]);
+        }
+        pos += __popc(bw);
+      }
+      if (++wr == IW) {
+        wr = 0;
+        ++r;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) st_release(P.sync + kSyncReady, 1u);
+}
+
+// The shared kernel's end of score task ts (expert e): the task that scores
+// the last slot routed to e sums e's batch scores (token order), and the task
+// that completes the last routed expert selects the batch's kept set.  The
+// routing is read from the input (validated as the screen does), so no other
+// task's writes are needed to know who routes where.
+__device__ void shared_after_score(const Params& P, int e, unsigned char* smem, int* flag) {
+  const Dims& d = P.d;
+  const int BT = P.B * d.topk;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t below = (1u << lane) - 1u;
+  int* lst = reinterpret_cast<int*>(smem);      // [BT] token slots routed to e, ascending
+  int* cw = lst + BT;                           // [kWarps]
+  int* seen = cw + kWarps;                      // [E] experts routed by the batch
+  int* sh = seen + d.E;                         // [4]
+  for (int q = threadIdx.x; q < d.E; q += kThreads) seen[q] = 0;
+  __syncthreads();
+  int n = 0;
+  for (int base = 0; base < BT; base += kThreads) {
+    const int ts = base + threadIdx.x;
+    int ei = ts < BT ? P.ids_in[ts] : -1;
+    if (ts < BT && (ei < 0 || ei >= d.E)) ei = 0;
+    if (ts < BT) seen[ei] = 1;
+    const bool hit = ts < BT && ei == e;
+    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) cw[wid] = __popc(bal);
+    __syncthreads();
+    int before = n, tot = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      before += w < wid ? cw[w] : 0;
+      tot += cw[w];
+    }
+    if (hit) lst[before + __popc(bal & below)] = ts;
+    n += tot;
+    __syncthreads();
+  }
+  int ne = 0;
+  for (int q0 = 0; q0 < d.E; q0 += kThreads) {
+    const int q = q0 + threadIdx.x;
+    ne += __syncthreads_count(q < d.E && seen[q]);
+  }
+  if (threadIdx.x == 0) {
+    sh[0] = ne;
+    // releases this slot's scores; the last of e's slots also acquires the others'
+    sh[1] = atom_add_acq_rel(P.ecount + e, 1u) == (uint32_t)(n - 1);
+  }
+  __syncthreads();
+  if (!sh[1]) return;
+  for (int i = threadIdx.x; i < d.I; i += kThreads) {
+    float sum = 0.f;
+    for (int q0 = 0; q0 < n; q0 += 8) {   // eight loads in flight, added in token order
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = q0 + u < n ? __ldcg(P.score + (size_t)lst[q0 + u] * d.I + i) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (q0 + u < n) sum += v[u];
+    }
+    P.sscore[(size_t)e * d.I + i] = sum;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    *flag = atom_add_acq_rel(P.sync + kSyncBatch, 1u) == (uint32_t)(sh[0] - 1);
+  __syncthreads();
+  if (*flag) shared_select(P, smem);
+  __syncthreads();
+}
+
+// Token t's share of the batch's set: its kept bitmap and ascending kept list
+// (n = slot I + i) and their count; y[t] zeroed; then the token is released.
+__device__ void shared_token(const Params& P, int t, unsigned char* smem) {
+  const Dims& d = P.d;
+  const int IW = d.I / 32, words = d.N / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t below = (1u << lane) - 1u;
+  int* wsum = reinterpret_cast<int*>(smem);   // [kWarps]
+  uint32_t* tw = reinterpret_cast<uint32_t*>(wsum + kWarps);   // [words]
+  for (int wd = threadIdx.x; wd < words; wd += kThreads) {
+    const int slot = wd / IW;
+    const int e = __ldcg(P.ids_ws + t * d.topk + slot);
+    const uint32_t bw = __ldcg(P.sbits + (size_t)e * IW + (wd - slot * IW));
+    tw[wd] = bw;
+    P.keptbits[(size_t)t * words + wd] = bw;
+  }
+  __syncthreads();
+  const int wper = (words + kWarps - 1) / kWarps;
+  const int w0 = wid * wper, w1 = min(words, w0 + wper);
+  int mine = 0;
+  for (int wd = w0; wd < w1; ++wd) mine += __popc(tw[wd]);
+  if (lane == 0) wsum[wid] = mine;
+  __syncthreads();
+  int pos = 0, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    pos += w < wid ? wsum[w] : 0;
+    total += wsum[w];
+  }
+  for (int wd = w0; wd < w1; ++wd) {
+    const uint32_t bw = tw[wd];
+    if ((bw >> lane) & 1u) P.kept[(size_t)t * d.N + pos + __popc(bw & below)] = wd * 32 + lane;
+    pos += __popc(bw);
+  }
+  if (threadIdx.x == 0) P.kcount[t] = total;
   __syncthreads();
   if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], 1u);
 }
@@ -878,7 +1327,8 @@ __device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
 // the block partials in block order, s = w ||d|| |phi(ghat) vhat|.  Returns
 // -1 on abort, 1 when this was the token's last slot to be scored (the CTA
 // then runs the token's top-k), else 0.
-__device__ int score_task(const Params& P, int ts, int* flag) {
+template <bool SH>
+__device__ int score_task(const Params& P, int ts, int* flag, unsigned char* smem) {
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int t = ts / d.topk, slot = ts % d.topk, I = d.I;
@@ -942,6 +1392,14 @@ __device__ int score_task(const Params& P, int ts, int* flag) {
     }
   }
   __syncthreads();
+  if (SH) {
+    // every output chunk of the batch adds into y[t]: start it from zero
+    // before the batch's set is released
+    if (slot == 0)
+      for (int h = threadIdx.x; h < d.H; h += kThreads) P.y[(size_t)t * d.H + h] = 0.f;
+    shared_after_score(P, e, smem, flag);
+    return 0;
+  }
   if (threadIdx.x == 0) {
     // releases this slot's scores; the last slot in also acquires the others'
     const uint32_t prev = atom_add_acq_rel(P.sync + so.tok + t, 1u);
@@ -1037,6 +1495,63 @@ __device__ void kept_item(const Params& P, int t, int qi, int n, const TokenSlot
   sv = warp_sum(sv);
   if (lane == 0) {
     P.wa[(size_t)t * d.N + qi] = wslot * silu_f(sg) * sv;
+  }
+}
+
+// Kept channel q of the batch's set: its gate and up rows serve every token
+// slot routed to its expert, four tokens per pass over the rows; w a lands in
+// the token's dense [N] slot of wa.
+// gid: the kept channel's global id; info: its expert's first elist entry *
+// 16384 + the expert's token-slot count (read ahead by the caller).
+__device__ void shared_kept_item(const Params& P, int gid, int info, int lane) {
+  const Dims& d = P.d;
+  const int e = gid / d.I, i = gid - e * d.I;
+  const int l0 = info >> 14, l1 = l0 + (info & 16383);
+  const size_t row = (size_t)e * d.I + i;
+  const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
+  const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
+  const int n8 = d.H / 8;
+  constexpr int kU = 8, kTG = 4;
+  for (int g0 = l0; g0 < l1; g0 += kTG) {
+    const int ng = min(kTG, l1 - g0);
+    int tsl[kTG];
+    float sg[kTG], sv[kTG];
+#pragma unroll
+    for (int u = 0; u < kTG; ++u) {   // independent of the rows' loads below
+      tsl[u] = u < ng ? __ldcg(P.elist + g0 + u) : 0;
+      sg[u] = 0.f;
+      sv[u] = 0.f;
+    }
+    for (int h8 = lane; h8 < n8; h8 += 32 * kU) {
+      uint4 gq[kU], vq[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const bool in = h8 + 32 * u < n8;
+        gq[u] = in ? ldg_nc4(g4 + h8 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+        vq[u] = in ? ldg_nc4(v4 + h8 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int tg = 0; tg < kTG; ++tg) {
+        if (tg >= ng) break;
+        const float4* x4 = reinterpret_cast<const float4*>(P.x + (size_t)(tsl[tg] / d.topk) * d.H);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          if (h8 + 32 * u >= n8) break;
+          const float4 xa = x4[2 * (h8 + 32 * u)], xb = x4[2 * (h8 + 32 * u) + 1];
+          dot8(gq[u], xa, xb, sg[tg]);
+          dot8(vq[u], xa, xb, sv[tg]);
+        }
+      }
+    }
+#pragma unroll
+    for (int tg = 0; tg < kTG; ++tg) {
+      if (tg >= ng) break;
+      const float a = warp_sum(sg[tg]), b = warp_sum(sv[tg]);
+      if (lane == 0) {
+        const int ts = tsl[tg], t = ts / d.topk, slot = ts - t * d.topk;
+        P.wa[(size_t)t * d.N + (size_t)slot * d.I + i] = __ldcg(P.w_ws + ts) * silu_f(a) * b;
+      }
+    }
   }
 }
 
@@ -1201,6 +1716,8 @@ __device__ void carry_block(const Params& P, int t, int cb, int ncb, int lane) {
 struct OutWait {
   int flag_t = -1, count_t = -1;
   TokenSlots sl{};
+  int kt = 0;          // the shared kernel: kept channels of token flag_t
+  bool shared_in = false;   // the shared kernel: every kept item of the batch counted
 };
 
 __device__ bool out_wait(const Params& P, const uint32_t* word, uint32_t target, int lane) {
@@ -1211,18 +1728,23 @@ __device__ bool out_wait(const Params& P, const uint32_t* word, uint32_t target,
   return ok != 0;
 }
 
+template <bool SH>
 __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int rc, int lane,
                           int per_tok, OutWait& ow) {
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int c0 = cb * kOutCols + lane * 8;
   const bool on = c0 < d.H;                  // H is a multiple of 8
-  const int qb0 = rc * op.RC, qe = min(P.k, qb0 + op.RC);
+  int qb0 = rc * op.RC, qe = min(P.k, qb0 + op.RC);
   const uint64_t pol = policy_evict_first();  // the last read of these rows
   const float* wa_t = P.wa + (size_t)t * d.N;
   auto counted = [&]() {
     if (ow.count_t == t) return true;
     if (!out_wait(P, P.sync + so.exact + t, (uint32_t)per_tok, lane)) return false;
+    if (SH && !ow.shared_in) {
+      if (!out_wait(P, P.sync + kSyncSdone, (uint32_t)__ldcg(P.sK), lane)) return false;
+      ow.shared_in = true;
+    }
     ow.count_t = t;
     return true;
   };
@@ -1231,6 +1753,26 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
   for (int u = 0; u < 8; ++u) acc[u] = 0.f;
   if (rc >= op.R) {   // recovery chunk: rank components j0 .. j0 + nj - 1 of U c
     const int j0 = (rc - op.R) * kOutBatch, nj = min(kOutBatch, d.r - j0);
+    if (SH) {   // the batch's kept rows are added by the shared chunks
+      uint4 v[kOutBatch];
+#pragma unroll
+      for (int u = 0; u < kOutBatch; ++u)
+        v[u] = u < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(j0 + u) * d.H + c0))
+                            : make_uint4(0u, 0u, 0u, 0u);
+      if (!out_wait(P, P.sync + so.exact + t, (uint32_t)per_tok, lane)) return false;
+      const float cj_l = lane < nj ? __ldcg(P.cvec + (size_t)t * d.r + j0 + lane) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kOutBatch; ++u) {
+        const float cw = __shfl_sync(0xffffffffu, cj_l, u);
+        axpy8h(u < nj ? cw : 0.f, v[u], acc);
+      }
+      if (on) {
+        float4* yo = reinterpret_cast<float4*>(P.y + (size_t)t * d.H + c0);
+        atomicAdd(yo, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        atomicAdd(yo + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+      }
+      return true;
+    }
     uint4 v[kOutBatch];
 #pragma unroll
     for (int u = 0; u < kOutBatch; ++u)   // U^T rows do not depend on the token: load first
@@ -1250,14 +1792,20 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
       if (!out_wait(P, P.sync + so.flag + t, 1u, lane)) return false;
       ow.flag_t = t;
       ow.sl = load_token_slots(P, t, lane);
+      if (SH) ow.kt = __ldcg(P.kcount + t);
+    }
+    if (SH) {   // the token's own kept count, in op.R chunks
+      const int rct = (ow.kt + op.R - 1) / op.R;
+      qb0 = rc * rct;
+      qe = min(ow.kt, qb0 + rct);
     }
     for (int qb = qb0; qb < qe; qb += 32) {
       const int nq = min(32, qe - qb);
-      int slot_l = 0, i_l = 0;
+      int slot_l = 0, i_l = 0, n_l = 0;
       if (lane < nq) {
-        const int n = __ldcg(P.kept + (size_t)t * d.N + qb + lane);
-        slot_l = n / d.I;
-        i_l = n - slot_l * d.I;
+        n_l = __ldcg(P.kept + (size_t)t * d.N + qb + lane);
+        slot_l = n_l / d.I;
+        i_l = n_l - slot_l * d.I;
       }
       const int e_l = slot_expert(ow.sl.e0, ow.sl.e1, slot_l);   // every lane takes part
       const int row_l = e_l * d.I + i_l;
@@ -1283,7 +1831,7 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
         }
         if (!have_w) {   // with the first rows in flight
           if (!counted()) return false;
-          cw_l = lane < nq ? __ldcg(wa_t + qb + lane) : 0.f;
+          cw_l = lane < nq ? __ldcg(wa_t + (SH ? n_l : qb + lane)) : 0.f;
           have_w = true;
         }
 #pragma unroll
@@ -1306,8 +1854,84 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
   return true;
 }
 
+// Output chunk c (rows c RCs .. of the batch's kept list) on column block cb:
+// each kept down row piece is read once and added, weighed by w a, into every
+// token routed to its expert (runs of one expert's rows, four tokens a pass).
+__device__ bool shared_out_chunk(const Params& P, int c, int cb, int RCs, int K, int lane,
+                                 OutWait& ow) {
+  const Dims& d = P.d;
+  if (!ow.shared_in) {
+    if (!out_wait(P, P.sync + kSyncSdone, (uint32_t)K, lane)) return false;
+    ow.shared_in = true;
+  }
+  const int c0 = cb * kOutCols + lane * 8;
+  const bool on = c0 < d.H;
+  const int q0 = c * RCs, q1 = min(K, q0 + RCs);
+  const uint64_t pol = policy_evict_first();
+  constexpr int kTG = 2, kSB = 8;   // tokens a pass, rows a load batch
+  for (int q = q0; q < q1;) {
+    // the next run of rows of one expert (at most 32)
+    const int nq = min(32, q1 - q);
+    const int info_l = lane < nq ? __ldcg(P.sinfo + q + lane) : -1;
+    const int gid_l = lane < nq ? __ldcg(P.skept + q + lane) : 0;
+    const int info = __shfl_sync(0xffffffffu, info_l, 0);
+    const unsigned other = __ballot_sync(0xffffffffu, lane < nq && info_l != info);
+    const int nr = other ? __ffs(other) - 1 : nq;
+    const int l0 = info >> 14, nt = info & 16383;
+    const int e = __shfl_sync(0xffffffffu, gid_l, 0) / d.I;
+    const int i_l = gid_l - e * d.I;
+    for (int g0 = 0; g0 < nt; g0 += kTG) {
+      const int ng = min(kTG, nt - g0);
+      float acc[kTG][8];
+      float cw_l[kTG];
+      int tt[kTG];
+#pragma unroll
+      for (int tg = 0; tg < kTG; ++tg) {
+        const int ts = tg < ng ? __ldcg(P.elist + l0 + g0 + tg) : 0;
+        const int t = ts / d.topk, slot = ts - t * d.topk;
+        tt[tg] = t;
+        cw_l[tg] = tg < ng && lane < nr ? __ldcg(P.wa + (size_t)t * d.N + (size_t)slot * d.I + i_l) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[tg][u] = 0.f;
+      }
+      for (int i0 = 0; i0 < nr; i0 += kSB) {
+        uint4 v[kSB];
+#pragma unroll
+        for (int u = 0; u < kSB; ++u) {
+          const int ii = i0 + u;
+          const int iro = __shfl_sync(0xffffffffu, i_l, ii & 31);
+          v[u] = ii < nr && on ? ldcg4_hint(P.Dt + ((size_t)e * d.I + iro) * d.H + c0, pol)
+                               : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int tg = 0; tg < kTG; ++tg) {
+          if (tg >= ng) break;
+#pragma unroll
+          for (int u = 0; u < kSB; ++u) {
+            const int ii = i0 + u;
+            const float cw = __shfl_sync(0xffffffffu, cw_l[tg], ii & 31);
+            axpy8(ii < nr ? cw : 0.f, v[u], acc[tg]);
+          }
+        }
+      }
+      if (on) {
+#pragma unroll
+        for (int tg = 0; tg < kTG; ++tg) {
+          if (tg >= ng) break;
+          float4* yo = reinterpret_cast<float4*>(P.y + (size_t)tt[tg] * d.H + c0);
+          atomicAdd(yo, make_float4(acc[tg][0], acc[tg][1], acc[tg][2], acc[tg][3]));
+          atomicAdd(yo + 1, make_float4(acc[tg][4], acc[tg][5], acc[tg][6], acc[tg][7]));
+        }
+      }
+    }
+    q += nr;
+  }
+  return true;
+}
+
 // ------------------------------- the kernel --------------------------------
 // One layer's decode by every CTA of the grid.  false: the launch is aborting.
+template <bool SH>
 __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* smem, int* ctl) {
   if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
@@ -1327,15 +1951,81 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   {
     int* flag = &ctl[1];   // static shared memory: the top-k's working area starts at smem
     for (int ts = blockIdx.x; ts < P.B * d.topk; ts += nctas) {
-      const int r = score_task(P, ts, flag);
+      const int r = score_task<SH>(P, ts, flag, smem);
       if (r < 0) return false;
-      if (r > 0) topk_token(P, ts / d.topk, smem);
+      if (!SH && r > 0) topk_token(P, ts / d.topk, smem);
       __syncthreads();
+    }
+    if (SH) {
+      // 1c: each token's share of the batch's kept set (selected by the
+      // score task that completed the last routed expert)
+      for (int t = blockIdx.x; t < P.B; t += nctas) {
+        if (threadIdx.x == 0)
+          *flag = wait_at_least(P.sync + kSyncReady, 1u, abort_flag, P.err);
+        __syncthreads();
+        if (!*flag) return false;
+        shared_token(P, t, smem);
+        __syncthreads();
+      }
     }
   }
   if (stamp && threadIdx.x == 0) stamp[2] = globaltimer();
   // phase 2: kept channels and recovery chunks, one warp each
-  const int per_tok = P.k + d.N / 64;
+  const int per_tok = SH ? d.N / 64 : P.k + d.N / 64;   // items counted per token
+  if (SH) {
+    // the batch's kept channels first (each serving all its tokens), then
+    // every token's recovery chunks
+    if (threadIdx.x == 0) ctl[1] = wait_at_least(P.sync + kSyncReady, 1u, abort_flag, P.err);
+    __syncthreads();
+    if (!ctl[1]) return false;
+    const long long K = __ldcg(P.sK);
+    const long long M = K + (long long)P.B * per_tok;
+    const long long wtot = (long long)nctas * kWarps;
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    const long long ipw = (M + wtot - 1) / wtot;
+    const long long q0 = gw * ipw, q1 = min(M, q0 + ipw);
+    int cur_t = -1, pend_t = -1, pend_n = 0, nk = 0;
+    bool ok = true;
+    long long kb = -64;
+    int gid_l = 0, info_l = 0;   // lane j: kept channel kb + j
+    for (long long q = q0; q < q1; ++q) {
+      if (q < K) {
+        if (q - kb >= 32) {
+          kb = q;
+          gid_l = kb + lane < K ? __ldcg(P.skept + kb + lane) : 0;
+          info_l = kb + lane < K ? __ldcg(P.sinfo + kb + lane) : 0;
+        }
+        const int j = (int)(q - kb);
+        shared_kept_item(P, __shfl_sync(0xffffffffu, gid_l, j), __shfl_sync(0xffffffffu, info_l, j),
+                         lane);
+        ++nk;
+        continue;
+      }
+      const long long r = q - K;
+      const int t = (int)(r / per_tok), ch = (int)(r % per_tok);
+      if (t != cur_t) {
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_at_least(P.sync + so.flag + t, 1u, abort_flag, P.err);
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        cur_t = t;
+      }
+      const bool flush = pend_t >= 0 && pend_t != t;
+      recovery_item(P, t, ch, lane, flush ? pend_t : -1, pend_n);
+      if (flush) pend_n = 0;
+      pend_t = t;
+      ++pend_n;
+    }
+    if (ok) publish_item(P, pend_t, pend_n, lane);
+    if (nk) {
+      __syncwarp();
+      if (lane == 0) red_add_release(P.sync + kSyncSdone, (uint32_t)nk);
+    }
+  } else {
   const long long M = (long long)P.B * per_tok;
   {
     const long long wtot = (long long)nctas * kWarps;
@@ -1379,6 +2069,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     }
     if (ok) publish_item(P, pend_t, pend_n, lane);
   }
+  }
   if (stamp) {
     __syncthreads();
     if (threadIdx.x == 0) stamp[3] = globaltimer();
@@ -1387,7 +2078,32 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   // from the last warp down so that warps without phase-2 work take them
   // first; an item loads its rows once the token's top-k is in and weighs
   // them once the token's phase-2 items are counted
-  {
+  if (SH) {
+    // the batch's kept rows in chunks of RCs rows per column block, then each
+    // token's recovery chunks
+    const int nwarps = nctas * kWarps;
+    const int K = __ldcg(P.sK);
+    const int ncb = (d.H + kOutCols - 1) / kOutCols;
+    const int rec = P.k < d.N ? (d.r + kOutBatch - 1) / kOutBatch : 0;
+    const int RCs = max(1, (int)(((long long)K * ncb + nwarps - 1) / nwarps));
+    const int C = (K + RCs - 1) / RCs;
+    const int items = C * ncb + P.B * ncb * rec;
+    const int gw = blockIdx.x * kWarps + warp;
+    OutPlan op;
+    op.ncb = ncb;
+    op.R = 0;
+    op.RC = 0;
+    op.NR = rec;
+    OutWait ow;
+    for (int it = nwarps - 1 - gw; it < items; it += nwarps) {
+      if (it < C * ncb) {
+        if (!shared_out_chunk(P, it / ncb, it % ncb, RCs, K, lane, ow)) break;
+      } else {
+        const int r = it - C * ncb, t = r / (ncb * rec);
+        if (!out_chunk<SH>(P, op, t, (r / rec) % ncb, r % rec, lane, per_tok, ow)) break;
+      }
+    }
+  } else {
     const int nwarps = nctas * kWarps;
     const OutPlan op = out_plan(P, nwarps);
     const int items = P.B * op.ncb * op.NR;
@@ -1395,7 +2111,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     OutWait ow;
     for (int it = nwarps - 1 - gw; it < items; it += nwarps) {
       const int t = it / (op.ncb * op.NR);
-      if (!out_chunk(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane, per_tok, ow)) break;
+      if (!out_chunk<SH>(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane, per_tok, ow)) break;
       if (P.hnext) {   // a layer of a stack: the block's last item carries the residual
         const int cb = (it / op.NR) % op.ncb;
         __syncwarp();
@@ -1432,6 +2148,12 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       }
     }
     if (threadIdx.x == 0) {
+      if (SH) {
+        for (int q = 0; q < d.E; ++q) P.sync[so.ecount + q] = 0u;
+        P.sync[kSyncBatch] = 0u;
+        P.sync[kSyncReady] = 0u;
+        P.sync[kSyncSdone] = 0u;
+      }
       P.sync[kSyncDone] = 0u;
     }
   }
@@ -1445,10 +2167,17 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
   return raw + ((256u - (smem_addr(raw) & 255u)) & 255u);
 }
 
+// The batch-shared selection variant: one kept set for the whole batch.
+__global__ void __launch_bounds__(kThreads, 1) decode_shared_kernel(const Params P) {
+  extern __shared__ __align__(256) unsigned char smem_raw[];
+  __shared__ int ctl[2];
+  decode_layer<true>(P, aligned_smem(smem_raw), ctl);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  decode_layer(P, aligned_smem(smem_raw), ctl);
+  decode_layer<false>(P, aligned_smem(smem_raw), ctl);
   if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
     // the next layer would wait for inputs that never come
     atomicOr(P.next_err, kErrTimeout);
@@ -1467,6 +2196,14 @@ size_t decode_smem_bytes(const Dims& d) {
 
 size_t sync_words(const Dims& d) { return (size_t)sync_offsets(d).total; }
 
+bool shared_supported(const Dims& d, int B) {
+  // the selection CTA's tables and the score tasks' slot lists fit the
+  // decode's shared memory; the elist packing holds 8192 token slots
+  return shared_select_bytes(d) <= decode_smem_bytes(d) - 256 &&
+         (size_t)(B * d.topk + kWarps + d.E + 4) * 4 <= decode_smem_bytes(d) - 256 &&
+         B * d.topk <= 8192;
+}
+
 cudaError_t configure_decode_kernels(const Dims& d) {
   if (screen_plan(d).bytes == 0) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes(d);
@@ -1475,6 +2212,11 @@ cudaError_t configure_decode_kernels(const Dims& d) {
   if (err != cudaSuccess) return err;
   if ((size_t)fa.maxDynamicSharedSizeBytes < smem)
     err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+  if (err != cudaSuccess) return err;
+  if ((err = cudaFuncGetAttributes(&fa, decode_shared_kernel)) != cudaSuccess) return err;
+  if ((size_t)fa.maxDynamicSharedSizeBytes < smem)
+    err = cudaFuncSetAttribute(decode_shared_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
   return err;
 }
@@ -1536,6 +2278,16 @@ static Params make_params(const moe_reader& h, const float* x, int B, const int3
   P.xnext_ready = nullptr;
   P.next_abort = nullptr;
   P.next_err = nullptr;
+  P.sscore = ws.sscore;
+  P.skept = ws.skept;
+  P.sbits = ws.sbits;
+  P.estart = ws.estart;
+  P.elist = ws.elist;
+  P.kcount = ws.kcount;
+  P.sK = ws.sK;
+  P.sinfo = ws.sinfo;
+  P.ecount = ws.sync + sync_offsets(d).ecount;
+  P.smem_bytes = (int)decode_smem_bytes(d) - 256;
   return P;
 }
 
@@ -1562,7 +2314,8 @@ __global__ void __launch_bounds__(kThreads) stack_input_kernel(const float* h, f
   }
 }
 
-static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStream_t s) {
+static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStream_t s,
+                                 bool shared = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h.grid);
   cfg.blockDim = dim3(kThreads);
@@ -1573,12 +2326,13 @@ static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStrea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, P);
+  return shared ? cudaLaunchKernelEx(&cfg, decode_shared_kernel, P)
+                : cudaLaunchKernelEx(&cfg, decode_kernel, P);
 }
 
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
                           const float* w, int k, float* y, cudaStream_t s, const cudaEvent_t* ev,
-                          unsigned long long* stamps) {
+                          unsigned long long* stamps, bool shared) {
   cudaError_t err;
   unsigned int rec_flags = cudaEventRecordDefault;
   if (ev) {
@@ -1590,7 +2344,7 @@ cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int3
     if ((err = cudaEventRecordWithFlags(ev[0], s, rec_flags)) != cudaSuccess) return err;
   }
   const Params P = make_params(h, x, B, ids, w, k, y, stamps);
-  if ((err = launch_params(h, P, s)) != cudaSuccess) return err;
+  if ((err = launch_params(h, P, s, shared)) != cudaSuccess) return err;
   if (ev && (err = cudaEventRecordWithFlags(ev[1], s, rec_flags)) != cudaSuccess) return err;
   return cudaSuccess;
 }

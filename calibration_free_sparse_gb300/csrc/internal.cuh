@@ -53,6 +53,15 @@ struct Workspace {
   float* y_stage;       // [Bmax][H]
   float* h_stage;       // [Bmax][H]      residual stream entering this layer of a stack
   float* xscale;        // [Bmax]         1 / RMS of that residual, per token
+  // batch-shared selection
+  float* sscore;        // [E][I]         batch scores
+  int32_t* skept;       // [E * I]        the batch's kept global ids, ascending
+  uint32_t* sbits;      // [E][I / 32]    the batch's kept set
+  int32_t* estart;      // [E + 1]        per expert: first entry in elist
+  int32_t* elist;       // [Bmax*topk]    token slots routed to each expert, ascending
+  int32_t* kcount;      // [Bmax]         kept channels per token
+  int32_t* sK;          // [1]            the batch's kept count
+  int32_t* sinfo;       // [E * I]        per kept channel: expert's elist start * 16384 + count
   int32_t* ids_stage;   // [Bmax][topk]
   float* w_stage;       // [Bmax][topk]
   // accounting scratch
@@ -99,6 +108,7 @@ struct moe_reader {
   // last decode
   int has_decode;
   int last_B, last_k;
+  int last_shared;          // the last decode used the batch-shared selection
   cudaStream_t last_stream;
 };
 
@@ -121,9 +131,11 @@ cudaError_t launch_project_b(const Dims& d, const __nv_bfloat16* Dt, const __hal
 // ---- decode launchers (decode.cu) ----
 // `ev` (may be null): 2 events recorded around the kernel; `stamps` (may be
 // null): [grid][5] globaltimer stamps of the phase ends.
+// `shared`: the batch-shared selection kernel (one kept set for the batch).
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
                           const float* w, int k, float* y, cudaStream_t s,
-                          const cudaEvent_t* ev, unsigned long long* stamps);
+                          const cudaEvent_t* ev, unsigned long long* stamps, bool shared = false);
+bool shared_supported(const Dims& d, int B);   // the shared kernel's tables fit at batch B
 // A stack of L layers (distinct handles of equal shape), one launch per layer,
 // with the residual stream h carried on the device: h_0 = h_in, layer l decodes
 // x_l = h_l / RMS(h_l) (formed by layer l's screen into handle l's x_stage), h_{l+1} = h_l + y_l

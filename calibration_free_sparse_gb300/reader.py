@@ -28,7 +28,7 @@ EXPORTED_SYMBOLS = (
     "moe_reader_get_stats", "moe_reader_get_kept", "moe_reader_export_size", "moe_reader_export",
     "moe_reader_get_info", "moe_reader_destroy", "moe_reader_strerror", "moe_reader_abi_version",
     "moe_reader_set_profiling", "moe_reader_read_profile", "moe_reader_topk_noalloc",
-    "moe_reader_decode_stack",
+    "moe_reader_decode_stack", "moe_reader_decode_shared", "moe_reader_get_kept_shared",
 )
 PHASES = ("decode", "screen", "score_topk", "exact", "out")
 
@@ -80,6 +80,10 @@ def _lib():
         lib.moe_reader_decode_host.restype = ctypes.c_int
         lib.moe_reader_decode_stack.argtypes = [vp, i32, vp, i32, vp, vp, i32, vp, vp, vp]
         lib.moe_reader_decode_stack.restype = ctypes.c_int
+        lib.moe_reader_decode_shared.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp]
+        lib.moe_reader_decode_shared.restype = ctypes.c_int
+        lib.moe_reader_get_kept_shared.argtypes = [vp, vp, i64, ctypes.POINTER(ctypes.c_int32)]
+        lib.moe_reader_get_kept_shared.restype = ctypes.c_int
         lib.moe_reader_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.moe_reader_status.restype = ctypes.c_int
         lib.moe_reader_get_stats.argtypes = [vp, ctypes.POINTER(Stats)]
@@ -219,6 +223,25 @@ class MoeReader:
         code = _lib().moe_reader_decode(self._h, _ptr(x), B, _ptr(ids), _ptr(w), int(k), _ptr(y),
                                         _stream(stream))
         _check(code, "moe_reader_decode")
+
+    def decode_shared(self, x, ids, w, k, y, stream=None):
+        """Enqueue one decode of B = x.shape[0] tokens with one kept set for
+        the whole batch (device tensors)."""
+        B = int(x.shape[0])
+        code = _lib().moe_reader_decode_shared(self._h, _ptr(x), B, _ptr(ids), _ptr(w), int(k),
+                                               _ptr(y), _stream(stream))
+        _check(code, "moe_reader_decode_shared")
+
+    def kept_shared(self):
+        """The last shared decode's kept set: ascending global ids (host int32)."""
+        K = ctypes.c_int32(0)
+        code = _lib().moe_reader_get_kept_shared(self._h, None, 0, ctypes.byref(K))
+        if code not in (OK, EINVAL):
+            _check(code, "moe_reader_get_kept_shared")
+        out = np.zeros(max(1, K.value), np.int32)
+        _check(_lib().moe_reader_get_kept_shared(self._h, _ptr(out), out.size, ctypes.byref(K)),
+               "moe_reader_get_kept_shared")
+        return out[:K.value]
 
     def decode_host(self, x, ids, w, k, y=None, stream=None):
         """Decode with host numpy buffers; returns y (host, fp32 [B][H])."""

@@ -157,6 +157,36 @@ int moe_reader_decode(moe_reader_t* h, const float* x, int32_t B, const int32_t*
                       const float* expert_w, int32_t k, float* y, void* stream);
 
 /*
+ * moe_reader_decode_shared -- one decode step of B tokens with ONE kept set
+ * for the whole batch (batch-shared selection, the direction the Chinese
+ * summary page's 未来方向 (1) names for keeping the gains at larger batches).
+ * Arguments, alignment, errors and asynchrony as for moe_reader_decode.
+ *
+ * Every token is screened and scored as in moe_reader_decode.  The union of
+ * the batch's routed channels (all I channels of each of the n_e distinct
+ * routed experts) is ranked by the batch score S(e, i) = the sum of s_t(e, i)
+ * over the tokens routed to e, in token order (fp32).  The top
+ * K = round_half_up(k * n_e / topk) channels are kept (ties to the lower
+ * global id e*I + i); each token computes its routed channels in that set
+ * exactly, reading each kept gate/up row once for all its tokens, and
+ * recovers its other routed channels with its own estimates.  At B = 1 this
+ * is moe_reader_decode.  Needs B*topk + 16 and the selection's tables
+ * (about 21 KB + E*I/8 bytes) to fit the decode's shared memory: EINVAL
+ * otherwise.  After it, moe_reader_get_kept answers ESTATE; use
+ * moe_reader_get_kept_shared.  Statistics count the union of the tokens'
+ * reads as for moe_reader_decode.
+ */
+int moe_reader_decode_shared(moe_reader_t* h, const float* x, int32_t B, const int32_t* expert_ids,
+                             const float* expert_w, int32_t k, float* y, void* stream);
+
+/* moe_reader_get_kept_shared -- the kept set of the last shared decode:
+ * host int32 [K] global ids e*I + i, ascending; *count (host, may be NULL)
+ * receives K even when capacity < K (then EINVAL).  Synchronizes the
+ * decode's stream.  ESTATE if the last decode was not a shared one. */
+int moe_reader_get_kept_shared(moe_reader_t* h, int32_t* kept_host, int64_t capacity,
+                               int32_t* count);
+
+/*
  * moe_reader_decode_host -- the same decode with HOST buffers: copies x, ids
  * and w to the handle's device staging area, decodes, copies y back and
  * synchronizes `stream`.  Arguments as for moe_reader_decode but every array
@@ -222,7 +252,8 @@ int moe_reader_get_stats(moe_reader_t* h, moe_reader_stats* out);
 
 /* moe_reader_get_kept -- kept global channel ids e*I + i of the last decode,
  * ascending per token: host int32 [B][k], `capacity` >= B*k entries.
- * Synchronizes the last decode's stream.  ESTATE if no decode. */
+ * Synchronizes the last decode's stream.  ESTATE if no decode or if the last
+ * decode was a shared one (its tokens keep different counts). */
 int moe_reader_get_kept(moe_reader_t* h, int32_t* kept_host, int64_t capacity);
 
 /* Exportable arrays (moe_reader_export).  Prepared data: */
