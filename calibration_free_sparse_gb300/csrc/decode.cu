@@ -1631,6 +1631,7 @@ __device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
 
 constexpr int kOutCols = 256;        // columns of an output block: 8 per lane
 constexpr int kOutBatch = 12;        // kept rows whose loads a warp issues together
+constexpr int kOutRows = 48;         // kept rows of an output item at most
 
 struct OutPlan {
   int ncb;   // output blocks
@@ -1647,7 +1648,8 @@ __device__ __forceinline__ OutPlan out_plan(const Params& P, int nwarps) {
   // the recovery U c comes in chunks of kOutBatch rank components
   const int rec = P.k < P.d.N ? (P.d.r + kOutBatch - 1) / kOutBatch : 0;
   int R = nwarps / per - rec;                 // one round of warp items,
-  R = min(R, (P.k + kOutBatch - 1) / kOutBatch);   // each at least one full load batch
+  R = min(R, (P.k + kOutBatch - 1) / kOutBatch);   // each at least one full load batch,
+  R = max(R, (P.k + kOutRows - 1) / kOutRows);     // at most kOutRows rows (large batches)
   R = max(1, min(R, P.k));
   op.RC = (P.k + R - 1) / R;
   op.R = op.RC > 0 ? (P.k + op.RC - 1) / op.RC : 1;
