@@ -216,6 +216,53 @@ def unpack_codes(packed: np.ndarray, I: int) -> np.ndarray:
     return out
 
 
+# 1.6 bit per trit: five trits per byte ([CN] §方法步骤详情 load-time (1): a
+# 128-coordinate block of 256 BF16 bytes shrinks to about 30 bytes; 128 trits
+# at 8/5 bits are 26 bytes, plus the FP16 scale and the FP16 rho)
+TRIT5_DIGIT = {0: 0, 1: 1, -1: 2}   # the base-3 digit of a trit (the 2-bit code order)
+
+
+def run_bytes5(I: int) -> int:
+    """Bytes of one coordinate run of five-trit bytes (I channels, 5 per byte)."""
+    return (I + 4) // 5
+
+
+def run_stride5(I: int) -> int:
+    """Five-trit run length padded to whole 32-byte sectors."""
+    return 32 * math.ceil(run_bytes5(I) / 32)
+
+
+def pack_codes5(t: np.ndarray) -> np.ndarray:
+    """Five trits per byte along the last axis (channels): byte j holds
+    channels 5j .. 5j+4 as sum_m digit(t[5j+m]) * 3^m, digit 0 -> 0, +1 -> 1,
+    -1 -> 2 (at most 242).  Zero-padded to a whole number of 32-byte sectors."""
+    I = t.shape[-1]
+    q = np.where(t == 1, 1, np.where(t == -1, 2, 0)).astype(np.int64)
+    padI = 5 * run_bytes5(I)
+    if padI != I:
+        q = np.concatenate([q, np.zeros(q.shape[:-1] + (padI - I,), np.int64)], axis=-1)
+    q = q.reshape(q.shape[:-1] + (padI // 5, 5))
+    packed = (q * (3 ** np.arange(5))).sum(axis=-1).astype(np.uint8)
+    stride = run_stride5(I)
+    if stride != packed.shape[-1]:
+        packed = np.concatenate(
+            [packed, np.zeros(packed.shape[:-1] + (stride - packed.shape[-1],), np.uint8)], axis=-1)
+    return packed
+
+
+def unpack_codes5(packed: np.ndarray, I: int) -> np.ndarray:
+    """Inverse of pack_codes5: int8 trits [..., I]."""
+    b = packed[..., : run_bytes5(I)].astype(np.int64)
+    if np.any(b > 242):
+        raise ValueError("invalid five-trit byte (> 242)")
+    digits = np.stack([(b // 3 ** m) % 3 for m in range(5)], axis=-1)
+    digits = digits.reshape(b.shape[:-1] + (5 * b.shape[-1],))[..., :I]
+    out = np.zeros(digits.shape, np.int8)
+    out[digits == 1] = 1
+    out[digits == 2] = -1
+    return out
+
+
 @dataclass
 class ExpertSketch:
     """Sketch of one expert: trits t[gv][I][nb][128] (gv 0 = gate, 1 = up),

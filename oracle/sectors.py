@@ -12,7 +12,8 @@ as documented for the library:
 
   codes   u8   [E][nb][128][2][S]   S = ceil(ceil(I/4)/32)*32; a screened
                                     coordinate reads its gate run and its up run,
-                                    ceil(I/4) bytes each
+                                    ceil(I/4) bytes each (five-trit layout:
+                                    ceil(I/5) bytes, S = ceil(ceil(I/5)/32)*32)
   scales  f16  [E][nb][2][I]        a routed expert reads all of them
   dnorm   f32  [E][I]               a routed expert reads all of them
   G, V    bf16 [E][I][H]            a kept channel reads its row
@@ -52,16 +53,20 @@ def _ranges_to_sectors(starts: np.ndarray, length: int) -> np.ndarray:
     return np.unique(ids)
 
 
-def decode_sectors(shape, ids, masks, kept):
+def decode_sectors(shape, ids, masks, kept, codes="2bit"):
     """Distinct 32-byte sectors read per parameter array for one decode call.
 
     shape: oracle.reader.Shape; ids: int [B][topk] routed experts;
     masks: bool [B][nb][128] screened coordinates per token;
-    kept: list of B arrays of kept global channel ids (e*I + i).
+    kept: list of B arrays of kept global channel ids (e*I + i);
+    codes: "2bit" (4 trits a byte) or "trit5" (5 trits a byte: runs of
+    ceil(I/5) bytes, the 1.6-bit layout).
     Returns dict array-name -> sector count, plus "dense" (the denominator).
     """
     E, I, H, r, nb = shape.E, shape.I, shape.H, shape.r, shape.nb
-    run = (I + 3) // 4
+    if codes not in ("2bit", "trit5"):
+        raise ValueError(codes)
+    run = (I + 3) // 4 if codes == "2bit" else (I + 4) // 5
     stride = SECTOR * ((run + SECTOR - 1) // SECTOR)
     B = len(ids)
 
