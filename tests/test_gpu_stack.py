@@ -215,3 +215,46 @@ def test_qwen3_30b_stack_properties(qwen3_stack):
         assert np.array_equal(rd.kept(B, WL.k), kept[l]), l
         yl = yl.cpu().numpy()
         assert np.abs(yl - y[l]).max() <= 1e-5 * np.abs(y[l]).max(), l
+
+
+def test_qwen3_30b_48_layer_stack():
+    """The 48-layer stack of Qwen3-30B-A3B-shaped layers (independent weights
+    per layer, residual carried) at batch 1 and 8 and at the 17.8% and 12.8%
+    budgets: every layer's status clean, the fp32 residual chain exact, and
+    sampled layers equal to a lone decode of their input."""
+    torch = _torch()
+    from calibration_free_sparse_gb300.reader import MoeReader
+
+    L = 48
+    readers, keep = [], []
+    for l in range(L):
+        g, v, d = S.weights_device(400 + l, WL.E, WL.I, WL.H, "cuda")
+        sigma = S.signs(400 + l, R.Shape(H=WL.H, E=WL.E, topk=WL.topk, I=WL.I).Hp)
+        readers.append(MoeReader(WL.H, WL.E, WL.topk, WL.I, g, v, d, sigma, screen_coords=WL.c,
+                                 rank=WL.r, max_batch=8))
+        keep.append((g, v))
+        del d
+    torch.cuda.synchronize()
+    try:
+        for B, k in ((1, WL.k), (8, WL.k), (8, S.QWEN3_30B_LOW.k)):
+            h0 = S.activations(500 + B + k, B, WL.H)
+            ids, w = routing_stack(L, B, WL.E, WL.topk, seed=600 + B)
+            h_out, y = run_stack(readers, h0, ids, w, k)
+            for rd in readers:
+                assert rd.status() == (0, 0)
+            hs = fp32_chain(h0, y)
+            assert np.array_equal(h_out, hs[-1])
+            assert np.isfinite(h_out).all()
+            for l in (0, 23, 47):
+                kept = readers[l].kept(B, k)
+                x = torch.from_numpy(kernel_input(hs[l])).cuda()
+                yl = torch.empty_like(x)
+                readers[l].decode(x, torch.from_numpy(ids[l]).cuda(), torch.from_numpy(w[l]).cuda(),
+                                  k, yl)
+                torch.cuda.synchronize()
+                assert readers[l].status() == (0, 0)
+                assert np.array_equal(readers[l].kept(B, k), kept), (B, k, l)
+                assert np.abs(yl.cpu().numpy() - y[l]).max() <= 1e-5 * np.abs(y[l]).max(), (B, k, l)
+    finally:
+        for rd in readers:
+            rd.close()
