@@ -644,7 +644,8 @@ __host__ __device__ inline size_t shared_select_bytes(const Dims& d) {
          (size_t)kCandMax * 12 + (size_t)d.E * (d.I / 32) * 4 + 256;
 }
 
-// The batch's kept set, by the CTA that completed the last batch-score task.
+// The batch's kept set, by the CTA whose score task completed the last routed
+// expert (all batch scores are in).
 __device__ void shared_select(const Params& P, unsigned char* smem) {
   const Dims& d = P.d;
   const int BT = P.B * d.topk, E = d.E, I = d.I, IW = d.I / 32;
@@ -1774,18 +1775,19 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
         atomicAdd(yo + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
       }
       return true;
-    }
-    uint4 v[kOutBatch];
+    } else {
+      uint4 v[kOutBatch];
 #pragma unroll
-    for (int u = 0; u < kOutBatch; ++u)   // U^T rows do not depend on the token: load first
-      v[u] = u < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(j0 + u) * d.H + c0))
-                          : make_uint4(0u, 0u, 0u, 0u);
-    if (!counted()) return false;
-    const float cj_l = lane < nj ? __ldcg(P.cvec + (size_t)t * d.r + j0 + lane) : 0.f;
+      for (int u = 0; u < kOutBatch; ++u)   // U^T rows do not depend on the token: load first
+        v[u] = u < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(j0 + u) * d.H + c0))
+                            : make_uint4(0u, 0u, 0u, 0u);
+      if (!counted()) return false;
+      const float cj_l = lane < nj ? __ldcg(P.cvec + (size_t)t * d.r + j0 + lane) : 0.f;
 #pragma unroll
-    for (int u = 0; u < kOutBatch; ++u) {
-      const float cw = __shfl_sync(0xffffffffu, cj_l, u);
-      axpy8h(u < nj ? cw : 0.f, v[u], acc);
+      for (int u = 0; u < kOutBatch; ++u) {
+        const float cw = __shfl_sync(0xffffffffu, cj_l, u);
+        axpy8h(u < nj ? cw : 0.f, v[u], acc);
+      }
     }
   } else {
     // the rows come from the kept list and the expert ids alone (known at the
