@@ -534,6 +534,72 @@ def decode(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int):
 
 
 # --------------------------------------------------------------------------
+# full screen ranked by the expected squared output error (budgets >= 28.7%)
+# --------------------------------------------------------------------------
+def silu_grad(z):
+    """d/dz z sigmoid(z)."""
+    sg = 1.0 / (1.0 + np.exp(-z))
+    return sg * (1.0 + z * (1.0 - sg))
+
+
+def expected_skip_error(layer: Layer, x: np.ndarray, ids, w):
+    """[topk][I] expected squared output error of skipping each routed channel
+    under the full screen ([CN] §方法步骤详情 decode (2): from the 28.7% budget
+    the whole sketch is read and rho_b ranks channels by the expected squared
+    output error after skipping; the pages give no formula, the reading here):
+
+    - skipping j leaves w_j (a_j d_j - p_j U b_j) in the output (the exact
+      term missing, its recovery present); with U orthonormal and a_j = p_j +
+      err, its expected squared norm is
+      w_j^2 (p_j^2 (||d_j||^2 - ||b_j||^2) + var(a_j) ||d_j||^2), the first
+      term clamped at 0 (FP16 b can exceed the FP32 ||d_j|| by rounding);
+    - var(a_j) = (phi'(ghat_j) vhat_j)^2 var(g_j) + phi(ghat_j)^2 var(v_j)
+      (first order in the sketch errors, which are taken as independent);
+    - var(g_j) = sum_b rho^g_{j,b} ||(Rx)_b||^2: the block's ternary error has
+      mean square rho_b per coordinate and meets Rx_b in every coordinate;
+      var(v_j) likewise.
+    Uses the stored FP16 rho and b and the FP32 ||d_j||."""
+    sh = layer.shape
+    if sh.c != BLOCK:
+        raise ValueError("the expected-error ranking uses the full screen (c = 128)")
+    sc = screen_token(layer, x, ids, w)
+    Rx = rotate(pad_hidden(np.asarray(x, dtype=np.float64), sh.Hp), layer.sigma).reshape(sh.nb, BLOCK)
+    rn2 = (Rx * Rx).sum(axis=1)                                  # [nb]
+    wv = np.asarray(w, dtype=np.float64)
+    out = np.zeros((len(ids), sh.I))
+    for s_, e in enumerate(int(v) for v in ids):
+        rho = layer.sketch(e).rho.astype(np.float64)             # [nb][2][I]
+        var_g = rn2 @ rho[:, 0, :]
+        var_v = rn2 @ rho[:, 1, :]
+        g, v = sc.ghat[s_], sc.vhat[s_]
+        var_a = (silu_grad(g) * v) ** 2 * var_g + silu(g) ** 2 * var_v
+        dn2 = layer.dnorm(e).astype(np.float64) ** 2
+        bn2 = (layer.b(e).astype(np.float64) ** 2).sum(axis=1)
+        out[s_] = wv[s_] ** 2 * (sc.p[s_] ** 2 * np.maximum(dn2 - bn2, 0.0) + var_a * dn2)
+    return sc, out
+
+
+def decode_token_rho(layer: Layer, x: np.ndarray, ids, w, k: int) -> TokenResult:
+    """One token with the full screen and the top-k by expected_skip_error
+    (ties to the lower global id); kept channels exact, the rest recovered."""
+    sh = layer.shape
+    sc, err = expected_skip_error(layer, x, ids, w)
+    gid = np.array([[int(e) * sh.I + i for i in range(sh.I)] for e in ids], dtype=np.int64)
+    flat, flat_id = err.reshape(-1), gid.reshape(-1)
+    order = np.lexsort((flat_id, -flat))
+    kth = float(flat[order[k - 1]]) if k > 0 else float("nan")
+    nxt = float(flat[order[k]]) if k < flat.size else float("nan")
+    keep = np.zeros(flat.size, bool)
+    keep[order[:k]] = True
+    y_exact, y_rec = exact_and_recovery(layer, x, ids, w, sc.p, keep.reshape(len(ids), sh.I))
+    return TokenResult(
+        y=y_exact + y_rec, y_exact=y_exact, y_recovery=y_rec,
+        kept=np.sort(flat_id[order[:k]]), kept_order=flat_id[order[:k]],
+        score=err, p=sc.p, ghat=sc.ghat, vhat=sc.vhat, mask=sc.mask,
+        kth_score=kth, next_score=nxt)
+
+
+# --------------------------------------------------------------------------
 # batch-shared selection
 # --------------------------------------------------------------------------
 @dataclass
