@@ -17,7 +17,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int check_config(const moe_reader_config* c) {
   if (!c) return MOE_READER_EINVAL;
-  if (c->flags != 0) return MOE_READER_EINVAL;
+  if (c->flags != 0 && c->flags != MOE_READER_FLAG_RHO_RANK) return MOE_READER_EINVAL;
+  if ((c->flags & MOE_READER_FLAG_RHO_RANK) && c->screen_coords != mr::kBlock)
+    return MOE_READER_EINVAL;   // the expected-error ranking reads the whole sketch
   if (c->hidden < 8 || c->hidden % 8 != 0 || c->hidden > 65536) return MOE_READER_EINVAL;
   if (c->num_experts < 1 || c->num_experts > 65536) return MOE_READER_EINVAL;
   if (c->experts_per_token < 1 || c->experts_per_token > std::min(c->num_experts, mr::kMaxTopk))
@@ -46,6 +48,7 @@ Dims make_dims(const moe_reader_config& c) {
   const int run = (d.I + 3) / 4;
   d.S = ((run + mr::kSector - 1) / mr::kSector) * mr::kSector;
   d.runW = d.I / 16;
+  d.rho_rank = (c.flags & MOE_READER_FLAG_RHO_RANK) ? 1 : 0;
   return d;
 }
 
@@ -199,6 +202,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t o_b = pa.take((size_t)d.E * d.I * d.r * 2);
   const size_t o_sigma = pa.take((size_t)d.Hp);
   const size_t o_eig = pa.take((size_t)d.r * 8);
+  const size_t o_bn2 = pa.take((size_t)d.E * d.I * 4);
   void* pbase = nullptr;
   cudaError_t ce = cudaMalloc(&pbase, pa.off);
   if (ce != cudaSuccess) {
@@ -210,6 +214,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->p.scales = reinterpret_cast<__half*>(pb + o_scales);
   h->p.rho = reinterpret_cast<__half*>(pb + o_rho);
   h->p.dnorm = reinterpret_cast<float*>(pb + o_dnorm);
+  h->p.bnorm2 = reinterpret_cast<float*>(pb + o_bn2);
   h->p.Dt = reinterpret_cast<__nv_bfloat16*>(pb + o_dt);
   h->p.U = reinterpret_cast<__half*>(pb + o_u);
   h->p.Ut = reinterpret_cast<__half*>(pb + o_ut);
@@ -245,6 +250,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_ys = wa.take(Bm * d.H * 4);
   const size_t w_hs = wa.take(Bm * d.H * 4);
   const size_t w_xsc = wa.take(Bm * 4);
+  const size_t w_rn2 = wa.take(Bm * d.nb * 4);
   const size_t EI = (size_t)d.E * d.I;
   const size_t w_ssc = wa.take(EI * 4);
   const size_t w_skp = wa.take(EI * 4);
@@ -287,6 +293,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   h->ws.y_stage = reinterpret_cast<float*>(wb + w_ys);
   h->ws.h_stage = reinterpret_cast<float*>(wb + w_hs);
   h->ws.xscale = reinterpret_cast<float*>(wb + w_xsc);
+  h->ws.rn2 = reinterpret_cast<float*>(wb + w_rn2);
   h->ws.sscore = reinterpret_cast<float*>(wb + w_ssc);
   h->ws.skept = reinterpret_cast<int32_t*>(wb + w_skp);
   h->ws.sbits = reinterpret_cast<uint32_t*>(wb + w_sbt);
@@ -322,6 +329,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
     if (st != MOE_READER_OK) break;
     if ((ce = mr::launch_transpose_u(d, h->p.U, h->p.Ut, s)) != cudaSuccess) break;
     if ((ce = mr::launch_project_b(d, h->p.Dt, h->p.U, h->p.b, s)) != cudaSuccess) break;
+    if ((ce = mr::launch_bnorm2(d, h->p.b, h->p.bnorm2, s)) != cudaSuccess) break;
     if ((ce = mr::configure_decode_kernels(d)) != cudaSuccess) break;
     h->grid = mr::decode_grid(d);
     if (h->grid <= 0) {

@@ -145,6 +145,10 @@ struct Params {
   int32_t* sK;            // [1]           the batch's kept count
   int32_t* sinfo;         // [E * I]       per kept channel: its expert's first elist entry
                           //               * 16384 + the expert's token-slot count
+  // the expected-error ranking (d.rho_rank)
+  const __half* rho;      // [E][nb][2][I] block mean squared ternary error
+  const float* bnorm2;    // [E][I]        ||b_j||^2
+  float* rn2;             // [Bmax][nb]    ||(R x)_b||^2
   uint32_t* ecount;       // [E]           per expert: score tasks in (synchronisation)
   int smem_bytes;         // dynamic shared memory of a CTA (after alignment)
 };
@@ -1090,6 +1094,10 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     const int uu = unit_of(n), b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk, slot = ts % d.topk;
     uint32_t word[4];
     rotate_select_loaded(P, lane, xu, word);
+    if (d.rho_rank) {   // ||(R x)_b||^2 for the expected-error ranking (every slot writes it)
+      const float ss = warp_sum(xu[0] * xu[0] + xu[1] * xu[1] + xu[2] * xu[2] + xu[3] * xu[3]);
+      if (lane == 0) P.rn2[(size_t)t * d.nb + b] = ss;
+    }
     // the unit's side outputs: the block's screened set (the same from every
     // slot), the input checks, and at block 0 the slot's sanitised expert id
     // and weight (and, for slot 0, the token's zeroed recovery vector); the
@@ -1384,7 +1392,25 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
       if (h == 1 && !two) break;
       const int ii = h ? i2 : i;
       const float pv = silu_f(g[h]) * v[h];
-      const float sc = wv * dn[h] * fabsf(pv);
+      float sc = wv * dn[h] * fabsf(pv);
+      if (d.rho_rank) {
+        // the expected squared output error that skipping leaves:
+        // w^2 (p^2 max(|d|^2 - |b|^2, 0) + var(a) |d|^2), var(a) to first order
+        float var_g = 0.f, var_v = 0.f;
+        for (int bb2 = 0; bb2 < d.nb; ++bb2) {
+          const float r2 = __ldcg(P.rn2 + (size_t)t * d.nb + bb2);
+          const __half* rb = P.rho + (((size_t)e * d.nb + bb2) * 2) * I + ii;
+          var_g = fmaf(__half2float(rb[0]), r2, var_g);
+          var_v = fmaf(__half2float(rb[I]), r2, var_v);
+        }
+        const float sg = 1.f / (1.f + expf(-g[h]));
+        const float dphi = sg * (1.f + g[h] * (1.f - sg));
+        const float phi = g[h] * sg;
+        const float var_a = (dphi * v[h]) * (dphi * v[h]) * var_g + phi * phi * var_v;
+        const float dn2 = dn[h] * dn[h];
+        const float keep2 = fmaxf(dn2 - __ldg(P.bnorm2 + (size_t)e * I + ii), 0.f);
+        sc = wv * wv * (pv * pv * keep2 + var_a * dn2);
+      }
       const size_t o = (size_t)t * d.N + (size_t)slot * I + ii;
       P.ghat[o] = g[h];
       P.vhat[o] = v[h];
@@ -2290,6 +2316,9 @@ static Params make_params(const moe_reader& h, const float* x, int B, const int3
   P.kcount = ws.kcount;
   P.sK = ws.sK;
   P.sinfo = ws.sinfo;
+  P.rho = h.p.rho;
+  P.bnorm2 = h.p.bnorm2;
+  P.rn2 = ws.rn2;
   P.ecount = ws.sync + sync_offsets(d).ecount;
   P.smem_bytes = (int)decode_smem_bytes(d) - 256;
   return P;

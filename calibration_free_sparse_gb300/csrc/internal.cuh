@@ -32,6 +32,7 @@ struct Dims {
   int Hp, nb, N;
   int S;            // bytes per coordinate run (multiple of 32)
   int runW;         // 32-bit words of codes per run actually used: I / 16
+  int rho_rank;     // 1: full screen ranked by the expected skip error
 };
 
 // Decode workspace (device), sized for Bmax tokens.
@@ -53,6 +54,7 @@ struct Workspace {
   float* y_stage;       // [Bmax][H]
   float* h_stage;       // [Bmax][H]      residual stream entering this layer of a stack
   float* xscale;        // [Bmax]         1 / RMS of that residual, per token
+  float* rn2;           // [Bmax][nb]     ||(R x)_b||^2 (the expected-error ranking)
   // batch-shared selection
   float* sscore;        // [E][I]         batch scores
   int32_t* skept;       // [E * I]        the batch's kept global ids, ascending
@@ -83,6 +85,7 @@ struct Prepared {
   __half* U;            // [H][r]
   __half* Ut;           // [r][H]  U transposed: rank components as rows
   __half* b;            // [E][I][r]
+  float* bnorm2;        // [E][I]  ||b_j||^2 of the stored FP16 b
   int8_t* sigma;        // [Hp]
   double* eigvals;      // [r]
 };
@@ -125,6 +128,7 @@ cudaError_t launch_dnorm(const Dims& d, const __nv_bfloat16* Dt, float* dnorm, c
 int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, double* eigvals,
                          cudaStream_t s);
 cudaError_t launch_transpose_u(const Dims& d, const __half* U, __half* Ut, cudaStream_t s);
+cudaError_t launch_bnorm2(const Dims& d, const __half* b, float* bnorm2, cudaStream_t s);
 cudaError_t launch_project_b(const Dims& d, const __nv_bfloat16* Dt, const __half* U, __half* b,
                              cudaStream_t s);
 

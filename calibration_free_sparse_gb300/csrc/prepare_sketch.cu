@@ -169,6 +169,18 @@ dnorm_kernel(Dims d, const __nv_bfloat16* __restrict__ Dt, float* __restrict__ d
   if (lane == 0) dnorm[row] = __double2float_rn(__dsqrt_rn(acc));
 }
 
+// ||b_j||^2 of the stored FP16 coefficients, one thread per channel.
+__global__ void bnorm2_kernel(Dims d, const __half* __restrict__ b, float* __restrict__ out) {
+  const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= (long long)d.E * d.I) return;
+  float s = 0.f;
+  for (int j = 0; j < d.r; ++j) {
+    const float v = __half2float(b[q * d.r + j]);
+    s = fmaf(v, v, s);
+  }
+  out[q] = s;
+}
+
 // b_j = U^T d_j for every channel (FP16 U, BF16 d, fp32 accumulation of
 // exact products, FP16 result).  CTA = 64 channels; tiles of 128 coordinates.
 constexpr int kBRows = 64;
@@ -260,6 +272,12 @@ cudaError_t launch_dnorm(const Dims& d, const __nv_bfloat16* Dt, float* dnorm, c
 cudaError_t launch_transpose_u(const Dims& d, const __half* U, __half* Ut, cudaStream_t s) {
   const int n = d.H * d.r;
   transpose_u_kernel<<<(n + 255) / 256, 256, 0, s>>>(d.H, d.r, U, Ut);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bnorm2(const Dims& d, const __half* b, float* bnorm2, cudaStream_t s) {
+  const long long n = (long long)d.E * d.I;
+  bnorm2_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(d, b, bnorm2);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmoe_reader.so")
 
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EDEVICE, ESTATE, ETOOBIG = 0, -1, -2, -3, -4, -5, -6, -7
+FLAG_RHO_RANK = 0x1   # full screen ranked by the expected skip error (screen_coords = 128)
 ERR_EXPERT_RANGE, ERR_EXPERT_DUP, ERR_WEIGHT, ERR_X_NONFINITE, ERR_TIMEOUT = 1, 2, 4, 8, 16
 ARRAYS = ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")
 
@@ -183,10 +184,10 @@ class MoeReader:
     ([E][I][H], [E][I][H], [E][H][I]); gate and up must outlive the reader."""
 
     def __init__(self, hidden, num_experts, experts_per_token, inter, gate, up, down, sigma,
-                 screen_coords=80, rank=32, max_batch=16, stream=None):
+                 screen_coords=80, rank=32, max_batch=16, stream=None, flags=0):
         lib = _lib()
         self.cfg = Config(hidden, num_experts, experts_per_token, inter, screen_coords, rank,
-                          max_batch, 0)
+                          max_batch, flags)
         sig = np.ascontiguousarray(sigma, dtype=np.int8)
         self._keep = (gate, up)
         h = ctypes.c_void_p()

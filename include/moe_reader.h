@@ -72,8 +72,20 @@ typedef struct {
   int32_t screen_coords;      /* c: coordinates screened per block, 1..128 (80 = partial screen) */
   int32_t rank;               /* r: recovery rank, 1 <= r <= min(H, 64) */
   int32_t max_batch;          /* B_max: 1..1024 tokens per decode (workspace sizing) */
-  int32_t flags;              /* reserved, must be 0 */
+  int32_t flags;              /* 0, or MOE_READER_FLAG_RHO_RANK */
 } moe_reader_config;
+
+/* Full-screen ranking (Chinese summary page, 方法步骤详情 decode (2): from the
+ * 28.7% budget the whole sketch is read and rho_b ranks channels by the
+ * expected squared output error after skipping).  Needs screen_coords = 128.
+ * The score of channel j becomes
+ *   w_j^2 (p_j^2 max(||d_j||^2 - ||b_j||^2, 0) + var(a_j) ||d_j||^2),
+ *   var(a_j) = (phi'(ghat_j) vhat_j)^2 var(g_j) + phi(ghat_j)^2 var(v_j),
+ *   var(g_j) = sum_b rho^g_{j,b} ||(R x)_b||^2 (likewise var(v_j)),
+ * the expected squared norm of what skipping leaves, w_j (a_j d_j - p_j U b_j),
+ * to first order in the sketch errors; the top-k and everything after it are
+ * unchanged. */
+#define MOE_READER_FLAG_RHO_RANK 0x1
 
 /* Read accounting of the last decode, in 32-byte sectors.  Every parameter
  * array starts on a 256-byte boundary; a count is the number of distinct

@@ -22,7 +22,7 @@ def to_device_bf16(bits, torch):
 class Pair:
     """The same layer prepared by the CUDA library and described to the oracle."""
 
-    def __init__(self, H, E, topk, I, c, r, max_batch, seed=0, device_weights=False):
+    def __init__(self, H, E, topk, I, c, r, max_batch, seed=0, device_weights=False, flags=0):
         import torch
 
         from calibration_free_sparse_gb300.reader import MoeReader
@@ -37,7 +37,7 @@ class Pair:
         self.sigma = S.signs(seed, self.shape.Hp)
         self.dev = (g, v, d)
         self.reader = MoeReader(H, E, topk, I, g, v, d, self.sigma, screen_coords=c, rank=r,
-                                max_batch=max_batch)
+                                max_batch=max_batch, flags=flags)
         self.layer = R.Layer(self.shape, self.G, self.V, self.D, self.sigma)
 
     def tokens(self, B, seed):
