@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-shared", action="store_true")
+    ap.add_argument("--rho-rank", action="store_true",
+                    help="also time the full-screen expected-error ranking (screen_coords 128, "
+                         "28.7%% budget) on four layers")
     ap.add_argument("--large-batch", action="store_true",
                     help="also time the GPT-OSS-120B-shaped layer at batch 1-128, per-token "
                          "against batch-shared selection")
@@ -285,6 +288,64 @@ def traffic_for(kernel, batch):
     if not ent or ent.get("decode_cu_sha256_16") != digest or ent.get("batch") != batch:
         return None
     return ent.get("bytes_per_launch")
+
+
+def rho_rank_timing(torch, dev, stream, args, batches, nl=4):
+    """The full-screen expected-error ranking (MOE_READER_FLAG_RHO_RANK) on nl
+    Qwen3-30B-shaped layers at the 28.7% budget: microseconds per decode and
+    the read fraction of the first layer, one CUDA graph per batch."""
+    from calibration_free_sparse_gb300 import synthetic as S
+    from calibration_free_sparse_gb300.reader import FLAG_RHO_RANK, MoeReader
+
+    wl = S.QWEN3_30B
+    k = S.budget_to_k(0.287, wl.N)
+    readers, keep = [], []
+    for l in range(nl):
+        g, v, d = S.weights_device(700 + l, wl.E, wl.I, wl.H, dev)
+        readers.append(MoeReader(wl.H, wl.E, wl.topk, wl.I, g, v, d, S.signs(700 + l, wl.Hp),
+                                 screen_coords=128, rank=wl.r, max_batch=max(batches),
+                                 flags=FLAG_RHO_RANK))
+        keep.append((g, v))
+        del d
+    out = {"workload": wl.name, "k": k, "screen_coords": 128, "layers": nl, "per_batch": {}}
+    for B in batches:
+        x = torch.from_numpy(S.activations(7, B, wl.H)).to(dev)
+        ids, w = S.routing(7, B, wl.E, wl.topk)
+        ids, w = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
+        y = torch.empty_like(x)
+
+        def run():
+            for rd in readers:
+                rd.decode(x, ids, w, k, y)
+        with torch.cuda.stream(stream):
+            run()
+        st = readers[0].stats()
+        frac = sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")) / st["dense"]
+        for rd in readers:
+            code, bits = rd.status()
+            if code != 0:
+                raise RuntimeError(f"rho rank: device status {code} bits {bits}")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            run()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        reps = max(3, min(args.steps, 20))
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        us = 1000.0 * ev0.elapsed_time(ev1) / (reps * nl)
+        out["per_batch"][str(B)] = {"us_per_decode": us, "tokens_per_s": B / (us / 1e6),
+                                    "read_fraction": frac}
+    for rd in readers:
+        rd.close()
+    return out
 
 
 def large_batch_stress(torch, dev, stream, args, nl=6, batches=(1, 16, 64, 128)):
@@ -594,6 +655,9 @@ def run_ours(args, wl, world, rank, local):
     large = None
     if args.large_batch and rank == 0:
         large = large_batch_stress(torch, dev, stream, args)
+    rho = None
+    if args.rho_rank and rank == 0:
+        rho = rho_rank_timing(torch, dev, stream, args, batches)
 
     # -- end to end through the host-buffer C ABI (pinned host memory)
     e2e = None
@@ -675,6 +739,7 @@ def run_ours(args, wl, world, rank, local):
             "stack": stack,
             "shared": shared,
             "large_batch": large,
+            "rho_rank": rho,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
