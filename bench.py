@@ -50,12 +50,14 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--no-shared", action="store_true")
-    ap.add_argument("--rho-rank", action="store_true",
-                    help="also time the full-screen expected-error ranking (screen_coords 128, "
-                         "28.7%% budget) on four layers")
-    ap.add_argument("--large-batch", action="store_true",
-                    help="also time the GPT-OSS-120B-shaped layer at batch 1-128, per-token "
-                         "against batch-shared selection")
+    ap.add_argument("--no-rho-rank", action="store_true",
+                    help="skip the full-screen expected-error ranking (screen_coords 128, "
+                         "28.7%% budget)")
+    ap.add_argument("--no-large-batch", action="store_true",
+                    help="skip the GPT-OSS-120B-shaped layer at batch 1-128 (per-token against "
+                         "batch-shared selection)")
+    ap.add_argument("--no-235b", action="store_true",
+                    help="skip the Qwen3-235B-A22B-shaped layer at the 12.8%% budget")
     return ap.parse_args()
 
 
@@ -290,98 +292,54 @@ def traffic_for(kernel, batch):
     return ent.get("bytes_per_launch")
 
 
-def rho_rank_timing(torch, dev, stream, args, batches, nl=4):
-    """The full-screen expected-error ranking (MOE_READER_FLAG_RHO_RANK) on nl
-    Qwen3-30B-shaped layers at the 28.7% budget: microseconds per decode and
-    the read fraction of the first layer, one CUDA graph per batch."""
-    from calibration_free_sparse_gb300 import synthetic as S
-    from calibration_free_sparse_gb300.reader import FLAG_RHO_RANK, MoeReader
-
-    wl = S.QWEN3_30B
-    k = S.budget_to_k(0.287, wl.N)
-    readers, keep = [], []
-    for l in range(nl):
-        g, v, d = S.weights_device(700 + l, wl.E, wl.I, wl.H, dev)
-        readers.append(MoeReader(wl.H, wl.E, wl.topk, wl.I, g, v, d, S.signs(700 + l, wl.Hp),
-                                 screen_coords=128, rank=wl.r, max_batch=max(batches),
-                                 flags=FLAG_RHO_RANK))
-        keep.append((g, v))
-        del d
-    out = {"workload": wl.name, "k": k, "screen_coords": 128, "layers": nl, "per_batch": {}}
-    for B in batches:
-        x = torch.from_numpy(S.activations(7, B, wl.H)).to(dev)
-        ids, w = S.routing(7, B, wl.E, wl.topk)
-        ids, w = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
-        y = torch.empty_like(x)
-
-        def run():
-            for rd in readers:
-                rd.decode(x, ids, w, k, y)
-        with torch.cuda.stream(stream):
-            run()
-        st = readers[0].stats()
-        frac = sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")) / st["dense"]
-        for rd in readers:
-            code, bits = rd.status()
-            if code != 0:
-                raise RuntimeError(f"rho rank: device status {code} bits {bits}")
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            run()
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                graph.replay()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        reps = max(3, min(args.steps, 20))
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(reps):
-                graph.replay()
-            ev1.record(stream)
-        torch.cuda.synchronize()
-        us = 1000.0 * ev0.elapsed_time(ev1) / (reps * nl)
-        out["per_batch"][str(B)] = {"us_per_decode": us, "tokens_per_s": B / (us / 1e6),
-                                    "read_fraction": frac}
-    for rd in readers:
-        rd.close()
-    return out
-
-
-def large_batch_stress(torch, dev, stream, args, nl=6, batches=(1, 16, 64, 128)):
-    """Per-token against batch-shared selection on nl GPT-OSS-120B-shaped
-    layers (17.8% budget): microseconds per layer decode and the read fraction
-    of the first layer, one CUDA graph per (mode, batch)."""
+def layer_sweep(torch, dev, stream, args, wl, k, batches, nl, seed0, modes=("per_token",),
+                screen_coords=None, flags=0):
+    """Decode time of nl prepared layers of workload wl at each batch (one CUDA
+    graph per (mode, batch) cycling the layers, so their weights are not in
+    L2), with the sector-accounted bytes of every layer's decode: microseconds
+    per decode, layer-tokens/s, read fraction, GB/s and its fraction of the
+    measured copy bandwidth."""
     from calibration_free_sparse_gb300 import synthetic as S
     from calibration_free_sparse_gb300.reader import MoeReader
 
-    wl = S.GPT_OSS_120B
+    c = wl.c if screen_coords is None else screen_coords
     readers, keep = [], []
     for l in range(nl):
-        g, v, d = S.weights_device(300 + l, wl.E, wl.I, wl.H, dev)
-        readers.append(MoeReader(wl.H, wl.E, wl.topk, wl.I, g, v, d, S.signs(300 + l, wl.Hp),
-                                 screen_coords=wl.c, rank=wl.r, max_batch=max(batches)))
+        g, v, d = S.weights_device(seed0 + l, wl.E, wl.I, wl.H, dev)
+        readers.append(MoeReader(wl.H, wl.E, wl.topk, wl.I, g, v, d, S.signs(seed0 + l, wl.Hp),
+                                 screen_coords=c, rank=wl.r, max_batch=max(batches), flags=flags))
         keep.append((g, v))
         del d
-    out = {"workload": wl.name, "k": wl.k, "layers": nl, "per_batch": {}}
+    torch.cuda.empty_cache()
+    peak, _ = measured_peaks()
+    out = {"workload": wl.name, "H": wl.H, "E": wl.E, "topk": wl.topk, "I": wl.I, "k": k,
+           "screen_coords": c, "r": wl.r, "layers": nl, "per_batch": {}}
     for B in batches:
-        x = torch.from_numpy(S.activations(5, B, wl.H)).to(dev)
-        ids, w = S.routing(5, B, wl.E, wl.topk)
-        ids, w = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
-        y = torch.empty_like(x)
+        xs, idw = [], []
+        for l in range(nl):
+            sd = seed0 + 50_000 + 100 * B + l
+            xs.append(torch.from_numpy(S.activations(sd, B, wl.H)).to(dev))
+            ids, w = S.routing(sd, B, wl.E, wl.topk)
+            idw.append((torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)))
+        y = torch.empty((B, wl.H), device=dev)
         row = {}
-        for mode in ("per_token", "shared"):
+        for mode in modes:
             def run(mode=mode):
-                for rd in readers:
-                    (rd.decode_shared if mode == "shared" else rd.decode)(x, ids, w, wl.k, y)
+                for l, rd in enumerate(readers):
+                    fn = rd.decode_shared if mode == "shared" else rd.decode
+                    fn(xs[l], idw[l][0], idw[l][1], k, y)
+            sbytes = dbytes = 0
             with torch.cuda.stream(stream):
-                run()
-            st = readers[0].stats()
-            frac = sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")) / st["dense"]
-            for rd in readers:
-                code, bits = rd.status()
-                if code != 0:
-                    raise RuntimeError(f"large batch: device status {code} bits {bits}")
+                for l, rd in enumerate(readers):
+                    fn = rd.decode_shared if mode == "shared" else rd.decode
+                    fn(xs[l], idw[l][0], idw[l][1], k, y)
+                    st = rd.stats()
+                    sbytes += 32 * sum(st[a] for a in ("codes", "scales", "dnorm", "G", "V", "Dt",
+                                                        "b", "U"))
+                    dbytes += 32 * st["dense"]
+                    code, bits = rd.status()
+                    if code != 0:
+                        raise RuntimeError(f"{wl.name} {mode}: device status {code} bits {bits}")
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 run()
@@ -398,10 +356,17 @@ def large_batch_stress(torch, dev, stream, args, nl=6, batches=(1, 16, 64, 128))
                 ev1.record(stream)
             torch.cuda.synchronize()
             us = 1000.0 * ev0.elapsed_time(ev1) / (reps * nl)
-            row[mode] = {"us_per_decode": us, "tokens_per_s": B / (us / 1e6), "read_fraction": frac}
-        out["per_batch"][str(B)] = row
+            gbs = (sbytes / nl) / (us * 1e-6) / 1e9
+            row[mode] = {"us_per_decode": us, "tokens_per_s": B / (us * 1e-6),
+                         "sector_bytes_per_decode": sbytes / nl, "read_fraction": sbytes / dbytes,
+                         "hbm_gbs": gbs, "frac_of_measured_peak": gbs / peak}
+        if "shared" in row and "per_token" in row:
+            row["shared"]["vs_per_token"] = row["per_token"]["us_per_decode"] / row["shared"]["us_per_decode"]
+        out["per_batch"][str(B)] = row if len(modes) > 1 else row[modes[0]]
     for rd in readers:
         rd.close()
+    del keep
+    torch.cuda.empty_cache()
     return out
 
 
@@ -651,13 +616,25 @@ def run_ours(args, wl, world, rank, local):
                          "vs_independent_decodes compares with the headline's unchained "
                          "per-layer decodes, which carry no residual" % L)
 
-    # -- large-batch stress: the GPT-OSS-120B-shaped layer, both selections
-    large = None
-    if args.large_batch and rank == 0:
-        large = large_batch_stress(torch, dev, stream, args)
-    rho = None
-    if args.rho_rank and rank == 0:
-        rho = rho_rank_timing(torch, dev, stream, args, batches)
+    # -- the other configurations of the workload family, each on its own
+    # prepared layers (informational keys; the headline is the Qwen3-30B layer)
+    large = q235 = rho = None
+    if not args.no_235b:
+        wl2 = S.QWEN3_235B
+        q235 = layer_sweep(torch, dev, stream, args, wl2, wl2.k, (1, 4, 8, 16), 6,
+                           2000 + 7919 * rank)
+        q235["budget"] = 0.128
+    if not args.no_large_batch:
+        wl3 = S.GPT_OSS_120B
+        large = layer_sweep(torch, dev, stream, args, wl3, wl3.k, (1, 4, 8, 16, 32, 64, 128), 6,
+                            300 + 7919 * rank, modes=("per_token", "shared"))
+        large["budget"] = 0.178
+    if not args.no_rho_rank:
+        from calibration_free_sparse_gb300.reader import FLAG_RHO_RANK
+
+        rho = layer_sweep(torch, dev, stream, args, wl, S.budget_to_k(0.287, wl.N), batches, 4,
+                          700 + 7919 * rank, screen_coords=128, flags=FLAG_RHO_RANK)
+        rho["budget"] = 0.287
 
     # -- end to end through the host-buffer C ABI (pinned host memory)
     e2e = None
@@ -738,6 +715,7 @@ def run_ours(args, wl, world, rank, local):
             "roofline": roofline,
             "stack": stack,
             "shared": shared,
+            "qwen3_235b": q235,
             "large_batch": large,
             "rho_rank": rho,
             "cpu_baseline": cpu,

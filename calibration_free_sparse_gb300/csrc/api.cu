@@ -5,11 +5,16 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "internal.cuh"
 
 namespace {
+
+// Pending one-shot fault injections that are not tied to a handle.
+std::atomic<int> g_fail_next_alloc{0};
+std::atomic<int> g_stall_next_prepare{0};
 
 using mr::Dims;
 
@@ -150,6 +155,18 @@ cudaError_t launch_profiled(moe_reader* h, const float* x, int B, const int32_t*
 
 }  // namespace
 
+namespace mr {
+
+cudaError_t device_alloc(void** p, size_t bytes) {
+  *p = nullptr;
+  if (g_fail_next_alloc.exchange(0)) return cudaErrorMemoryAllocation;
+  return cudaMalloc(p, bytes);
+}
+
+bool take_prepare_stall() { return g_stall_next_prepare.exchange(0) != 0; }
+
+}  // namespace mr
+
 extern "C" {
 
 int moe_reader_abi_version(void) { return MOE_READER_ABI_VERSION; }
@@ -204,10 +221,10 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t o_eig = pa.take((size_t)d.r * 8);
   const size_t o_bn2 = pa.take((size_t)d.E * d.I * 4);
   void* pbase = nullptr;
-  cudaError_t ce = cudaMalloc(&pbase, pa.off);
+  cudaError_t ce = mr::device_alloc(&pbase, pa.off);
   if (ce != cudaSuccess) {
     free(h);
-    return MOE_READER_ENOMEM;
+    return cuda_status(ce);
   }
   char* pb = static_cast<char*>(pbase);
   h->p.codes = reinterpret_cast<uint8_t*>(pb + o_codes);
@@ -269,11 +286,11 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
   const size_t w_cnt = wa.take(16 * 8);
   const size_t w_err = wa.take(4);
   void* wbase = nullptr;
-  ce = cudaMalloc(&wbase, wa.off);
+  ce = mr::device_alloc(&wbase, wa.off);
   if (ce != cudaSuccess) {
     cudaFree(pbase);
     free(h);
-    return MOE_READER_ENOMEM;
+    return cuda_status(ce);
   }
   char* wb = static_cast<char*>(wbase);
   h->ws.mask = reinterpret_cast<uint32_t*>(wb + w_mask);
@@ -325,7 +342,7 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
         cudaSuccess)
       break;
     if ((ce = mr::launch_dnorm(d, h->p.Dt, h->p.dnorm, s)) != cudaSuccess) break;
-    st = mr::build_recovery_basis(d, h->p.Dt, h->p.U, h->p.eigvals, s);
+    st = mr::build_recovery_basis(d, h->p.Dt, h->p.U, h->p.eigvals, s, mr::take_prepare_stall());
     if (st != MOE_READER_OK) break;
     if ((ce = mr::launch_transpose_u(d, h->p.U, h->p.Ut, s)) != cudaSuccess) break;
     if ((ce = mr::launch_project_b(d, h->p.Dt, h->p.U, h->p.b, s)) != cudaSuccess) break;
@@ -359,6 +376,7 @@ int moe_reader_decode(moe_reader_t* h, const float* x, int32_t B, const int32_t*
   if ((const void*)x == (const void*)y) return MOE_READER_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t ce = launch_profiled(h, x, B, expert_ids, expert_w, k, y, s);
+  h->inject = 0;
   if (ce != cudaSuccess) return cuda_status(ce);
   h->has_decode = 1;
   h->last_B = B;
@@ -379,6 +397,7 @@ int moe_reader_decode_shared(moe_reader_t* h, const float* x, int32_t B, const i
   if (!mr::shared_supported(h->d, B)) return MOE_READER_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t ce = launch_profiled(h, x, B, expert_ids, expert_w, k, y, s, true);
+  h->inject = 0;
   if (ce != cudaSuccess) return cuda_status(ce);
   h->has_decode = 1;
   h->last_B = B;
@@ -424,9 +443,9 @@ int moe_reader_decode_host(moe_reader_t* h, const float* x_host, int32_t B,
   if ((ce = cudaMemcpyAsync(h->ws.w_stage, w_host, (size_t)B * d.topk * 4, cudaMemcpyHostToDevice,
                             s)) != cudaSuccess)
     return cuda_status(ce);
-  if ((ce = launch_profiled(h, h->ws.x_stage, B, h->ws.ids_stage, h->ws.w_stage, k,
-                            h->ws.y_stage, s)) != cudaSuccess)
-    return cuda_status(ce);
+  ce = launch_profiled(h, h->ws.x_stage, B, h->ws.ids_stage, h->ws.w_stage, k, h->ws.y_stage, s);
+  h->inject = 0;
+  if (ce != cudaSuccess) return cuda_status(ce);
   h->has_decode = 1;
   h->last_B = B;
   h->last_k = k;
@@ -482,6 +501,7 @@ int moe_reader_decode_stack(moe_reader_t* const* layers, int32_t L, const float*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t ce =
       mr::launch_decode_stack(layers, L, h_in, B, expert_ids, expert_w, k, h_out, y_layers, s);
+  for (int l = 0; l < L; ++l) layers[l]->inject = 0;
   if (ce != cudaSuccess) return cuda_status(ce);
   for (int l = 0; l < L; ++l) {
     layers[l]->has_decode = 1;
@@ -490,6 +510,26 @@ int moe_reader_decode_stack(moe_reader_t* const* layers, int32_t L, const float*
     layers[l]->last_shared = 0;
     layers[l]->last_stream = s;
   }
+  return MOE_READER_OK;
+}
+
+int moe_reader_set_wait_limit(moe_reader_t* h, uint64_t ns) {
+  if (!h) return MOE_READER_EINVAL;
+  h->wait_ns = ns;
+  return MOE_READER_OK;
+}
+
+int moe_reader_inject_fault(moe_reader_t* h, uint32_t what) {
+  const uint32_t handle_bits = MOE_READER_INJECT_DECODE_STALL;
+  const uint32_t global_bits = MOE_READER_INJECT_PREPARE_STALL | MOE_READER_INJECT_ALLOC_FAIL;
+  if (what == 0 || (what & ~(handle_bits | global_bits))) return MOE_READER_EINVAL;
+  if (h ? (what & global_bits) != 0 : (what & handle_bits) != 0) return MOE_READER_EINVAL;
+  if (h) {
+    h->inject |= what;
+    return MOE_READER_OK;
+  }
+  if (what & MOE_READER_INJECT_PREPARE_STALL) g_stall_next_prepare.store(1);
+  if (what & MOE_READER_INJECT_ALLOC_FAIL) g_fail_next_alloc.store(1);
   return MOE_READER_OK;
 }
 
@@ -551,8 +591,8 @@ int moe_reader_get_kept(moe_reader_t* h, int32_t* kept_host, int64_t capacity) {
   if (n == 0) return MOE_READER_OK;
   cudaStream_t s = h->last_stream;
   int32_t* dev = nullptr;
-  cudaError_t ce = cudaMalloc(&dev, (size_t)n * 4);
-  if (ce != cudaSuccess) return MOE_READER_ENOMEM;
+  cudaError_t ce = mr::device_alloc(reinterpret_cast<void**>(&dev), (size_t)n * 4);
+  if (ce != cudaSuccess) return cuda_status(ce);
   do {
     if ((ce = mr::launch_gather_kept(*h, B, k, dev, s)) != cudaSuccess) break;
     if ((ce = cudaMemcpyAsync(kept_host, dev, (size_t)n * 4, cudaMemcpyDeviceToHost, s)) !=
@@ -601,8 +641,9 @@ int moe_reader_set_profiling(moe_reader_t* h, int32_t enable) {
         const cudaError_t ce = cudaEventCreate(&h->prof_ev[i][j]);
         if (ce != cudaSuccess) return cuda_status(ce);
       }
-    const cudaError_t ce = cudaMalloc(
-        &h->prof_stamps, (size_t)mr::kProfSlots * h->grid * 5 * sizeof(unsigned long long));
+    const cudaError_t ce = mr::device_alloc(
+        reinterpret_cast<void**>(&h->prof_stamps),
+        (size_t)mr::kProfSlots * h->grid * 5 * sizeof(unsigned long long));
     if (ce != cudaSuccess) return cuda_status(ce);
     h->prof_created = 1;
   }

@@ -30,7 +30,6 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr unsigned long long kWaitNs = 1000000000ull;
 
 // Shared-memory plan of the screen (host-computed, passed to the kernel).
 constexpr size_t kSmemBudget = 226 * 1024 - 256;   // dynamic shared memory: 227 KB less static, slack
@@ -151,6 +150,8 @@ struct Params {
   float* rn2;             // [Bmax][nb]    ||(R x)_b||^2
   uint32_t* ecount;       // [E]           per expert: score tasks in (synchronisation)
   int smem_bytes;         // dynamic shared memory of a CTA (after alignment)
+  unsigned long long wait_ns;   // bound of every wait (globaltimer nanoseconds)
+  int stall;              // fault injection: score tasks wait for one screen unit too many
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -216,23 +217,10 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Wait (one thread) until *flag >= target.  false: timed out or aborted.
-__device__ bool wait_at_least(const uint32_t* flag, uint32_t target, uint32_t* abort_flag,
-                              uint32_t* err) {
-  if (ld_acquire(flag) >= target) return true;
-  const unsigned long long t0 = globaltimer();
-  while (true) {
-    // poll without ordering; the acquire load orders what follows once it is met
-    if (ld_relaxed(flag) >= target && ld_acquire(flag) >= target) return true;
-    if (ld_relaxed(abort_flag)) return false;
-    if (globaltimer() - t0 > kWaitNs) {
-      atomicOr(err, kErrTimeout);
-      atomicExch(abort_flag, 1u);
-      return false;
-    }
-    __nanosleep(64);
-  }
-}
+// Wait (one thread) until *flag >= target, for at most P.wait_ns of the
+// global timer.  false: timed out (the timeout bit and the launch's abort
+// flag are raised) or another wait of the launch timed out first.
+__device__ bool wait_at_least(const Params& P, const uint32_t* flag, uint32_t target);
 
 // Offsets (in uint32) of the synchronisation area, fixed per handle.
 // slot .. exact: the decode's own hand-offs; cbdone .. ssum: the residual
@@ -255,6 +243,23 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   return o;
 }
 constexpr int kSyncDone = 0, kSyncAbort = 2;
+
+__device__ bool wait_at_least(const Params& P, const uint32_t* flag, uint32_t target) {
+  if (ld_acquire(flag) >= target) return true;
+  uint32_t* abort_flag = P.sync + kSyncAbort;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    // poll without ordering; the acquire load orders what follows once it is met
+    if (ld_relaxed(flag) >= target && ld_acquire(flag) >= target) return true;
+    if (ld_relaxed(abort_flag)) return false;
+    if (globaltimer() - t0 > P.wait_ns) {
+      atomicOr(P.err, kErrTimeout);
+      atomicExch(abort_flag, 1u);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
 // the shared kernel's batch-wide hand-offs: routed experts scored, the
 // batch's kept set released, shared kept items done
 constexpr int kSyncBatch = 5, kSyncReady = 6, kSyncSdone = 7;
@@ -1080,7 +1085,7 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
     if (P.xwait) {   // a stacked layer: token t's input comes from the layer before
       int ok = 1;
-      if (lane == 0) ok = wait_at_least(P.xwait + t, 1u, P.sync + kSyncAbort, P.err);
+      if (lane == 0) ok = wait_at_least(P, P.xwait + t, 1u);
       __shfl_sync(0xffffffffu, ok, 0);   // on a timeout the abort flag ends the launch
       __syncwarp();
     }
@@ -1342,8 +1347,7 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
   const SyncOff so = sync_offsets(d);
   const int t = ts / d.topk, slot = ts % d.topk, I = d.I;
   if (threadIdx.x == 0)
-    *flag = wait_at_least(P.sync + so.slot + ts, (uint32_t)(d.nb * P.sp.tw), P.sync + kSyncAbort,
-                          P.err);
+    *flag = wait_at_least(P, P.sync + so.slot + ts, (uint32_t)(d.nb * P.sp.tw + P.stall));
   __syncthreads();
   if (!*flag) return -1;
   int e = P.ids_in[ts];
@@ -1751,7 +1755,7 @@ struct OutWait {
 
 __device__ bool out_wait(const Params& P, const uint32_t* word, uint32_t target, int lane) {
   int ok = 1;
-  if (lane == 0) ok = wait_at_least(word, target, P.sync + kSyncAbort, P.err);
+  if (lane == 0) ok = wait_at_least(P, word, target);
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
@@ -1968,7 +1972,6 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   const SyncOff so = sync_offsets(d);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nctas = gridDim.x;
-  uint32_t* abort_flag = P.sync + kSyncAbort;
   unsigned long long* stamp = P.stamps ? P.stamps + (size_t)blockIdx.x * 5 : nullptr;
   if (stamp && threadIdx.x == 0) stamp[0] = globaltimer();
 
@@ -1991,7 +1994,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       // score task that completed the last routed expert)
       for (int t = blockIdx.x; t < P.B; t += nctas) {
         if (threadIdx.x == 0)
-          *flag = wait_at_least(P.sync + kSyncReady, 1u, abort_flag, P.err);
+          *flag = wait_at_least(P, P.sync + kSyncReady, 1u);
         __syncthreads();
         if (!*flag) return false;
         shared_token(P, t, smem);
@@ -2005,7 +2008,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   if (SH) {
     // the batch's kept channels first (each serving all its tokens), then
     // every token's recovery chunks
-    if (threadIdx.x == 0) ctl[1] = wait_at_least(P.sync + kSyncReady, 1u, abort_flag, P.err);
+    if (threadIdx.x == 0) ctl[1] = wait_at_least(P, P.sync + kSyncReady, 1u);
     __syncthreads();
     if (!ctl[1]) return false;
     const long long K = __ldcg(P.sK);
@@ -2035,7 +2038,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       const int t = (int)(r / per_tok), ch = (int)(r % per_tok);
       if (t != cur_t) {
         int w_ok = 1;
-        if (lane == 0) w_ok = wait_at_least(P.sync + so.flag + t, 1u, abort_flag, P.err);
+        if (lane == 0) w_ok = wait_at_least(P, P.sync + so.flag + t, 1u);
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) {
           ok = false;
@@ -2072,7 +2075,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       const int t = (int)(q / per_tok), local = (int)(q % per_tok);
       if (t != cur_t) {
         int w_ok = 1;
-        if (lane == 0) w_ok = wait_at_least(P.sync + so.flag + t, 1u, abort_flag, P.err);
+        if (lane == 0) w_ok = wait_at_least(P, P.sync + so.flag + t, 1u);
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) {
           ok = false;
@@ -2321,6 +2324,8 @@ static Params make_params(const moe_reader& h, const float* x, int B, const int3
   P.rn2 = ws.rn2;
   P.ecount = ws.sync + sync_offsets(d).ecount;
   P.smem_bytes = (int)decode_smem_bytes(d) - 256;
+  P.wait_ns = h.wait_ns ? (unsigned long long)h.wait_ns : kDefaultWaitNs;
+  P.stall = (h.inject & MOE_READER_INJECT_DECODE_STALL) ? 1 : 0;
   return P;
 }
 

@@ -109,6 +109,8 @@ struct moe_reader {
   cudaEvent_t prof_ev[mr::kProfSlots][2];
   unsigned long long* prof_stamps;      // device [kProfSlots][grid][5]
   // last decode
+  uint64_t wait_ns;          // bound of every device-side wait (0: the default)
+  uint32_t inject;           // MOE_READER_INJECT_DECODE_STALL pending for the next decode
   int has_decode;
   int last_B, last_k;
   int last_shared;          // the last decode used the batch-shared selection
@@ -117,6 +119,14 @@ struct moe_reader {
 
 namespace mr {
 
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;   // one second
+
+// Every device allocation of the library goes through here (api.cu), so a
+// test can make one fail on purpose (MOE_READER_INJECT_ALLOC_FAIL).
+cudaError_t device_alloc(void** p, size_t bytes);
+// One-shot injection of a stall at the next prepare's grid barrier.
+bool take_prepare_stall();
+
 // ---- prepare launchers (prepare_sketch.cu / prepare_svd.cu) ----
 cudaError_t launch_sketch(const Dims& d, const __nv_bfloat16* G, const __nv_bfloat16* V,
                           const int8_t* sigma, uint8_t* codes, __half* scales, __half* rho,
@@ -124,9 +134,10 @@ cudaError_t launch_sketch(const Dims& d, const __nv_bfloat16* G, const __nv_bflo
 cudaError_t launch_transpose_down(const Dims& d, const __nv_bfloat16* D, __nv_bfloat16* Dt,
                                   cudaStream_t s);
 cudaError_t launch_dnorm(const Dims& d, const __nv_bfloat16* Dt, float* dnorm, cudaStream_t s);
-// Recovery basis: U (fp16 [H][r]) and eigenvalues from Dt; returns ETIMEOUT via *timeout.
+// Recovery basis: U (fp16 [H][r]) and eigenvalues from Dt; OK, ENOMEM, ECUDA or
+// ETIMEOUT (a grid barrier ran out; `stall` adds one CTA the barrier never sees).
 int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, double* eigvals,
-                         cudaStream_t s);
+                         cudaStream_t s, bool stall = false);
 cudaError_t launch_transpose_u(const Dims& d, const __half* U, __half* Ut, cudaStream_t s);
 cudaError_t launch_bnorm2(const Dims& d, const __half* b, float* bnorm2, cudaStream_t s);
 cudaError_t launch_project_b(const Dims& d, const __nv_bfloat16* Dt, const __half* U, __half* b,

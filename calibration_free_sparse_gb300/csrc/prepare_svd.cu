@@ -152,13 +152,14 @@ __device__ double block_sum_d(double v, double* red) {
 __global__ void __launch_bounds__(512)
 tridiag_kernel(int n, double* __restrict__ A, double* __restrict__ dg, double* __restrict__ eg,
                double* __restrict__ tau, double* __restrict__ vscale, double* __restrict__ p,
-               double* __restrict__ part, GridSync* gs, uint32_t* err) {
+               double* __restrict__ part, GridSync* gs, uint32_t* err, unsigned int extra) {
   extern __shared__ double sm[];
   double* v = sm;            // [n]
   double* w = sm + n;        // [n]
   double* red = sm + 2 * n;  // [32]
   __shared__ double bcast;
   const unsigned int P = gridDim.x;
+  const unsigned int arrivals = P + extra;   // extra > 0 only under fault injection
   const int warps = blockDim.x >> 5, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Wtot = (int)P * warps;
   const int gw = blockIdx.x * warps + wid;
@@ -202,7 +203,7 @@ tridiag_kernel(int n, double* __restrict__ A, double* __restrict__ dg, double* _
       for (int q = 0; q < warps; ++q) t += red[q];
       __stcg(part + blockIdx.x, t);
     }
-    if (!grid_barrier(gs, P)) goto fail;
+    if (!grid_barrier(gs, arrivals)) goto fail;
 
     if (threadIdx.x == 0) {
       double t = 0.0;
@@ -230,7 +231,7 @@ tridiag_kernel(int n, double* __restrict__ A, double* __restrict__ dg, double* _
       tau[k] = tk;
       vscale[k] = scale;
     }
-    if (!grid_barrier(gs, P)) goto fail;
+    if (!grid_barrier(gs, arrivals)) goto fail;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (n >= 2) {
@@ -461,7 +462,7 @@ __global__ void canonical_kernel(int n, int r, const double* __restrict__ Z, __h
 }  // namespace
 
 int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, double* eigvals,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool stall) {
   const int n = d.H, r = d.r, K = d.E * d.I;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_READER_ECUDA;
@@ -477,7 +478,11 @@ int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, doub
                          (size_t)n * r;
   const size_t bytes = doubles * sizeof(double) + (size_t)n * r + sizeof(GridSync) + 64;
   void* base = nullptr;
-  if (cudaMalloc(&base, bytes) != cudaSuccess) return MOE_READER_ENOMEM;
+  {
+    const cudaError_t ae = device_alloc(&base, bytes);
+    if (ae == cudaErrorMemoryAllocation) return MOE_READER_ENOMEM;
+    if (ae != cudaSuccess) return MOE_READER_ECUDA;
+  }
   double* M = static_cast<double*>(base);
   double* dg = M + nn;
   double* eg = dg + n;
@@ -518,7 +523,8 @@ int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, doub
     }
     const int grid = sms;   // one CTA per SM: co-resident under a cooperative launch
     int nn_arg = n;
-    void* args[] = {&nn_arg, &M, &dg, &eg, &tau, &vsc, &p, &part, &gs, &err};
+    unsigned int extra = stall ? 1u : 0u;
+    void* args[] = {&nn_arg, &M, &dg, &eg, &tau, &vsc, &p, &part, &gs, &err, &extra};
     if ((ce = cudaLaunchCooperativeKernel((void*)tridiag_kernel, dim3(grid), dim3(512), args, smem,
                                           s)) != cudaSuccess)
       break;

@@ -24,9 +24,12 @@ std::mutex g_setup_mu;
 void* g_scratch_ptr[kNoAllocMaxDevices];
 bool g_scratch_ready[kNoAllocMaxDevices];
 
-// Order-preserving map of an fp32 value to uint32 (larger float -> larger key).
+// Order-preserving map of an fp32 value to uint32 (larger float -> larger
+// key).  Values that compare equal get equal keys: -0 maps like +0, and every
+// NaN (either sign, any payload) maps to the largest key, above +infinity.
 __device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+  if (f != f) return 0xffffffffu;
+  const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -71,6 +74,7 @@ topk_noalloc_kernel(const float* __restrict__ scores, const int32_t* __restrict_
   __shared__ int hist[256];
   __shared__ int sh[2];
   __shared__ int wsum[32];
+  __shared__ int wsum2[32];
   const int row = blockIdx.x;
   uint32_t* keys = reinterpret_cast<uint32_t*>(scratch) + (size_t)row * N;
   uint32_t* keys2 = reinterpret_cast<uint32_t*>(scratch) + total + (size_t)row * N;
@@ -113,38 +117,59 @@ topk_noalloc_kernel(const float* __restrict__ scores, const int32_t* __restrict_
       T2 = row_radix_select(keys2, valid, N, need, hist, sh, &dummy);
     }
   }
-  // compact the kept columns in ascending order
+  // compact the kept columns in ascending order.  Strictly kept: a larger
+  // score, or the threshold score with a smaller id than the threshold id.
+  // Entries equal to the threshold in score and id ("tied") fill the rest,
+  // k - (strictly kept), in ascending column order.
   const int per = (N + blockDim.x - 1) / blockDim.x;
-  const int n0 = threadIdx.x * per, n1 = min(N, n0 + per);
-  int cnt = 0;
+  const int n0 = min(N, (int)threadIdx.x * per), n1 = min(N, n0 + per);
+  auto strict = [&](uint32_t a, uint32_t b2) { return all || a > T || (a == T && b2 > T2); };
+  auto tied = [&](uint32_t a, uint32_t b2) { return !all && a == T && b2 == T2; };
+  int cs = 0, ct = 0;
   for (int n = n0; n < n1; ++n) {
     const uint32_t a = __ldcg(keys + n), b2 = __ldcg(keys2 + n);
-    cnt += all || (!none && (a > T || (a == T && b2 >= T2)));
+    cs += strict(a, b2);
+    ct += tied(a, b2);
   }
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int incl = cnt;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+  int is = cs, it = ct;
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  __syncthreads();
-  if (lane == 31) wsum[wid] = incl;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) {
-      const int v = wsum[q];
-      wsum[q] = run;
-      run += v;
+    const int vs = __shfl_up_sync(0xffffffffu, is, o);
+    const int vt = __shfl_up_sync(0xffffffffu, it, o);
+    if (lane >= o) {
+      is += vs;
+      it += vt;
     }
   }
   __syncthreads();
-  int pos = wsum[wid] + incl - cnt;
+  if (lane == 31) {
+    wsum[wid] = is;
+    wsum2[wid] = it;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int rs = 0, rt = 0;
+    for (int q = 0; q < nw; ++q) {
+      const int vs = wsum[q], vt = wsum2[q];
+      wsum[q] = rs;
+      wsum2[q] = rt;
+      rs += vs;
+      rt += vt;
+    }
+    sh[0] = rs;   // strictly kept in the row
+  }
+  __syncthreads();
+  const int take = k - sh[0];
+  int ps = wsum[wid] + is - cs, pt = wsum2[wid] + it - ct;
   for (int n = n0; n < n1; ++n) {
     const uint32_t a = __ldcg(keys + n), b2 = __ldcg(keys2 + n);
-    if (all || (!none && (a > T || (a == T && b2 >= T2)))) {
-      if (pos < k) kept[(size_t)row * k + pos] = n;
-      ++pos;
+    if (strict(a, b2)) {
+      const int at = ps + min(pt, take);
+      if (at < k) kept[(size_t)row * k + at] = n;
+      ++ps;
+    } else if (tied(a, b2)) {
+      if (pt < take) kept[(size_t)row * k + ps + pt] = n;
+      ++pt;
     }
   }
 }

@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(HERE, "libmoe_reader.so")
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EDEVICE, ESTATE, ETOOBIG = 0, -1, -2, -3, -4, -5, -6, -7
 FLAG_RHO_RANK = 0x1   # full screen ranked by the expected skip error (screen_coords = 128)
 ERR_EXPERT_RANGE, ERR_EXPERT_DUP, ERR_WEIGHT, ERR_X_NONFINITE, ERR_TIMEOUT = 1, 2, 4, 8, 16
+# one-shot fault injections for tests of failure detection (moe_reader_inject_fault)
+INJECT_DECODE_STALL, INJECT_PREPARE_STALL, INJECT_ALLOC_FAIL = 0x1, 0x2, 0x4
 ARRAYS = ("codes", "scales", "dnorm", "G", "V", "Dt", "b", "U")
 
 EXPORT = {
@@ -30,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "moe_reader_get_info", "moe_reader_destroy", "moe_reader_strerror", "moe_reader_abi_version",
     "moe_reader_set_profiling", "moe_reader_read_profile", "moe_reader_topk_noalloc",
     "moe_reader_decode_stack", "moe_reader_decode_shared", "moe_reader_get_kept_shared",
+    "moe_reader_set_wait_limit", "moe_reader_inject_fault",
 )
 PHASES = ("decode", "screen", "score_topk", "exact", "out")
 
@@ -108,6 +111,10 @@ def _lib():
         lib.moe_reader_read_profile.restype = ctypes.c_int
         lib.moe_reader_topk_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, vp]
         lib.moe_reader_topk_noalloc.restype = ctypes.c_int
+        lib.moe_reader_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+        lib.moe_reader_set_wait_limit.restype = ctypes.c_int
+        lib.moe_reader_inject_fault.argtypes = [vp, ctypes.c_uint32]
+        lib.moe_reader_inject_fault.restype = ctypes.c_int
         lib.moe_reader_abi_version.argtypes = []
         lib.moe_reader_abi_version.restype = ctypes.c_int
         _LIB = lib
@@ -156,13 +163,47 @@ def _check(code, what):
         raise ReaderError(code, what)
 
 
+def _require(t, dtype, shape, what):
+    """A contiguous CUDA tensor of the given dtype and shape on the current device."""
+    import torch
+
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{what} is on cuda:{t.device.index}, not the current device")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+
+
 def topk_noalloc(scores, k, kept, ids=None, stream=None):
     """Exact top-k per row of device scores [rows][cols] into device kept
-    [rows][k] (ascending column indices) without any device allocation."""
+    [rows][k] (ascending column indices) without any device allocation.
+    scores: float32 [rows][cols]; kept: int32 [rows][k]; ids: int32
+    [rows][cols] tie-break ids or None (the column index)."""
+    import torch
+
+    if scores.dim() != 2:
+        raise ValueError("scores must be 2-D [rows][cols]")
     rows, cols = int(scores.shape[0]), int(scores.shape[1])
+    _require(scores, torch.float32, (rows, cols), "scores")
+    _require(kept, torch.int32, (rows, int(k)), "kept")
+    if ids is not None:
+        _require(ids, torch.int32, (rows, cols), "ids")
     code = _lib().moe_reader_topk_noalloc(_ptr(scores), _ptr(ids), rows, cols, int(k),
                                           _ptr(kept), _stream(stream))
     _check(code, "moe_reader_topk_noalloc")
+
+
+def inject_fault(what, reader=None):
+    """Arm a one-shot failure (INJECT_* bits): a decode stall on `reader`, or,
+    with reader None, a stall in the next prepare or a failed next device
+    allocation.  Nothing faults the GPU; the failure surfaces as a status."""
+    _check(_lib().moe_reader_inject_fault(None if reader is None else reader.handle, int(what)),
+           "moe_reader_inject_fault")
 
 
 def decode_stack(readers, h_in, ids, w, k, h_out, y_layers=None, stream=None):
@@ -256,6 +297,10 @@ class MoeReader:
                                              _ptr(y), _stream(stream))
         _check(code, "moe_reader_decode_host")
         return y
+
+    def set_wait_limit(self, ns):
+        """Bound (ns of the GPU timer) of every device wait of later decodes; 0 = 1 s."""
+        _check(_lib().moe_reader_set_wait_limit(self._h, int(ns)), "moe_reader_set_wait_limit")
 
     def status(self):
         bits = ctypes.c_uint32(0)

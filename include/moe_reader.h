@@ -253,6 +253,41 @@ int moe_reader_decode_stack(moe_reader_t* const* layers, int32_t L, const float*
                             const int32_t* expert_ids, const float* expert_w, int32_t k,
                             float* h_out, float* y_layers, void* stream);
 
+/*
+ * moe_reader_set_wait_limit -- bound, in nanoseconds of the GPU's global
+ * timer, of every device-side wait of this handle's later decode calls (a
+ * wait for another CTA's hand-off: screen units, scores, the kept list,
+ * exact items, a stacked layer's input).  0 restores the default of one
+ * second.  When a wait runs out, the kernel sets MOE_READER_ERR_TIMEOUT and
+ * an abort flag that ends every other wait of the launch, and returns;
+ * moe_reader_status then answers ETIMEOUT and clears the handle's counters
+ * so that the next decode runs normally.  Takes effect for decode calls
+ * enqueued after it (a captured graph keeps the limit it was captured with).
+ */
+int moe_reader_set_wait_limit(moe_reader_t* h, uint64_t ns);
+
+/*
+ * moe_reader_inject_fault -- make one failure happen on purpose, for tests
+ * of failure detection; nothing faults, traps or hangs the GPU:
+ *   MOE_READER_INJECT_DECODE_STALL   (h required) the next decode call on h
+ *       waits, in its score tasks, for one screen unit more than exist: the
+ *       count is never reached, the wait runs out after the wait limit and
+ *       the call ends with MOE_READER_ERR_TIMEOUT.  In a stack, later layers
+ *       inherit the abort (see moe_reader_decode_stack).
+ *   MOE_READER_INJECT_PREPARE_STALL  (h = NULL) the next moe_reader_prepare's
+ *       cooperative tridiagonalisation waits at its grid barrier for one CTA
+ *       more than it launched; the barrier's bound (about one second) runs
+ *       out and prepare returns ETIMEOUT with nothing allocated.
+ *   MOE_READER_INJECT_ALLOC_FAIL     (h = NULL) the library's next device
+ *       allocation reports failure as if the device were out of memory; the
+ *       call that made it returns ENOMEM after freeing what it holds.
+ * Each injection fires once.  EINVAL for an unknown bit or a wrong h.
+ */
+#define MOE_READER_INJECT_DECODE_STALL  0x1u
+#define MOE_READER_INJECT_PREPARE_STALL 0x2u
+#define MOE_READER_INJECT_ALLOC_FAIL    0x4u
+int moe_reader_inject_fault(moe_reader_t* h, uint32_t what);
+
 /* moe_reader_status -- synchronize the stream of the last decode, read and
  * clear the device error word.  *bits (host, may be NULL) receives the
  * MOE_READER_ERR_* bits.  Returns OK, EDEVICE (input check) or ETIMEOUT. */
@@ -330,9 +365,13 @@ int moe_reader_read_profile(moe_reader_t* h, double* ms_out, int64_t capacity,
  * that may only touch memory the engine hands them, and processes whose
  * allocator forbids device allocations after start-up.
  *
- *   scores  dev, fp32 [rows][cols]; any finite values (NaN sorts above all).
+ *   scores  dev, fp32 [rows][cols].  Values are ordered as floats: -0 ties
+ *           with +0, and every NaN (either sign, any payload) ranks above
+ *           +infinity, NaNs tying with one another.
  *   ids     dev, int32 [rows][cols] tie-break ids, or NULL to use the column
- *           index (the decode passes global channel ids e*I + i).
+ *           index (the decode passes global channel ids e*I + i).  Ids are
+ *           compared as unsigned 32-bit values; entries equal in both score
+ *           and id are taken in ascending column order.
  *   k       0 <= k <= cols kept entries per row.
  *   kept    dev, int32 [rows][k]: kept COLUMN indices, ascending per row.
  *

@@ -106,32 +106,6 @@ def rotate(a: np.ndarray, sigma: np.ndarray) -> np.ndarray:
     return out.reshape(a.shape)
 
 
-def butterfly_magnitudes_fp32(x_pad: np.ndarray, sigma: np.ndarray) -> np.ndarray:
-    """|H_128 (sigma * x)| per block, evaluated in fp32 by the Sylvester butterfly.
-
-    This is used ONLY to decide which coordinates the partial screen reads.
-    The decision is taken in the kernel's precision (fp32; the pages fix none)
-    so that both sides make the same integer choice: the transform is the
-    in-place butterfly over strides 1, 2, 4, ..., 64 where element i (bit h
-    clear) and i + h become (a + b, a - b), each rounded to fp32.  The positive
-    1/sqrt(128) factor does not change the order and is omitted.
-    Returns float32 magnitudes of shape [nb, 128].
-    """
-    u = (np.asarray(x_pad, dtype=np.float32) * np.asarray(sigma, dtype=np.float32))
-    u = u.reshape(-1, BLOCK).copy()
-    idx = np.arange(BLOCK)
-    h = 1
-    while h < BLOCK:
-        lo = idx[(idx & h) == 0]
-        hi = lo + h
-        a = u[:, lo].copy()
-        b = u[:, hi].copy()
-        u[:, lo] = a + b
-        u[:, hi] = a - b
-        h *= 2
-    return np.abs(u)
-
-
 def select_coordinates(mag: np.ndarray, c: int) -> np.ndarray:
     """Partial-screen coordinate set T_b: the c coordinates with the largest
     |Rx| in each 128-block ([CN] §方法步骤详情, decode (1); [KR] §어떻게 쓰나:
@@ -143,6 +117,24 @@ def select_coordinates(mag: np.ndarray, c: int) -> np.ndarray:
         order = np.argsort(-mag[b].astype(np.float64), kind="stable")
         mask[b, order[:c]] = True
     return mask
+
+
+def selection_gaps(mag: np.ndarray, c: int) -> np.ndarray:
+    """Per block, the relative gap (m_c - m_{c+1}) / m_c between the c-th and
+    the (c+1)-th largest |Rx| (m sorted descending, float64); +inf when every
+    coordinate is screened (c = 128) or the block is zero.  A block whose gap
+    is tiny is a near-tie: an implementation that rounds Rx differently (an
+    fp32 butterfly, say) may legitimately screen the other coordinate, so
+    parity checks of the screened set excuse such blocks.  Returns float64 [nb].
+    """
+    srt = -np.sort(-np.asarray(mag, dtype=np.float64), axis=1)
+    out = np.full(srt.shape[0], np.inf)
+    if c >= BLOCK:
+        return out
+    top, nxt = srt[:, c - 1], srt[:, c]
+    pos = top > 0
+    out[pos] = (top[pos] - nxt[pos]) / top[pos]
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -416,6 +408,7 @@ class TokenResult:
     mask: np.ndarray         # bool [nb][128] screened coordinates
     kth_score: float         # score of the k-th kept channel (nan if k == 0)
     next_score: float        # best skipped score (nan if k == N)
+    gap: np.ndarray = None   # float64 [nb]: relative gap at the screen's c-th |Rx| per block
 
 
 def screen_estimates(layer: Layer, e: int, Rx: np.ndarray, mask: np.ndarray):
@@ -442,19 +435,28 @@ class TokenScreen:
     vhat: np.ndarray
     p: np.ndarray            # phi(ghat) vhat
     score: np.ndarray        # w ||d|| |p|
+    gap: np.ndarray          # float64 [nb]: selection_gaps of the token's blocks
 
 
-def screen_token(layer: Layer, x: np.ndarray, ids, w) -> TokenScreen:
+def screen_token(layer: Layer, x: np.ndarray, ids, w, mask=None) -> TokenScreen:
     """Rotate x once, partial screen of the c largest-|Rx| coordinates per
     block, and the output-unit score s_j = w_j ||d_j|| |phi(ghat_j) vhat_j| of
     every routed channel ([CN] §方法步骤详情, decode (1)-(2); the placement of
-    |.| follows [KR] §어떻게 쓰나, [CN] writes phi(ghat)|vhat|)."""
+    |.| follows [KR] §어떻게 쓰나, [CN] writes phi(ghat)|vhat|).
+
+    mask (bool [nb][128], optional) replaces the screened set: a parity check
+    passes the other side's set where a block's c-th and (c+1)-th |Rx| are a
+    near-tie (selection_gaps), so that both sides then screen the same
+    coordinates.  Every other step is unchanged."""
     sh = layer.shape
     x64 = np.asarray(x, dtype=np.float64)
     xpad = pad_hidden(x64, sh.Hp)
     Rx = rotate(xpad, layer.sigma).reshape(sh.nb, BLOCK)
-    mask = select_coordinates(butterfly_magnitudes_fp32(pad_hidden(np.asarray(x, np.float32), sh.Hp),
-                                                        layer.sigma), sh.c)
+    gap = selection_gaps(np.abs(Rx), sh.c)
+    if mask is None:
+        mask = select_coordinates(np.abs(Rx), sh.c)
+    else:
+        mask = np.asarray(mask, dtype=bool).reshape(sh.nb, BLOCK)
     ids = [int(e) for e in ids]
     topk = len(ids)
     ghat = np.zeros((topk, sh.I))
@@ -466,7 +468,7 @@ def screen_token(layer: Layer, x: np.ndarray, ids, w) -> TokenScreen:
     p = silu(ghat) * vhat
     wv = np.asarray(w, dtype=np.float64)
     score = wv[:, None] * dn * np.abs(p)
-    return TokenScreen(mask=mask, ghat=ghat, vhat=vhat, p=p, score=score)
+    return TokenScreen(mask=mask, ghat=ghat, vhat=vhat, p=p, score=score, gap=gap)
 
 
 def exact_and_recovery(layer: Layer, x: np.ndarray, ids, w, p: np.ndarray, keep: np.ndarray):
@@ -496,8 +498,10 @@ def exact_and_recovery(layer: Layer, x: np.ndarray, ids, w, p: np.ndarray, keep:
     return y_exact, y_rec
 
 
-def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int) -> TokenResult:
+def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int,
+                 mask=None) -> TokenResult:
     """One token through the reader ([CN] §方法步骤详情, decode (1)-(4)).
+    `mask` optionally fixes the screened coordinates (see screen_token).
 
     1. Rotate x once; partial screen of the c largest-|Rx| coordinates per block.
     2. s_j = w_j ||d_j|| |phi(ghat_j) vhat_j| for every routed channel, then the
@@ -508,7 +512,7 @@ def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k:
     4. Skipped channels: y_recovery = U sum_S w_j b_j p_j, p_j = phi(ghat_j) vhat_j.
     """
     sh = layer.shape
-    sc = screen_token(layer, x, ids, w)
+    sc = screen_token(layer, x, ids, w, mask=mask)
     ids = [int(e) for e in ids]
     gid = np.array([[e * sh.I + i for i in range(sh.I)] for e in ids], dtype=np.int64)
     flat_s = sc.score.reshape(-1)
@@ -524,7 +528,7 @@ def decode_token(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k:
         y=y_exact + y_rec, y_exact=y_exact, y_recovery=y_rec,
         kept=np.sort(flat_id[kept_idx]), kept_order=flat_id[kept_idx],
         score=sc.score, p=sc.p, ghat=sc.ghat, vhat=sc.vhat, mask=sc.mask,
-        kth_score=kth, next_score=nxt)
+        kth_score=kth, next_score=nxt, gap=sc.gap)
 
 
 def decode(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int):
@@ -596,7 +600,7 @@ def decode_token_rho(layer: Layer, x: np.ndarray, ids, w, k: int) -> TokenResult
         y=y_exact + y_rec, y_exact=y_exact, y_recovery=y_rec,
         kept=np.sort(flat_id[order[:k]]), kept_order=flat_id[order[:k]],
         score=err, p=sc.p, ghat=sc.ghat, vhat=sc.vhat, mask=sc.mask,
-        kth_score=kth, next_score=nxt)
+        kth_score=kth, next_score=nxt, gap=sc.gap)
 
 
 # --------------------------------------------------------------------------
@@ -620,7 +624,8 @@ def shared_kept_count(k: int, n_experts: int, topk: int) -> int:
     return (2 * k * n_experts + topk) // (2 * topk)
 
 
-def decode_shared(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int) -> SharedResult:
+def decode_shared(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k: int,
+                  masks=None) -> SharedResult:
     """Batch-shared selection: one kept set for the whole batch ([CN] §未来方向
     (1) names it as the way to keep the gains at larger batches and gives no
     formula; the reading taken here):
@@ -636,11 +641,13 @@ def decode_shared(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k
       channels outside K with its own p (steps 3-4).
 
     At batch 1, U is the token's N routed channels, K_B = k and S = s: the
-    per-token reader."""
+    per-token reader.  `masks` (bool [B][nb][128], optional) fixes the
+    tokens' screened coordinates (see screen_token)."""
     sh = layer.shape
     B = x.shape[0]
     ids = np.asarray(ids)
-    screens = [screen_token(layer, x[t], ids[t], w[t]) for t in range(B)]
+    screens = [screen_token(layer, x[t], ids[t], w[t], mask=None if masks is None else masks[t])
+               for t in range(B)]
     experts = np.array(sorted({int(e) for e in ids.reshape(-1)}), dtype=np.int64)
     rank = {int(e): r for r, e in enumerate(experts)}
     S = np.zeros((experts.size, sh.I))
@@ -665,7 +672,7 @@ def decode_shared(layer: Layer, x: np.ndarray, ids: np.ndarray, w: np.ndarray, k
         tokens.append(TokenResult(
             y=y_exact + y_rec, y_exact=y_exact, y_recovery=y_rec, kept=mine, kept_order=mine,
             score=sc.score, p=sc.p, ghat=sc.ghat, vhat=sc.vhat, mask=sc.mask,
-            kth_score=kth, next_score=nxt))
+            kth_score=kth, next_score=nxt, gap=sc.gap))
     return SharedResult(tokens=tokens, experts=experts, batch_score=S, K=K, kept=kept,
                         kth_score=kth, next_score=nxt)
 

@@ -78,3 +78,31 @@ def test_null_handles_and_arguments(lib):
     assert lib.moe_reader_get_kept_shared(None, None, 0, ctypes.byref(K)) == RD.EINVAL
     assert lib.moe_reader_get_kept(None, None, 0) == RD.EINVAL
     assert lib.moe_reader_status(None, None) == RD.EINVAL
+
+
+def test_fault_injection_arguments(lib):
+    lib.moe_reader_inject_fault.argtypes = [ctypes.c_void_p, ctypes.c_uint32]
+    lib.moe_reader_inject_fault.restype = ctypes.c_int
+    lib.moe_reader_set_wait_limit.argtypes = [ctypes.c_void_p, ctypes.c_uint64]
+    lib.moe_reader_set_wait_limit.restype = ctypes.c_int
+    assert lib.moe_reader_inject_fault(None, 0) == RD.EINVAL              # nothing to inject
+    assert lib.moe_reader_inject_fault(None, 0x8) == RD.EINVAL            # unknown bit
+    assert lib.moe_reader_inject_fault(None, RD.INJECT_DECODE_STALL) == RD.EINVAL   # needs a handle
+    assert lib.moe_reader_set_wait_limit(None, 1000) == RD.EINVAL
+
+
+def test_injected_allocation_failure_is_enomem(lib):
+    """An injected allocation failure makes prepare return ENOMEM before it
+    touches a device pointer, on any host; without the injection, a host with
+    no GPU fails its first allocation as a CUDA error, not as ENOMEM."""
+    lib.moe_reader_inject_fault.argtypes = [ctypes.c_void_p, ctypes.c_uint32]
+    lib.moe_reader_inject_fault.restype = ctypes.c_int
+    assert lib.moe_reader_inject_fault(None, RD.INJECT_ALLOC_FAIL) == RD.OK
+    assert prepare(lib) == RD.ENOMEM
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except ImportError:
+        has_gpu = False
+    if not has_gpu:   # with a GPU the call would run on the fake weight pointers
+        assert prepare(lib) == RD.ECUDA

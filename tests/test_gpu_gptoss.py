@@ -9,7 +9,6 @@ import numpy as np
 import pytest
 
 from calibration_free_sparse_gb300 import synthetic as S
-from oracle import reader as R
 from tests import gpu_common as C
 
 pytestmark = pytest.mark.gpu
@@ -31,15 +30,7 @@ def test_batch1_against_oracle(pair):
     x, ids, w = pair.tokens(1, 600)
     y = pair.decode_gpu(x, ids, w, WL.k)
     assert pair.reader.status() == (0, 0)
-    res = R.decode(pair.layer, x, ids, w, WL.k)
-    kept = pair.reader.kept(1, WL.k)
-    nd = C.assert_kept_match(kept[0], res[0], ids[0], WL.k)
-    C.assert_y_close(y[0], res[0].y)
-    if nd == 0:
-        st = pair.reader.stats()
-        ref = C.oracle_sectors(pair, ids, res)
-        for name in ref:
-            assert st[name] == ref[name], name
+    C.check_decode(pair, x, ids, w, WL.k, y)
 
 
 @pytest.mark.parametrize("B", [16, BMAX])
@@ -48,11 +39,8 @@ def test_large_batch(pair, B):
     y = pair.decode_gpu(x, ids, w, WL.k)
     assert pair.reader.status() == (0, 0)
     kept = pair.reader.kept(B, WL.k)
-    # sampled tokens against the oracle
-    for t in sorted({0, 1, B // 2, B - 1}):
-        res = R.decode_token(pair.layer, x[t], ids[t], w[t], WL.k)
-        C.assert_kept_match(kept[t], res, ids[t], WL.k)
-        C.assert_y_close(y[t], res.y)
+    # sampled tokens against the oracle; read accounting of the whole batch
+    C.check_decode(pair, x, ids, w, WL.k, y, tokens=sorted({0, 1, B // 2, B - 1}))
     # every token: the same result when decoded in batches of 8
     for t0 in range(0, B, 8):
         sl = slice(t0, min(B, t0 + 8))

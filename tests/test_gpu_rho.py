@@ -40,12 +40,15 @@ def test_against_oracle(case):
         assert pair.reader.status() == (0, 0), name
         kept = pair.reader.kept(B, k)
         keys = pair.reader.export("score")
+        gm = C.gpu_masks(pair, B)
+        assert gm.all()                      # the full screen reads every coordinate
         for t in range(B):
             res = R.decode_token_rho(pair.layer, x[t], ids[t], w[t], k)
             ref = res.score.reshape(-1)
             assert np.abs(keys[t] - ref).max() <= 1e-4 * np.abs(ref).max(), name
             C.assert_kept_match(kept[t], res, ids[t], k)
             C.assert_y_close(y[t], res.y)
+        C.assert_read_accounting(pair, ids, gm, [kept[t] for t in range(B)])
 
 
 def test_flag_needs_the_full_screen():

@@ -16,7 +16,6 @@ import numpy as np
 import pytest
 
 from calibration_free_sparse_gb300 import synthetic as S
-from oracle import reader as R
 from tests import gpu_common as C
 
 pytestmark = pytest.mark.gpu
@@ -48,17 +47,7 @@ def test_decode_parity(case):
         x, ids, w = pair.tokens(B, 40 + B)
         y = pair.decode_gpu(x, ids, w, k)
         assert pair.reader.status() == (0, 0), name
-        res = R.decode(pair.layer, x, ids, w, k)
-        kept = pair.reader.kept(B, k)
-        ndiff = 0
-        for t in range(B):
-            ndiff += C.assert_kept_match(kept[t], res[t], ids[t], k)
-            C.assert_y_close(y[t], res[t].y)
-        if ndiff == 0:
-            st = pair.reader.stats()
-            ref = C.oracle_sectors(pair, ids, res)
-            for arr in ref:
-                assert st[arr] == ref[arr], (name, B, arr)
+        C.check_decode(pair, x, ids, w, k, y)
 
 
 def test_screen_estimates(case):
@@ -66,8 +55,8 @@ def test_screen_estimates(case):
     name, sh, pair, k = case
     B = sh["batches"][-1]
     x, ids, w = pair.tokens(B, 70 + B)
-    pair.decode_gpu(x, ids, w, k)
-    res = R.decode(pair.layer, x, ids, w, k)
+    y = pair.decode_gpu(x, ids, w, k)
+    res, _, _ = C.check_decode(pair, x, ids, w, k, y)
     ghat = pair.reader.export("ghat")
     vhat = pair.reader.export("vhat")
     for t in range(B):

@@ -36,20 +36,29 @@ def check_against_oracle(pair, x, ids, w, k, band=C.KEPT_BAND, tokens=None):
     y = decode_shared_gpu(pair, x, ids, w, k)
     assert pair.reader.status() == (0, 0)
     kept = pair.reader.kept_shared()
+    B, I = x.shape[0], pair.shape.I
+    gm = C.gpu_masks(pair, B)
     res = R.decode_shared(pair.layer, x, ids, w, k)
+    if any(not np.array_equal(gm[t], res.tokens[t].mask) for t in range(B)):
+        for t in range(B):
+            if not np.array_equal(gm[t], res.tokens[t].mask):
+                C.check_near_tie(pair, x[t], res.tokens[t], gm[t])
+        res = R.decode_shared(pair.layer, x, ids, w, k, masks=gm)
     assert kept.size == res.K
     got, ref = set(int(v) for v in kept), set(int(v) for v in res.kept)
     diff = got ^ ref
     if diff:
-        I = pair.shape.I
         rank = {int(e): r for r, e in enumerate(res.experts)}
         for g in diff:
             sc = res.batch_score[rank[g // I], g % I]
             assert abs(sc - res.kth_score) <= band * res.kth_score, (g, sc, res.kth_score)
-    for t in (range(x.shape[0]) if tokens is None else tokens):
+    for t in (range(B) if tokens is None else tokens):
         C.assert_y_close(y[t], res.tokens[t].y)
+    # read accounting of the kernel's own screened sets and kept set, always
+    mine = [np.array([g for g in kept if int(g) // I in set(int(e) for e in ids[t])], np.int64)
+            for t in range(B)]
+    st = C.assert_read_accounting(pair, ids, gm, mine)
     if not diff:
-        st = pair.reader.stats()
         refs = C.oracle_sectors(pair, ids, res.tokens)
         for name in refs:
             assert st[name] == refs[name], name

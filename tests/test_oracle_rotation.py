@@ -54,25 +54,29 @@ def test_rotation_blocks_are_independent():
     assert np.all(R.rotate(y, sigma)[128:] == 0)
 
 
-def test_butterfly_fp32_agrees_with_fp64_rotation():
+def test_screen_selects_on_exact_rotation():
+    # the screened set is the c largest |Rx| of the float64 rotation, checked
+    # by brute force on rotations that the closed form R e_j pins above
     rng = np.random.default_rng(4)
-    sigma = np.where(rng.random(512) < 0.5, -1, 1).astype(np.int8)
-    x = rng.standard_normal(512).astype(np.float32)
-    x[[3, 77, 300, 450]] *= 20
-    mag = R.butterfly_magnitudes_fp32(x, sigma)
-    assert mag.dtype == np.float32 and mag.shape == (4, 128)
-    exact = np.abs(R.rotate(x.astype(np.float64), sigma)).reshape(4, 128) * math.sqrt(128)
-    assert np.allclose(mag, exact, rtol=2e-6, atol=1e-5)
+    sigma = np.where(rng.random(256) < 0.5, -1, 1).astype(np.int8)
+    x = rng.standard_normal(256)
+    x[[3, 77]] *= 20
+    mag = np.abs(R.rotate(x, sigma)).reshape(2, 128)
+    assert np.array_equal(R.select_coordinates(mag, 80), _brute_select(mag, 80))
 
 
-def test_butterfly_is_exact_on_small_integers():
-    # small integers: every fp32 butterfly sum is exact, so it must equal H (sigma x)
-    rng = np.random.default_rng(5)
-    sigma = np.where(rng.random(128) < 0.5, -1, 1).astype(np.int8)
-    x = rng.integers(-50, 50, 128).astype(np.float32)
-    mag = R.butterfly_magnitudes_fp32(x, sigma)[0]
-    ref = np.abs(scipy.linalg.hadamard(128) @ (sigma.astype(np.int64) * x.astype(np.int64)))
-    assert np.array_equal(mag.astype(np.int64), ref)
+def test_selection_gaps_hand_values():
+    mag = np.zeros((3, 128))
+    mag[0, :10] = np.arange(10, 0, -1)      # 10, 9, ..., 1 then zeros
+    mag[1, :] = 5.0                          # all tied: gap 0
+    # block 2 stays zero: no order to protect
+    g = R.selection_gaps(mag, 3)
+    assert g[0] == (8.0 - 7.0) / 8.0
+    assert g[1] == 0.0
+    assert np.isinf(g[2])
+    assert np.all(np.isinf(R.selection_gaps(mag, 128)))
+    # the gap at c = 10 of block 0: (1 - 0) / 1
+    assert R.selection_gaps(mag, 10)[0] == 1.0
 
 
 def _brute_select(mag, c):
