@@ -96,7 +96,13 @@ struct GridSync {
   unsigned int pad;
 };
 
-constexpr long long kSpinLimit = 1LL << 24;   // x ~64 ns sleep: about 1 s
+constexpr unsigned long long kBarrierNs = 1000000000ull;   // one second of the global timer
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ bool grid_barrier(GridSync* gs, unsigned int nblocks) {
   __shared__ int ok;
@@ -112,10 +118,10 @@ __device__ bool grid_barrier(GridSync* gs, unsigned int nblocks) {
       __threadfence();
       atomicAdd(&gs->gen, 1u);
     } else {
-      long long spins = 0;
+      const unsigned long long t0 = global_ns();
       while (*vgen == gen) {
         if (*vab) break;
-        if (++spins > kSpinLimit) {
+        if (global_ns() - t0 > kBarrierNs) {
           atomicExch(&gs->abort, 1u);
           break;
         }
