@@ -160,6 +160,23 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
+// Development trace: built with -DMR_TRACE, each CTA records the global timer
+// at numbered points of the decode into g_trace[CTA][point] (the last time a
+// point is passed); moe_reader_trace_read copies the table out.  Without the
+// macro the points compile to nothing.
+#ifdef MR_TRACE
+constexpr int kTraceCtas = 256, kTracePoints = 32;
+__device__ unsigned long long g_trace[kTraceCtas][kTracePoints];
+#define TRACE_POINT(id)                                                            \
+  do {                                                                             \
+    if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x][(id)] = globaltimer();        \
+  } while (0)
+#else
+#define TRACE_POINT(id) \
+  do {                  \
+  } while (0)
+#endif
+
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -317,21 +334,27 @@ __device__ void rotate_select_loaded(const Params& P, int lane, float (&u)[4], u
     u[0] = __fadd_rn(a0, a2); u[2] = __fsub_rn(a0, a2);
     u[1] = __fadd_rn(a1, a3); u[3] = __fsub_rn(a1, a3);
   }
-  // the c-th largest |z| by a bit search over its fp32 pattern, then ties by index
+  // the c-th largest |z|: T = the largest bit pattern with at least c
+  // magnitudes >= T, searched two bits at a time from bit 30 (the sign bit of
+  // a magnitude is 0), the three candidates of a step counted side by side;
+  // then ties by index
   uint32_t m[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) m[s] = __float_as_uint(fabsf(u[s]));
+  auto count_ge = [&](uint32_t v) {
+    return (int)__reduce_add_sync(0xffffffffu, (unsigned)((m[0] >= v) + (m[1] >= v) + (m[2] >= v) +
+                                                          (m[3] >= v)));
+  };
   uint32_t T = 0;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    int cnt = 0;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) cnt += __popc(__ballot_sync(0xffffffffu, m[s] >= cand));
-    if (cnt >= d.c) T = cand;
+  if (count_ge(1u << 30) >= d.c) T = 1u << 30;
+#pragma unroll 1
+  for (int bit = 28; bit >= 0; bit -= 2) {
+    const uint32_t c1 = T | (1u << bit), c2 = T | (2u << bit), c3 = T | (3u << bit);
+    const int n1 = count_ge(c1), n2 = count_ge(c2), n3 = count_ge(c3);
+    T = n3 >= d.c ? c3 : (n2 >= d.c ? c2 : (n1 >= d.c ? c1 : T));
   }
-  int gt = 0;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) gt += __popc(__ballot_sync(0xffffffffu, m[s] > T));
+  const int gt = (int)__reduce_add_sync(0xffffffffu, (unsigned)((m[0] > T) + (m[1] > T) + (m[2] > T) +
+                                                                (m[3] > T)));
   const int need = d.c - gt;
   const uint32_t below = (1u << lane) - 1u;
   int before = 0;
@@ -442,11 +465,13 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   int* eid = wsum + kWarps;                                                 // [topk]
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int s = threadIdx.x; s < d.topk; s += kThreads) eid[s] = __ldcg(P.ids_ws + t * d.topk + s);
+  if (threadIdx.x == 0) TRACE_POINT(8);
   for (int n = threadIdx.x; n < N; n += kThreads)
     keys[n] = __float_as_uint(__ldcg(P.score + (size_t)t * N + n));
   for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
   if (threadIdx.x == 0) sh[2] = 0;
   __syncthreads();
+  if (threadIdx.x == 0) TRACE_POINT(22);
 
   const bool all = k >= N, none = k <= 0;
   if (all || none) {
@@ -455,6 +480,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     // 1. histogram of the 12-bit digit (keys spread over hundreds of bins)
     for (int n = threadIdx.x; n < N; n += kThreads) atomicAdd(&hist[key_digit(keys[n])], 1);
     __syncthreads();
+    if (threadIdx.x == 0) TRACE_POINT(9);
     // 2. the digit D holding the k-th largest key: 8 digits per thread, from the top
     constexpr int kPer = kBins / kThreads;
     int cnt[kPer], tot = 0;
@@ -488,6 +514,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     }
     __syncthreads();
     const int D = sh[0], need = sh[1], m = sh[3];
+    if (threadIdx.x == 0) TRACE_POINT(10);
     if (m <= kCandMax) {
       // 3. the candidates (digit D) ranked exactly: larger key, then lower global id
       for (int n = threadIdx.x; n < N; n += kThreads) {
@@ -501,6 +528,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
         }
       }
       __syncthreads();
+      if (threadIdx.x == 0) TRACE_POINT(23);
       // a warp per candidate: its lanes count the candidates ahead of it
       for (int ci = wid; ci < m; ci += kWarps) {
         const uint32_t ki = ckey[ci], gi = cgid[ci];
@@ -545,6 +573,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   }
   __syncthreads();
   // 4. compaction in ascending n and the kept bitmap: warp w owns a contiguous
+  if (threadIdx.x == 0) TRACE_POINT(11);
   //    range of whole 32-channel words; one ballot per word
   const int words = N / 32;
   const int wper = (words + kWarps - 1) / kWarps;
@@ -566,10 +595,14 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     if (lane == 0) P.keptbits[(size_t)t * words + wd] = bal;
     pos += __popc(bal);
   }
+  if (threadIdx.x == 0) TRACE_POINT(24);
   // the output phase adds its chunks into y[t]: start it from zero
   for (int h = threadIdx.x; h < d.H; h += kThreads) P.y[(size_t)t * d.H + h] = 0.f;
   __syncthreads();
-  if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], 1u);
+  if (threadIdx.x == 0) {
+    st_release(&P.sync[sync_offsets(d).flag + t], 1u);
+    TRACE_POINT(12);
+  }
 }
 
 // ------------------------- batch-shared selection ---------------------------
@@ -1041,6 +1074,86 @@ __device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) 
   if (lane == 0) red_add_release(P.sync + sync_offsets(P.d).slot + ts, 1u);
 }
 
+// The first warp's part of screen unit uu: rotation and selection of the
+// unit's (token, block) from sigma x (xu, loaded by rotate_load), the side
+// outputs (screened set, input checks, sanitised routing, zeroed recovery
+// vector), and into `buf` the screened coordinate list, their Rx values and
+// the pair tables.  Returns the unit's expert id, clamped into range.
+__device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane, float (&xu)[4],
+                          bool xbad, int e_raw, int team) {
+  const Dims& d = P.d;
+  uint8_t* cbuf = buf + P.sp.coord_off;
+  float* rbuf = reinterpret_cast<float*>(cbuf + 128);
+  const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk, slot = ts % d.topk;
+  uint32_t word[4];
+  rotate_select_loaded(P, lane, xu, word);
+  if (lane == 0 && team == 0) TRACE_POINT(2);
+  if (d.rho_rank) {   // ||(R x)_b||^2 for the expected-error ranking (every slot writes it)
+    const float ss = warp_sum(xu[0] * xu[0] + xu[1] * xu[1] + xu[2] * xu[2] + xu[3] * xu[3]);
+    if (lane == 0) P.rn2[(size_t)t * d.nb + b] = ss;
+  }
+  // the unit's side outputs: the block's screened set (the same from every
+  // slot), the input checks, and at block 0 the slot's sanitised expert id
+  // and weight (and, for slot 0, the token's zeroed recovery vector); the
+  // warp's unit publication orders them before every later reader
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4)
+    if (lane == s4) P.mask[((size_t)t * d.nb + b) * 4 + s4] = word[s4];
+  if (slot == 0 && __any_sync(0xffffffffu, xbad) && lane == 0) atomicOr(P.err, kErrXNonFinite);
+  if (b == 0) {
+    if (lane == 0) {
+      int e = P.ids_in[ts];
+      const float wv = P.w_in[ts];
+      uint32_t bits = 0;
+      if (e < 0 || e >= d.E) {
+        bits |= kErrExpertRange;
+        e = 0;
+      }
+      for (int s2 = 0; s2 < slot; ++s2)
+        if (P.ids_in[t * d.topk + s2] == P.ids_in[ts]) bits |= kErrExpertDup;
+      if (!(wv >= 0.f) || !isfinite(wv)) bits |= kErrWeight;
+      if (bits) atomicOr(P.err, bits);
+      P.ids_ws[ts] = e;
+      P.w_ws[ts] = wv;
+    }
+    if (slot == 0)
+      for (int j = lane; j < d.r; j += 32) P.cvec[(size_t)t * d.r + j] = 0.f;
+  }
+  // the screened list in ascending coordinate order; an odd count's spare
+  // position repeats the last coordinate
+  const uint32_t below = (1u << lane) - 1u;
+  int listed = 0;
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4) {
+    if ((word[s4] >> lane) & 1u) {
+      const int pos = listed + __popc(word[s4] & below);
+      cbuf[pos] = (uint8_t)(lane + 32 * s4);
+      rbuf[pos] = xu[s4];
+      if (pos == d.c - 1 && (d.c & 1)) cbuf[d.c] = (uint8_t)(lane + 32 * s4);
+    }
+    listed += __popc(word[s4]);
+  }
+  __syncwarp();
+  float rv[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) rv[v] = 4 * lane + v < d.c ? rbuf[4 * lane + v] : 0.f;
+  // pair tables: lane l holds list positions 4l .. 4l+3, i.e. pairs 2l, 2l+1
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int p = 4 * lane + 2 * h;
+    if (p < d.c) {
+      const float r0 = rv[2 * h], r1 = p + 1 < d.c ? rv[2 * h + 1] : 0.f;
+      float4* tab = reinterpret_cast<float4*>(buf) + (p >> 1) * 4;
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const float t1 = g4 == 1 ? r1 : (g4 == 3 ? -r1 : 0.f);   // code of the odd position
+        tab[g4] = make_float4(t1, r0 + t1, t1, t1 - r0);         // even position 00 01 10 11
+      }
+    }
+  }
+  return (e_raw < 0 || e_raw >= d.E) ? 0 : e_raw;
+}
+
 // A team of tw warps owns whole units (team k takes the CTA's units k,
 // k + nteams, ...).  Per unit the team's first warp writes the pair tables,
 // the screened coordinates and the expert id into one of two unit buffers.
@@ -1091,81 +1204,12 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     }
     xbad = rotate_load(P, t, b, ts - t * d.topk, lane, xu);
     enext = P.ids_in[ts];
+    if (lane == 0 && team == 0) TRACE_POINT(1);
   };
   auto write_unit = [&](int n) {   // first warp: unit n's tables, coordinates and expert
     unsigned char* buf = ubuf + (size_t)(n & 1) * sp.buf_bytes;
-    uint8_t* cbuf = buf + sp.coord_off;
-    float* rbuf = reinterpret_cast<float*>(cbuf + 128);
-    const int uu = unit_of(n), b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk, slot = ts % d.topk;
-    uint32_t word[4];
-    rotate_select_loaded(P, lane, xu, word);
-    if (d.rho_rank) {   // ||(R x)_b||^2 for the expected-error ranking (every slot writes it)
-      const float ss = warp_sum(xu[0] * xu[0] + xu[1] * xu[1] + xu[2] * xu[2] + xu[3] * xu[3]);
-      if (lane == 0) P.rn2[(size_t)t * d.nb + b] = ss;
-    }
-    // the unit's side outputs: the block's screened set (the same from every
-    // slot), the input checks, and at block 0 the slot's sanitised expert id
-    // and weight (and, for slot 0, the token's zeroed recovery vector); the
-    // warp's unit publication orders them before every later reader
-#pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4)
-      if (lane == s4) P.mask[((size_t)t * d.nb + b) * 4 + s4] = word[s4];
-    if (slot == 0 && __any_sync(0xffffffffu, xbad) && lane == 0) atomicOr(P.err, kErrXNonFinite);
-    if (b == 0) {
-      if (lane == 0) {
-        int e = P.ids_in[ts];
-        const float wv = P.w_in[ts];
-        uint32_t bits = 0;
-        if (e < 0 || e >= d.E) {
-          bits |= kErrExpertRange;
-          e = 0;
-        }
-        for (int s2 = 0; s2 < slot; ++s2)
-          if (P.ids_in[t * d.topk + s2] == P.ids_in[ts]) bits |= kErrExpertDup;
-        if (!(wv >= 0.f) || !isfinite(wv)) bits |= kErrWeight;
-        if (bits) atomicOr(P.err, bits);
-        P.ids_ws[ts] = e;
-        P.w_ws[ts] = wv;
-      }
-      if (slot == 0)
-        for (int j = lane; j < d.r; j += 32) P.cvec[(size_t)t * d.r + j] = 0.f;
-    }
-    // the screened list in ascending coordinate order; an odd count's spare
-    // position repeats the last coordinate
-    const uint32_t below = (1u << lane) - 1u;
-    int listed = 0;
-#pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) {
-      if ((word[s4] >> lane) & 1u) {
-        const int pos = listed + __popc(word[s4] & below);
-        cbuf[pos] = (uint8_t)(lane + 32 * s4);
-        rbuf[pos] = xu[s4];
-        if (pos == d.c - 1 && (d.c & 1)) cbuf[d.c] = (uint8_t)(lane + 32 * s4);
-      }
-      listed += __popc(word[s4]);
-    }
-    __syncwarp();
-    float rv[4];
-#pragma unroll
-    for (int v = 0; v < 4; ++v) rv[v] = 4 * lane + v < d.c ? rbuf[4 * lane + v] : 0.f;
-    // pair tables: lane l holds list positions 4l .. 4l+3, i.e. pairs 2l, 2l+1
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int p = 4 * lane + 2 * h;
-      if (p < d.c) {
-        const float r0 = rv[2 * h], r1 = p + 1 < d.c ? rv[2 * h + 1] : 0.f;
-        float4* tab = reinterpret_cast<float4*>(buf) + (p >> 1) * 4;
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const float t1 = g4 == 1 ? r1 : (g4 == 3 ? -r1 : 0.f);   // code of the odd position
-          tab[g4] = make_float4(t1, r0 + t1, t1, t1 - r0);         // even position 00 01 10 11
-        }
-      }
-    }
-    if (lane == 0) {
-      int e = enext;
-      flag[2 + (n & 1)] = (e < 0 || e >= d.E) ? 0 : e;
-    }
+    const int e = build_unit(P, buf, unit_of(n), lane, xu, xbad, enext, team);
+    if (lane == 0) flag[2 + (n & 1)] = e;
   };
   // asynchronous copies of chunk j (unit j / nch, chunk j % nch) into stage j % 2
   auto issue = [&](int j) {
@@ -1210,10 +1254,12 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   if (tw_i == 0) {
     load_list(unit_of(0));
     write_unit(0);
+    if (lane == 0 && team == 0) TRACE_POINT(18);
     if (unit_of(1) < units) load_list(unit_of(1));
   }
   team_sync(team, TT);
   issue(0);
+  if (tt == 0 && team == 0) TRACE_POINT(19);
   float acc[WPT][16];
   uint4 al[WPT][2];
   int pend = -1;
@@ -1228,8 +1274,10 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     }
     if (ch == 0) team_sync(team, TT);   // unit n + 1's buffer is written
     issue(j + 1);
+    if (tt == 0 && team == 0 && j == 0) TRACE_POINT(20);
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     team_sync(team, TT);   // every thread's copies of chunk j have landed
+    if (tt == 0 && team == 0) TRACE_POINT(3);
     const int e = flag[2 + (n & 1)];
     const int ts = u / d.nb, b = u % d.nb;
     // alpha of the thread's channels: requested with the first chunk when
@@ -1321,20 +1369,195 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   if (pend >= 0) publish_unit(P, pend, lane);
+  if (tt == 0) TRACE_POINT(4);
 }
 
+// Small batches (every group of f teams gets at most one unit): the f teams
+// of a group share one unit, each summing a contiguous slice of its
+// coordinate pairs, and the group's first team adds the f partial sums in
+// slice order.  Barrier 1 + group spans the group's f teams.
+template <int WPT>
+__device__ void screen_split(const Params& P, unsigned char* smem, int team, int tt, int f) {
+  const Dims& d = P.d;
+  const ScreenPlan& sp = P.sp;
+  const int lane = threadIdx.x & 31, tw_i = tt >> 5;
+  const int TT = 32 * sp.tw, R16 = d.I / 16, W4 = 2 * R16;
+  const int group = team / f, q = team % f;
+  const int units = P.B * d.topk * d.nb;
+  const int uu = blockIdx.x + group * (int)gridDim.x;
+  if (uu >= units) return;                       // the group's teams all leave together
+  const uint32_t S2 = 2u * (uint32_t)d.S;
+  const int P16 = (int)(S2 / 16);
+  unsigned char* gsm = smem + (size_t)(group * f) * sp.team_bytes;    // the group's first team
+  volatile int* flag = reinterpret_cast<volatile int*>(gsm);
+  unsigned char* buf = gsm + 256;                                       // its unit buffer 0
+  unsigned char* tsm = smem + (size_t)team * sp.team_bytes;
+  unsigned char* stage = tsm + 256 + 2 * (size_t)sp.buf_bytes;         // this team's stage 0
+  float* red = reinterpret_cast<float*>(stage + sp.stage_bytes);         // this team's stage 1
+  auto group_sync = [&]() {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(f * TT) : "memory");
+  };
+  uint32_t off[WPT];
+  int gv[WPT], jw[WPT];
+  bool has[WPT];
+#pragma unroll
+  for (int x = 0; x < WPT; ++x) {
+    const int w = tt + TT * x;
+    has[x] = w < W4;
+    gv[x] = has[x] ? w / R16 : 0;
+    jw[x] = has[x] ? w % R16 : 0;
+    off[x] = (uint32_t)(gv[x] * d.S + jw[x] * 4);
+  }
+  const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
+  if (q == 0 && tw_i == 0) {
+    float xu[4];
+    if (P.xwait) {   // a stacked layer: token t's input comes from the layer before
+      int ok = 1;
+      if (lane == 0) ok = wait_at_least(P, P.xwait + t, 1u);
+      __shfl_sync(0xffffffffu, ok, 0);   // on a timeout the abort flag ends the launch
+      __syncwarp();
+    }
+    const bool xbad = rotate_load(P, t, b, ts - t * d.topk, lane, xu);
+    if (lane == 0) TRACE_POINT(1);
+    const int e = build_unit(P, buf, uu, lane, xu, xbad, P.ids_in[ts], team);
+    if (lane == 0) flag[2] = e;
+  }
+  group_sync();   // the unit buffer is written
+  if (tt == 0 && q == 0) TRACE_POINT(25);
+  const int e = flag[2];
+  // this team's pairs [pr0, pr1) of the list, staged from stage slot 0
+  const int npair = (d.c + 1) >> 1, per = (npair + f - 1) / f;
+  const int pr0 = min(npair, q * per), pr1 = min(npair, pr0 + per);
+  const int p0 = 2 * pr0, npos = min(d.c, 2 * pr1) - p0;
+  const uint8_t* coords = buf + sp.coord_off;
+  {
+    const uint8_t* rec = P.codes + ((size_t)e * d.nb + b) * kBlock * S2;
+    const uint32_t dst0 = smem_addr(stage);
+    const int pieces = npos * P16;
+    for (int qq = tt; qq < pieces; qq += TT) {
+      const int p = qq / P16, o = qq - p * P16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + (uint32_t)p * S2 + 16u * o),
+                   "l"(rec + (size_t)coords[p0 + p] * S2 + 16 * o)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  uint4 al[WPT][2];
+  if (q == 0) {   // the reducing team's alpha, requested while the codes land
+#pragma unroll
+    for (int x = 0; x < WPT; ++x) {
+      const uint4* a4 = reinterpret_cast<const uint4*>(
+          P.scales + (((size_t)e * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
+      al[x][0] = has[x] ? ldg_nc4(a4) : make_uint4(0u, 0u, 0u, 0u);
+      al[x][1] = has[x] ? ldg_nc4(a4 + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  group_sync();   // every team's records have landed
+  if (tt == 0 && q == 0) TRACE_POINT(26);
+  float acc[WPT][16];
+#pragma unroll
+  for (int x = 0; x < WPT; ++x)
+#pragma unroll
+    for (int m = 0; m < 16; ++m) acc[x][m] = 0.f;
+  const uint32_t stg = smem_addr(stage);
+  const uint32_t lut_base = smem_addr(buf);
+  for (int pp = pr0; pp < pr1; ++pp) {
+    const uint32_t blk = lut_base + 256u * (uint32_t)(pp >> 2);
+    const uint32_t sub = (uint32_t)(pp & 3) * 0x40404040u;
+    const uint32_t ra = stg + (uint32_t)(2 * (pp - pr0)) * S2;
+#pragma unroll
+    for (int x = 0; x < WPT; ++x) {
+      // an odd count's last pair reads a stage slot that was not copied; its
+      // table ignores the odd position's code
+      const uint32_t wa = has[x] ? lds_u32(ra + off[x]) : 0u;
+      const uint32_t wb = has[x] ? lds_u32(ra + S2 + off[x]) : 0u;
+      const uint32_t ze = (wa & 0x33333333u) | ((wb << 2) & 0xCCCCCCCCu);
+      const uint32_t zo = ((wa >> 2) & 0x33333333u) | (wb & 0xCCCCCCCCu);
+      const uint32_t bee = ((ze << 2) & 0x3C3C3C3Cu) | sub;
+      const uint32_t beo = ((ze >> 2) & 0x3C3C3C3Cu) | sub;
+      const uint32_t boe = ((zo << 2) & 0x3C3C3C3Cu) | sub;
+      const uint32_t boo = ((zo >> 2) & 0x3C3C3C3Cu) | sub;
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const uint32_t sel = 0x7650u + kb;
+        acc[x][4 * kb] += lds_f32(__byte_perm(bee, blk, sel));
+        acc[x][4 * kb + 1] += lds_f32(__byte_perm(boe, blk, sel));
+        acc[x][4 * kb + 2] += lds_f32(__byte_perm(beo, blk, sel));
+        acc[x][4 * kb + 3] += lds_f32(__byte_perm(boo, blk, sel));
+      }
+    }
+  }
+  if (q > 0) {
+#pragma unroll
+    for (int x = 0; x < WPT; ++x)
+#pragma unroll
+      for (int m = 0; m < 16; ++m) red[((size_t)tt * WPT + x) * 16 + m] = acc[x][m];
+  }
+  if (tt == 0 && q == 0) TRACE_POINT(27);
+  group_sync();   // every slice's sums are in
+  if (tt == 0 && q == 0) TRACE_POINT(28);
+  if (q > 0) return;
+  for (int qq = 1; qq < f; ++qq) {   // slices in order: the same sum whatever the timing
+    const float* rq = reinterpret_cast<const float*>(
+        smem + (size_t)(team + qq) * sp.team_bytes + 256 + 2 * (size_t)sp.buf_bytes + sp.stage_bytes);
+#pragma unroll
+    for (int x = 0; x < WPT; ++x)
+#pragma unroll
+      for (int m = 0; m < 16; ++m) acc[x][m] += rq[((size_t)tt * WPT + x) * 16 + m];
+  }
+#pragma unroll
+  for (int x = 0; x < WPT; ++x) {
+    if (!has[x]) continue;
+    const uint32_t hw[8] = {al[x][0].x, al[x][0].y, al[x][0].z, al[x][0].w,
+                            al[x][1].x, al[x][1].y, al[x][1].z, al[x][1].w};
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&hw[m]));
+      acc[x][2 * m] *= fa.x;
+      acc[x][2 * m + 1] *= fa.y;
+    }
+    float4* out = reinterpret_cast<float4*>(
+        P.partial + (((size_t)ts * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      out[m] = make_float4(acc[x][4 * m], acc[x][4 * m + 1], acc[x][4 * m + 2], acc[x][4 * m + 3]);
+  }
+  publish_unit(P, ts, lane);
+  if (tt == 0) TRACE_POINT(4);
+}
+
+// Teams per unit at batch B: the largest f with every group of f teams
+// taking at most one unit, when the slices fit the stages (1 = no split).
+__host__ __device__ inline int screen_split_factor(const Dims& d, const ScreenPlan& sp, int B,
+                                                   int nctas) {
+  const long long units = (long long)B * d.topk * d.nb;
+  int f = 1;
+  for (int cand = 2; cand <= sp.nteams; ++cand) {
+    const long long groups = (long long)(sp.nteams / cand) * nctas;
+    if (groups < units) break;
+    const int npair = (d.c + 1) / 2, per = (npair + cand - 1) / cand;
+    const bool fits = 2 * per <= sp.cc + 1 && (size_t)32 * sp.tw * sp.wpt * 64 <= (size_t)sp.stage_bytes;
+    if (fits) f = cand;
+  }
+  return f;
+}
+
+// Phase 1a of a CTA: WPT code words per thread, SPLIT: the small-batch split
+// screen (the launcher picks the kernel whose SPLIT matches the batch).
+template <int WPT, bool SPLIT>
 __device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
   const ScreenPlan& sp = P.sp;
   const int team = warp / sp.tw;
   if (team >= sp.nteams) return;   // warps left over by the team size
-  unsigned char* tsm = smem + (size_t)team * sp.team_bytes;
   const int tt = (warp % sp.tw) * 32 + (threadIdx.x & 31);
-  if (sp.wpt == 1)
-    screen_team<1>(P, tsm, team, tt);
-  else if (sp.wpt == 2)
-    screen_team<2>(P, tsm, team, tt);
-  else
-    screen_team<3>(P, tsm, team, tt);
+  if (SPLIT) {
+    const int f = screen_split_factor(P.d, sp, P.B, gridDim.x);
+    if (team >= (sp.nteams / f) * f) return;   // teams left over by the group size
+    screen_split<WPT>(P, smem, team, tt, f);
+  } else {
+    screen_team<WPT>(P, smem + (size_t)team * sp.team_bytes, team, tt);
+  }
 }
 
 // Score the channels of one (token, slot) once all its blocks are in: sum
@@ -1351,6 +1574,7 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
   __syncthreads();
   if (!*flag) return -1;
   int e = P.ids_in[ts];
+  if (threadIdx.x == 0) TRACE_POINT(6);
   if (e < 0 || e >= d.E) e = 0;
   const float wv = P.w_in[ts];
   const float* pg0 = P.partial + ((size_t)ts * d.nb) * 2 * I;
@@ -1391,6 +1615,7 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
         v[1] += __ldcg(pb + I + i2);
       }
     }
+    if (threadIdx.x == 0) TRACE_POINT(21);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (h == 1 && !two) break;
@@ -1435,6 +1660,7 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
     // releases this slot's scores; the last slot in also acquires the others'
     const uint32_t prev = atom_add_acq_rel(P.sync + so.tok + t, 1u);
     *flag = prev == (uint32_t)(d.topk - 1);
+    TRACE_POINT(7);
   }
   __syncthreads();
   return *flag ? 1 : 0;
@@ -1774,6 +2000,7 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
   auto counted = [&]() {
     if (ow.count_t == t) return true;
     if (!out_wait(P, P.sync + so.exact + t, (uint32_t)per_tok, lane)) return false;
+    if (lane == 0) TRACE_POINT(15);
     if (SH && !ow.shared_in) {
       if (!out_wait(P, P.sync + kSyncSdone, (uint32_t)__ldcg(P.sK), lane)) return false;
       ow.shared_in = true;
@@ -1965,7 +2192,7 @@ __device__ bool shared_out_chunk(const Params& P, int c, int cb, int RCs, int K,
 
 // ------------------------------- the kernel --------------------------------
 // One layer's decode by every CTA of the grid.  false: the launch is aborting.
-template <bool SH>
+template <bool SH, int WPT, bool SPLIT>
 __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* smem, int* ctl) {
   if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
@@ -1974,11 +2201,13 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   const int nctas = gridDim.x;
   unsigned long long* stamp = P.stamps ? P.stamps + (size_t)blockIdx.x * 5 : nullptr;
   if (stamp && threadIdx.x == 0) stamp[0] = globaltimer();
+  if (threadIdx.x == 0) TRACE_POINT(0);
 
   // phase 1a: screen units (rotation, selection and sketch sums), computed by teams of warps
-  screen_compute(P, smem, warp);
+  screen_compute<WPT, SPLIT>(P, smem, warp);
   __syncthreads();
   if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
+  if (threadIdx.x == 0) TRACE_POINT(5);
   // phase 1b: scoring tasks spread over the CTAs; the CTA that scores a
   // token's last slot runs the token's top-k (1c) at once
   {
@@ -2084,6 +2313,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
         __syncwarp();
         cur_t = t;
         sl = load_token_slots(P, t, lane);
+        if (lane == 0 && warp == 0) TRACE_POINT(13);
         kbase = -64;
       }
       const bool flush = pend_t >= 0 && pend_t != t;   // leaving token pend_t
@@ -2103,6 +2333,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     if (ok) publish_item(P, pend_t, pend_n, lane);
   }
   }
+  if (lane == 0) TRACE_POINT(14);
   if (stamp) {
     __syncthreads();
     if (threadIdx.x == 0) stamp[3] = globaltimer();
@@ -2156,6 +2387,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     }
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
+  if (threadIdx.x == 0) TRACE_POINT(16);
   // the last CTA out resets the synchronisation area for the next call
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -2201,21 +2433,36 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
 }
 
 // The batch-shared selection variant: one kept set for the whole batch.
+// Kernels are specialised on the screen's code words per thread (WPT) and on
+// the small-batch split screen, so that each holds only the code it runs.
+template <int WPT>
 __global__ void __launch_bounds__(kThreads, 1) decode_shared_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  decode_layer<true>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<true, WPT, false>(P, aligned_smem(smem_raw), ctl);
 }
 
+template <int WPT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  decode_layer<false>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<false, WPT, SPLIT>(P, aligned_smem(smem_raw), ctl);
+  if (threadIdx.x == 0) TRACE_POINT(17);
   if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
     // the next layer would wait for inputs that never come
     atomicOr(P.next_err, kErrTimeout);
     atomicExch(P.next_abort, 1u);
   }
+}
+
+using KernelFn = void (*)(const Params);
+
+// The kernel for a decode: shared selection or not, the shape's code words per
+// thread, and the split screen when the batch is small enough for it.
+KernelFn pick_kernel(bool shared, int wpt, bool split) {
+  if (shared) return wpt == 1 ? decode_shared_kernel<1> : wpt == 2 ? decode_shared_kernel<2> : decode_shared_kernel<3>;
+  if (split) return wpt == 1 ? decode_kernel<1, true> : wpt == 2 ? decode_kernel<2, true> : decode_kernel<3, true>;
+  return wpt == 1 ? decode_kernel<1, false> : wpt == 2 ? decode_kernel<2, false> : decode_kernel<3, false>;
 }
 
 size_t decode_smem_bytes(const Dims& d) {
@@ -2229,6 +2476,19 @@ size_t decode_smem_bytes(const Dims& d) {
 
 size_t sync_words(const Dims& d) { return (size_t)sync_offsets(d).total; }
 
+#ifdef MR_TRACE
+}  // namespace mr
+extern "C" int moe_reader_trace_read(unsigned long long* host, int clear) {
+  if (cudaMemcpyFromSymbol(host, mr::g_trace, sizeof(mr::g_trace)) != cudaSuccess) return -3;
+  if (clear) {
+    static unsigned long long zero[mr::kTraceCtas][mr::kTracePoints];
+    if (cudaMemcpyToSymbol(mr::g_trace, zero, sizeof(zero)) != cudaSuccess) return -3;
+  }
+  return 0;
+}
+namespace mr {
+#endif
+
 bool shared_supported(const Dims& d, int B) {
   // the selection CTA's tables and the score tasks' slot lists fit the
   // decode's shared memory; the elist packing holds 8192 token slots
@@ -2238,28 +2498,28 @@ bool shared_supported(const Dims& d, int B) {
 }
 
 cudaError_t configure_decode_kernels(const Dims& d) {
-  if (screen_plan(d).bytes == 0) return cudaErrorInvalidValue;
+  const ScreenPlan sp = screen_plan(d);
+  if (sp.bytes == 0) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes(d);
-  cudaFuncAttributes fa;
-  cudaError_t err = cudaFuncGetAttributes(&fa, decode_kernel);
-  if (err != cudaSuccess) return err;
-  if ((size_t)fa.maxDynamicSharedSizeBytes < smem)
-    err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-  if (err != cudaSuccess) return err;
-  if ((err = cudaFuncGetAttributes(&fa, decode_shared_kernel)) != cudaSuccess) return err;
-  if ((size_t)fa.maxDynamicSharedSizeBytes < smem)
-    err = cudaFuncSetAttribute(decode_shared_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
-  return err;
+  for (int v = 0; v < 3; ++v) {   // the shape's kernels: per-token, split, shared
+    const KernelFn fn = pick_kernel(v == 2, sp.wpt, v == 1);
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, fn);
+    if (err != cudaSuccess) return err;
+    if ((size_t)fa.maxDynamicSharedSizeBytes < smem &&
+        (err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+            cudaSuccess)
+      return err;
+  }
+  return cudaSuccess;
 }
 
 int decode_grid(const Dims& d) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads,
-                                                    decode_smem_bytes(d)) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pick_kernel(false, screen_plan(d).wpt, false),
+                                                    kThreads, decode_smem_bytes(d)) != cudaSuccess)
     return 0;
   return per_sm >= 1 ? sms : 0;   // one CTA per SM, all co-resident
 }
@@ -2364,8 +2624,8 @@ static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStrea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return shared ? cudaLaunchKernelEx(&cfg, decode_shared_kernel, P)
-                : cudaLaunchKernelEx(&cfg, decode_kernel, P);
+  const bool split = !shared && screen_split_factor(h.d, P.sp, P.B, h.grid) > 1;
+  return cudaLaunchKernelEx(&cfg, pick_kernel(shared, P.sp.wpt, split), P);
 }
 
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
