@@ -1067,6 +1067,7 @@ __device__ __forceinline__ void team_sync(int team, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(threads) : "memory");
 }
 
+
 // Publish a stored unit: the warp's partial stores, then (release add) its
 // share of the (token, slot) counter (complete at nb * tw).
 __device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) {
@@ -1268,12 +1269,16 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     const int u = unit_of(n);
     if (u >= units) break;
     team_sync(team, TT);   // chunk j - 1 is summed by everyone: its stage and unit buffer are free
+    // chunk j + 1 from this unit's buffer goes out before the next unit's
+    // rotation and selection, which then run while it is in flight
+    const bool early = ch + 1 < sp.nch;
+    if (early) issue(j + 1);
     if (ch == 0 && tw_i == 0 && unit_of(n + 1) < units) {
       write_unit(n + 1);
       if (unit_of(n + 2) < units) load_list(unit_of(n + 2));   // in flight while unit n is summed
     }
     if (ch == 0) team_sync(team, TT);   // unit n + 1's buffer is written
-    issue(j + 1);
+    if (!early) issue(j + 1);
     if (tt == 0 && team == 0 && j == 0) TRACE_POINT(20);
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     team_sync(team, TT);   // every thread's copies of chunk j have landed
@@ -1372,192 +1377,14 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   if (tt == 0) TRACE_POINT(4);
 }
 
-// Small batches (every group of f teams gets at most one unit): the f teams
-// of a group share one unit, each summing a contiguous slice of its
-// coordinate pairs, and the group's first team adds the f partial sums in
-// slice order.  Barrier 1 + group spans the group's f teams.
+// Phase 1a of a CTA: its teams' screen units, WPT code words per thread.
 template <int WPT>
-__device__ void screen_split(const Params& P, unsigned char* smem, int team, int tt, int f) {
-  const Dims& d = P.d;
-  const ScreenPlan& sp = P.sp;
-  const int lane = threadIdx.x & 31, tw_i = tt >> 5;
-  const int TT = 32 * sp.tw, R16 = d.I / 16, W4 = 2 * R16;
-  const int group = team / f, q = team % f;
-  const int units = P.B * d.topk * d.nb;
-  const int uu = blockIdx.x + group * (int)gridDim.x;
-  if (uu >= units) return;                       // the group's teams all leave together
-  const uint32_t S2 = 2u * (uint32_t)d.S;
-  const int P16 = (int)(S2 / 16);
-  unsigned char* gsm = smem + (size_t)(group * f) * sp.team_bytes;    // the group's first team
-  volatile int* flag = reinterpret_cast<volatile int*>(gsm);
-  unsigned char* buf = gsm + 256;                                       // its unit buffer 0
-  unsigned char* tsm = smem + (size_t)team * sp.team_bytes;
-  unsigned char* stage = tsm + 256 + 2 * (size_t)sp.buf_bytes;         // this team's stage 0
-  float* red = reinterpret_cast<float*>(stage + sp.stage_bytes);         // this team's stage 1
-  auto group_sync = [&]() {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(f * TT) : "memory");
-  };
-  uint32_t off[WPT];
-  int gv[WPT], jw[WPT];
-  bool has[WPT];
-#pragma unroll
-  for (int x = 0; x < WPT; ++x) {
-    const int w = tt + TT * x;
-    has[x] = w < W4;
-    gv[x] = has[x] ? w / R16 : 0;
-    jw[x] = has[x] ? w % R16 : 0;
-    off[x] = (uint32_t)(gv[x] * d.S + jw[x] * 4);
-  }
-  const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
-  if (q == 0 && tw_i == 0) {
-    float xu[4];
-    if (P.xwait) {   // a stacked layer: token t's input comes from the layer before
-      int ok = 1;
-      if (lane == 0) ok = wait_at_least(P, P.xwait + t, 1u);
-      __shfl_sync(0xffffffffu, ok, 0);   // on a timeout the abort flag ends the launch
-      __syncwarp();
-    }
-    const bool xbad = rotate_load(P, t, b, ts - t * d.topk, lane, xu);
-    if (lane == 0) TRACE_POINT(1);
-    const int e = build_unit(P, buf, uu, lane, xu, xbad, P.ids_in[ts], team);
-    if (lane == 0) flag[2] = e;
-  }
-  group_sync();   // the unit buffer is written
-  if (tt == 0 && q == 0) TRACE_POINT(25);
-  const int e = flag[2];
-  // this team's pairs [pr0, pr1) of the list, staged from stage slot 0
-  const int npair = (d.c + 1) >> 1, per = (npair + f - 1) / f;
-  const int pr0 = min(npair, q * per), pr1 = min(npair, pr0 + per);
-  const int p0 = 2 * pr0, npos = min(d.c, 2 * pr1) - p0;
-  const uint8_t* coords = buf + sp.coord_off;
-  {
-    const uint8_t* rec = P.codes + ((size_t)e * d.nb + b) * kBlock * S2;
-    const uint32_t dst0 = smem_addr(stage);
-    const int pieces = npos * P16;
-    for (int qq = tt; qq < pieces; qq += TT) {
-      const int p = qq / P16, o = qq - p * P16;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + (uint32_t)p * S2 + 16u * o),
-                   "l"(rec + (size_t)coords[p0 + p] * S2 + 16 * o)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
-  uint4 al[WPT][2];
-  if (q == 0) {   // the reducing team's alpha, requested while the codes land
-#pragma unroll
-    for (int x = 0; x < WPT; ++x) {
-      const uint4* a4 = reinterpret_cast<const uint4*>(
-          P.scales + (((size_t)e * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
-      al[x][0] = has[x] ? ldg_nc4(a4) : make_uint4(0u, 0u, 0u, 0u);
-      al[x][1] = has[x] ? ldg_nc4(a4 + 1) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  group_sync();   // every team's records have landed
-  if (tt == 0 && q == 0) TRACE_POINT(26);
-  float acc[WPT][16];
-#pragma unroll
-  for (int x = 0; x < WPT; ++x)
-#pragma unroll
-    for (int m = 0; m < 16; ++m) acc[x][m] = 0.f;
-  const uint32_t stg = smem_addr(stage);
-  const uint32_t lut_base = smem_addr(buf);
-  for (int pp = pr0; pp < pr1; ++pp) {
-    const uint32_t blk = lut_base + 256u * (uint32_t)(pp >> 2);
-    const uint32_t sub = (uint32_t)(pp & 3) * 0x40404040u;
-    const uint32_t ra = stg + (uint32_t)(2 * (pp - pr0)) * S2;
-#pragma unroll
-    for (int x = 0; x < WPT; ++x) {
-      // an odd count's last pair reads a stage slot that was not copied; its
-      // table ignores the odd position's code
-      const uint32_t wa = has[x] ? lds_u32(ra + off[x]) : 0u;
-      const uint32_t wb = has[x] ? lds_u32(ra + S2 + off[x]) : 0u;
-      const uint32_t ze = (wa & 0x33333333u) | ((wb << 2) & 0xCCCCCCCCu);
-      const uint32_t zo = ((wa >> 2) & 0x33333333u) | (wb & 0xCCCCCCCCu);
-      const uint32_t bee = ((ze << 2) & 0x3C3C3C3Cu) | sub;
-      const uint32_t beo = ((ze >> 2) & 0x3C3C3C3Cu) | sub;
-      const uint32_t boe = ((zo << 2) & 0x3C3C3C3Cu) | sub;
-      const uint32_t boo = ((zo >> 2) & 0x3C3C3C3Cu) | sub;
-#pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
-        const uint32_t sel = 0x7650u + kb;
-        acc[x][4 * kb] += lds_f32(__byte_perm(bee, blk, sel));
-        acc[x][4 * kb + 1] += lds_f32(__byte_perm(boe, blk, sel));
-        acc[x][4 * kb + 2] += lds_f32(__byte_perm(beo, blk, sel));
-        acc[x][4 * kb + 3] += lds_f32(__byte_perm(boo, blk, sel));
-      }
-    }
-  }
-  if (q > 0) {
-#pragma unroll
-    for (int x = 0; x < WPT; ++x)
-#pragma unroll
-      for (int m = 0; m < 16; ++m) red[((size_t)tt * WPT + x) * 16 + m] = acc[x][m];
-  }
-  if (tt == 0 && q == 0) TRACE_POINT(27);
-  group_sync();   // every slice's sums are in
-  if (tt == 0 && q == 0) TRACE_POINT(28);
-  if (q > 0) return;
-  for (int qq = 1; qq < f; ++qq) {   // slices in order: the same sum whatever the timing
-    const float* rq = reinterpret_cast<const float*>(
-        smem + (size_t)(team + qq) * sp.team_bytes + 256 + 2 * (size_t)sp.buf_bytes + sp.stage_bytes);
-#pragma unroll
-    for (int x = 0; x < WPT; ++x)
-#pragma unroll
-      for (int m = 0; m < 16; ++m) acc[x][m] += rq[((size_t)tt * WPT + x) * 16 + m];
-  }
-#pragma unroll
-  for (int x = 0; x < WPT; ++x) {
-    if (!has[x]) continue;
-    const uint32_t hw[8] = {al[x][0].x, al[x][0].y, al[x][0].z, al[x][0].w,
-                            al[x][1].x, al[x][1].y, al[x][1].z, al[x][1].w};
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&hw[m]));
-      acc[x][2 * m] *= fa.x;
-      acc[x][2 * m + 1] *= fa.y;
-    }
-    float4* out = reinterpret_cast<float4*>(
-        P.partial + (((size_t)ts * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-      out[m] = make_float4(acc[x][4 * m], acc[x][4 * m + 1], acc[x][4 * m + 2], acc[x][4 * m + 3]);
-  }
-  publish_unit(P, ts, lane);
-  if (tt == 0) TRACE_POINT(4);
-}
-
-// Teams per unit at batch B: the largest f with every group of f teams
-// taking at most one unit, when the slices fit the stages (1 = no split).
-__host__ __device__ inline int screen_split_factor(const Dims& d, const ScreenPlan& sp, int B,
-                                                   int nctas) {
-  const long long units = (long long)B * d.topk * d.nb;
-  int f = 1;
-  for (int cand = 2; cand <= sp.nteams; ++cand) {
-    const long long groups = (long long)(sp.nteams / cand) * nctas;
-    if (groups < units) break;
-    const int npair = (d.c + 1) / 2, per = (npair + cand - 1) / cand;
-    const bool fits = 2 * per <= sp.cc + 1 && (size_t)32 * sp.tw * sp.wpt * 64 <= (size_t)sp.stage_bytes;
-    if (fits) f = cand;
-  }
-  return f;
-}
-
-// Phase 1a of a CTA: WPT code words per thread, SPLIT: the small-batch split
-// screen (the launcher picks the kernel whose SPLIT matches the batch).
-template <int WPT, bool SPLIT>
 __device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
   const ScreenPlan& sp = P.sp;
   const int team = warp / sp.tw;
   if (team >= sp.nteams) return;   // warps left over by the team size
   const int tt = (warp % sp.tw) * 32 + (threadIdx.x & 31);
-  if (SPLIT) {
-    const int f = screen_split_factor(P.d, sp, P.B, gridDim.x);
-    if (team >= (sp.nteams / f) * f) return;   // teams left over by the group size
-    screen_split<WPT>(P, smem, team, tt, f);
-  } else {
-    screen_team<WPT>(P, smem + (size_t)team * sp.team_bytes, team, tt);
-  }
+  screen_team<WPT>(P, smem + (size_t)team * sp.team_bytes, team, tt);
 }
 
 // Score the channels of one (token, slot) once all its blocks are in: sum
@@ -1706,55 +1533,6 @@ __device__ __forceinline__ TokenSlots load_token_slots(const Params& P, int t, i
   return ts;
 }
 
-// Kept channel n (list position qi) of token t: a = phi(g^T x)(v^T x) from the
-// native rows, stored as w a.  The kept index and the token's slots were read
-// ahead by the caller, so the row loads are the item's only round trip.
-__device__ void kept_item(const Params& P, int t, int qi, int n, const TokenSlots& sl, int lane,
-                          int pend_t, int pend_n) {
-  const Dims& d = P.d;
-  publish_item(P, pend_t, pend_n, lane);
-
-  const int slot = n / d.I, i = n % d.I;
-  const int e = slot_expert(sl.e0, sl.e1, slot);
-  const float wslot =
-      __int_as_float(slot_expert(__float_as_int(sl.w0), __float_as_int(sl.w1), slot));
-  const size_t row = (size_t)e * d.I + i;
-  const uint64_t pol = policy_evict_first();
-  const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
-  const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
-  const float4* x4 = reinterpret_cast<const float4*>(P.x + (size_t)t * d.H);
-  float sg = 0.f, sv = 0.f;
-  const int n8 = d.H / 8;
-  int h8 = lane;
-  constexpr int kU = 8;   // 16-byte loads per lane and row issued together
-  for (; h8 + 32 * (kU - 1) < n8; h8 += 32 * kU) {
-    uint4 gq[kU], vq[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      gq[u] = ldg_nc4_hint(g4 + h8 + 32 * u, pol);
-      vq[u] = ldg_nc4_hint(v4 + h8 + 32 * u, pol);
-    }
-
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const float4 xa = x4[2 * (h8 + 32 * u)], xb = x4[2 * (h8 + 32 * u) + 1];
-      dot8(gq[u], xa, xb, sg);
-      dot8(vq[u], xa, xb, sv);
-    }
-  }
-  for (; h8 < n8; h8 += 32) {
-    const uint4 gq = ldg_nc4_hint(g4 + h8, pol), vq = ldg_nc4_hint(v4 + h8, pol);
-    const float4 xa = x4[2 * h8], xb = x4[2 * h8 + 1];
-    dot8(gq, xa, xb, sg);
-    dot8(vq, xa, xb, sv);
-  }
-  sg = warp_sum(sg);
-  sv = warp_sum(sv);
-  if (lane == 0) {
-    P.wa[(size_t)t * d.N + qi] = wslot * silu_f(sg) * sv;
-  }
-}
-
 // Kept channel q of the batch's set: its gate and up rows serve every token
 // slot routed to its expert, four tokens per pass over the rows; w a lands in
 // the token's dense [N] slot of wa.
@@ -1878,6 +1656,98 @@ __device__ void recovery_item(const Params& P, int t, int ch, int lane, int pend
   }
 }
 
+// The warp that completes token t's output in a stacked layer: hnext = hres +
+// y over all H columns (fp32), the fp64 sum of squares, and, when a next layer
+// reads it, that layer's input scale 1 / sqrt(sum / H + 1e-6) and its release.
+__device__ void carry_token(const Params& P, int t, int lane) {
+  const Dims& d = P.d;
+  const size_t row = (size_t)t * d.H;
+  double ss = 0.0;
+  for (int c0 = 4 * lane; c0 < d.H; c0 += 128) {   // H is a multiple of 8
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(P.hres + row + c0));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(P.y + row + c0));
+    const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    *reinterpret_cast<float4*>(P.hnext + row + c0) = v;
+    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
+  }
+  if (!P.xscale_next) return;   // the last layer: h_out only
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  __syncwarp();   // every lane's hnext stores precede the release
+  if (lane == 0) {
+    P.xscale_next[t] = (float)(1.0 / sqrt(ss / d.H + 1e-6));
+    st_release(P.xnext_ready + t, 1u);
+  }
+}
+
+// Count `n` output contributions of token t (kept channels added into y, or
+// one recovery output chunk) in a stacked layer; the contribution that
+// completes the token (k kept channels plus the recovery chunks) carries the
+// residual.  Returns true when the caller's warp must run carry_token.
+__device__ __forceinline__ bool count_output(const Params& P, int t, uint32_t n, uint32_t total) {
+  const uint32_t prev = atom_add_acq_rel(P.sync + sync_offsets(P.d).tokdone + t, n);
+  return prev + n == total;
+}
+
+// ---------------- exact channels and their output, per CTA (per-token) ----------------
+// Kept channel n (kept-list position qi) of token t: a = phi(g^T x)(v^T x)
+// from the native rows.  w a and the channel's row go to the CTA's lists
+// (wa_s, row_s; global wa when they do not fit), and the transposed down row
+// heads for L2: the CTA adds every kept row's output once its channels are in.
+__device__ void kept_item_cta(const Params& P, int t, int qi, int n, const TokenSlots& sl, int lane,
+                              float* wa_s, int* row_s) {
+  const Dims& d = P.d;
+  const int slot = n / d.I, i = n % d.I;
+  const int e = slot_expert(sl.e0, sl.e1, slot);
+  const float wslot =
+      __int_as_float(slot_expert(__float_as_int(sl.w0), __float_as_int(sl.w1), slot));
+  const size_t row = (size_t)e * d.I + i;
+  const uint64_t pol = policy_evict_first();
+  const uint4* g4 = reinterpret_cast<const uint4*>(P.G + row * d.H);
+  const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
+  const float4* x4 = reinterpret_cast<const float4*>(P.x + (size_t)t * d.H);
+  const int n8 = d.H / 8;
+  {
+    const uint4* d4 = reinterpret_cast<const uint4*>(P.Dt + row * d.H);
+    for (int l8 = 8 * lane; l8 < n8; l8 += 256)   // one prefetch per 128-byte line of the down row
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(d4 + l8));
+  }
+  float sg = 0.f, sv = 0.f;
+  int h8 = lane;
+  constexpr int kU = 8;   // 16-byte loads per lane and row issued together
+  for (; h8 + 32 * (kU - 1) < n8; h8 += 32 * kU) {
+    uint4 gq[kU], vq[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      gq[u] = ldg_nc4_hint(g4 + h8 + 32 * u, pol);
+      vq[u] = ldg_nc4_hint(v4 + h8 + 32 * u, pol);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const float4 xa = x4[2 * (h8 + 32 * u)], xb = x4[2 * (h8 + 32 * u) + 1];
+      dot8(gq[u], xa, xb, sg);
+      dot8(vq[u], xa, xb, sv);
+    }
+  }
+  for (; h8 < n8; h8 += 32) {
+    const uint4 gq = ldg_nc4_hint(g4 + h8, pol), vq = ldg_nc4_hint(v4 + h8, pol);
+    const float4 xa = x4[2 * h8], xb = x4[2 * h8 + 1];
+    dot8(gq, xa, xb, sg);
+    dot8(vq, xa, xb, sv);
+  }
+  sg = warp_sum(sg);
+  sv = warp_sum(sv);
+  if (lane == 0) {
+    const float wa = wslot * silu_f(sg) * sv;
+    if (wa_s) {
+      wa_s[qi] = wa;
+      row_s[qi] = (int)row;
+    } else {
+      P.wa[(size_t)t * d.N + qi] = wa;
+    }
+  }
+}
+
 // ------------------------------- phase 3 -----------------------------------
 __device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
   acc[0] = fmaf(c, bf16_lo(v.x), acc[0]); acc[1] = fmaf(c, bf16_hi(v.x), acc[1]);
@@ -1888,7 +1758,6 @@ __device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
 
 constexpr int kOutCols = 256;        // columns of an output block: 8 per lane
 constexpr int kOutBatch = 12;        // kept rows whose loads a warp issues together
-constexpr int kOutRows = 48;         // kept rows of an output item at most
 
 struct OutPlan {
   int ncb;   // output blocks
@@ -1896,23 +1765,6 @@ struct OutPlan {
   int RC;    // kept rows per chunk
   int NR;    // chunks per (token, block): R, plus the recovery chunks of U c when k < N
 };
-
-// Enough (token, block, chunk) warp items to occupy every warp once.
-__device__ __forceinline__ OutPlan out_plan(const Params& P, int nwarps) {
-  OutPlan op;
-  op.ncb = (P.d.H + kOutCols - 1) / kOutCols;
-  const int per = P.B * op.ncb;
-  // the recovery U c comes in chunks of kOutBatch rank components
-  const int rec = P.k < P.d.N ? (P.d.r + kOutBatch - 1) / kOutBatch : 0;
-  int R = nwarps / per - rec;                 // one round of warp items,
-  R = min(R, (P.k + kOutBatch - 1) / kOutBatch);   // each at least one full load batch,
-  R = max(R, (P.k + kOutRows - 1) / kOutRows);     // at most kOutRows rows (large batches)
-  R = max(1, min(R, P.k));
-  op.RC = (P.k + R - 1) / R;
-  op.R = op.RC > 0 ? (P.k + op.RC - 1) / op.RC : 1;
-  op.NR = op.R + rec;
-  return op;
-}
 
 __device__ __forceinline__ void axpy8h(float c, const uint4& v, float* acc) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -1924,51 +1776,66 @@ __device__ __forceinline__ void axpy8h(float c, const uint4& v, float* acc) {
   }
 }
 
+// The CTA's output of token t's kept rows [q0, q1) of its kept list (their w a
+// in wa_s / row_s at [s0, s0 + q1 - q0), or in global wa): 256-column chunks,
+// 8 columns a lane, each chunk's rows split between kWarps / chunks warps; a
+// warp loads its rows' 16-byte down pieces kO at a time, sums them in
+// registers and adds its 8 columns into y once.
+__device__ void cta_output(const Params& P, int t, int q0, int q1, const float* wa_s,
+                           const int* row_s, int s0, const TokenSlots& sl, int warp, int lane) {
+  const Dims& d = P.d;
+  const int nchunk = (d.H + kOutCols - 1) / kOutCols;
+  const int rsplit = max(1, kWarps / nchunk);          // warps per chunk
+  const int nr = q1 - q0, per = (nr + rsplit - 1) / rsplit;
+  const uint64_t pol = policy_evict_first();            // the last read of these rows
+  constexpr int kO = 12;
+  for (int wi = warp; wi < nchunk * rsplit; wi += kWarps) {
+    const int ch = wi % nchunk, part = wi / nchunk;
+    const int r_lo = q0 + part * per, r_hi = min(q1, r_lo + per);
+    if (r_lo >= r_hi) continue;
+    const int c0 = ch * kOutCols + 8 * lane;
+    const bool on = c0 < d.H;                          // H is a multiple of 8
+    float acc[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    for (int r0 = r_lo; r0 < r_hi; r0 += kO) {
+      uint4 v[kO];
+      float c[kO];
+#pragma unroll
+      for (int u = 0; u < kO; ++u) {
+        const int r = r0 + u;
+        int row = 0;
+        c[u] = 0.f;
+        if (r < r_hi) {
+          if (wa_s) {
+            row = row_s[s0 + r - q0];
+            c[u] = wa_s[s0 + r - q0];
+          } else {
+            const int n = __ldcg(P.kept + (size_t)t * d.N + r);
+            const int slot = n / d.I;
+            row = slot_expert(sl.e0, sl.e1, slot) * d.I + (n - slot * d.I);
+            c[u] = __ldcg(P.wa + (size_t)t * d.N + r);
+          }
+        }
+        v[u] = r < r_hi && on ? ldg_nc4_hint(P.Dt + (size_t)row * d.H + c0, pol)
+                              : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kO; ++u) axpy8(c[u], v[u], acc);
+    }
+    if (on) {
+      float4* yo = reinterpret_cast<float4*>(P.y + (size_t)t * d.H + c0);
+      atomicAdd(yo, make_float4(acc[0], acc[1], acc[2], acc[3]));
+      atomicAdd(yo + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+  }
+}
+
 // One warp item: columns cb*256 + 8 lane .. +7 of token t over kept rows
 // [rc RC, (rc+1) RC) of Dt, each row read as one coalesced 512-byte piece, or
 // for rc = R the recovery U c as the r rows of U^T weighted by c.  The
 // partial is added into y with fp32 atomics.
 // The token's sanitised expert ids and weights, lane-distributed (topk <= 64).
-// ------------------------------ stack hand-off ------------------------------
-// The warp that completes output block cb of token t: hnext = hres + y on the
-// block's 256 columns (fp32), and, when a next layer reads it, the block's sum
-// of squares (fp64) into the token's sum.  The token's last block sets the
-// next layer's input scale 1 / sqrt(sum / H + 1e-6) and releases the token.
-__device__ void carry_block(const Params& P, int t, int cb, int ncb, int lane) {
-  const Dims& d = P.d;
-  const SyncOff so = sync_offsets(d);
-  const size_t row = (size_t)t * d.H;
-  const int c0 = cb * kOutCols + lane * 8;
-  double ss = 0.0;
-  if (c0 < d.H) {
-    const float4* h4 = reinterpret_cast<const float4*>(P.hres + row + c0);
-    const float4* y4 = reinterpret_cast<const float4*>(P.y + row + c0);
-    const float4 a0 = __ldcg(h4), a1 = __ldcg(h4 + 1), b0 = __ldcg(y4), b1 = __ldcg(y4 + 1);
-    const float4 v0 = make_float4(a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w);
-    const float4 v1 = make_float4(a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w);
-    float4* o4 = reinterpret_cast<float4*>(P.hnext + row + c0);
-    o4[0] = v0;
-    o4[1] = v1;
-    ss = (double)v0.x * v0.x + (double)v0.y * v0.y + (double)v0.z * v0.z + (double)v0.w * v0.w +
-         (double)v1.x * v1.x + (double)v1.y * v1.y + (double)v1.z * v1.z + (double)v1.w * v1.w;
-  }
-  if (!P.xscale_next) return;   // the last layer: h_out only
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  double* sum = reinterpret_cast<double*>(P.sync + so.ssum) + t;
-  __syncwarp();
-  uint32_t prev = 0;
-  if (lane == 0) {
-    atomicAdd(sum, ss);
-    prev = atom_add_acq_rel(P.sync + so.tokdone + t, 1u);
-    if (prev == (uint32_t)(ncb - 1)) {
-      const double tot = __ldcg(sum);
-      P.xscale_next[t] = (float)(1.0 / sqrt(tot / d.H + 1e-6));
-      st_release(P.xnext_ready + t, 1u);
-    }
-  }
-}
-
 // Wait state of a warp's output items: the token whose top-k it has seen
 // (rows known) and the token whose phase-2 items it has seen counted (kept
 // weights and the recovery vector known).
@@ -2190,9 +2057,41 @@ __device__ bool shared_out_chunk(const Params& P, int c, int cb, int RCs, int K,
   return true;
 }
 
+// Recovery output chunk rc of token t on column block cb (the per-token
+// kernel): y += rank components rc*kOutBatch .. of U c, the U^T rows weighted
+// by c, once the token's recovery chunks are counted; the U^T rows load first.
+__device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane) {
+  const Dims& d = P.d;
+  const int c0 = cb * kOutCols + lane * 8;
+  const bool on = c0 < d.H;                  // H is a multiple of 8
+  const int j0 = rc * kOutBatch, nj = min(kOutBatch, d.r - j0);
+  uint4 v[kOutBatch];
+#pragma unroll
+  for (int u = 0; u < kOutBatch; ++u)
+    v[u] = u < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(j0 + u) * d.H + c0))
+                        : make_uint4(0u, 0u, 0u, 0u);
+  if (!out_wait(P, P.sync + sync_offsets(d).exact + t, (uint32_t)(d.N / 64), lane)) return false;
+  if (lane == 0) TRACE_POINT(15);
+  const float cj_l = lane < nj ? __ldcg(P.cvec + (size_t)t * d.r + j0 + lane) : 0.f;
+  float acc[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+#pragma unroll
+  for (int u = 0; u < kOutBatch; ++u) {
+    const float cw = __shfl_sync(0xffffffffu, cj_l, u);
+    axpy8h(u < nj ? cw : 0.f, v[u], acc);
+  }
+  if (on) {
+    float4* yo = reinterpret_cast<float4*>(P.y + (size_t)t * d.H + c0);
+    atomicAdd(yo, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    atomicAdd(yo + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+  }
+  return true;
+}
+
 // ------------------------------- the kernel --------------------------------
 // One layer's decode by every CTA of the grid.  false: the launch is aborting.
-template <bool SH, int WPT, bool SPLIT>
+template <bool SH, int WPT>
 __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* smem, int* ctl) {
   if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
@@ -2204,7 +2103,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   if (threadIdx.x == 0) TRACE_POINT(0);
 
   // phase 1a: screen units (rotation, selection and sketch sums), computed by teams of warps
-  screen_compute<WPT, SPLIT>(P, smem, warp);
+  screen_compute<WPT>(P, smem, warp);
   __syncthreads();
   if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(5);
@@ -2288,21 +2187,34 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       if (lane == 0) red_add_release(P.sync + kSyncSdone, (uint32_t)nk);
     }
   } else {
-  const long long M = (long long)P.B * per_tok;
-  {
+    // kept channels and recovery chunks in contiguous runs of items per warp;
+    // a warp meets one or two tokens and counts its recovery chunks of a token
+    // when it leaves the token.  Each CTA then adds the output of the kept
+    // rows of its range (register sums over the rows, one vector add per lane
+    // and column chunk): no hand-off between CTAs on the way to y.
+    const long long M = (long long)P.B * per_tok;
     const long long wtot = (long long)nctas * kWarps;
-    const long long gw = (long long)blockIdx.x * kWarps + warp;
-    // contiguous runs of items per warp: a warp meets one or two tokens, and
-    // counts its items of a token once it leaves that token
     const long long ipw = (M + wtot - 1) / wtot;
+    const long long cq0 = min(M, (long long)blockIdx.x * kWarps * ipw);
+    const long long cq1 = min(M, cq0 + (long long)kWarps * ipw);
+    const int nitems = (int)(cq1 - cq0);
+    // the CTA's lists of w a and rows when they fit (else global wa), then a
+    // flag per token of the range
+    const bool use_s = (size_t)nitems * 12 <= (size_t)P.smem_bytes;
+    float* wa_s = use_s ? reinterpret_cast<float*>(smem) : nullptr;
+    int* row_s = use_s ? reinterpret_cast<int*>(smem) + nitems : nullptr;
+    int* done_s = reinterpret_cast<int*>(smem) + (use_s ? 2 * nitems : 0);
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
     const long long q0 = gw * ipw, q1 = min(M, q0 + ipw);
-    int cur_t = -1, pend_t = -1, pend_n = 0;
+    int cur_t = -1, rec_t = -1, rec_n = 0;
     int kbase = 0, kn_l = 0;   // lane j: kept index at list position kbase + j
     TokenSlots sl{};
     bool ok = true;
     for (long long q = q0; q < q1; ++q) {
       const int t = (int)(q / per_tok), local = (int)(q % per_tok);
       if (t != cur_t) {
+        if (rec_n) publish_item(P, rec_t, rec_n, lane);
+        rec_n = 0;
         int w_ok = 1;
         if (lane == 0) w_ok = wait_at_least(P, P.sync + so.flag + t, 1u);
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -2316,33 +2228,77 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
         if (lane == 0 && warp == 0) TRACE_POINT(13);
         kbase = -64;
       }
-      const bool flush = pend_t >= 0 && pend_t != t;   // leaving token pend_t
       if (local < P.k) {
         if (local - kbase >= 32) {   // the next 32 kept indices in one read
           kbase = local;
           kn_l = kbase + lane < P.k ? __ldcg(P.kept + (size_t)t * d.N + kbase + lane) : 0;
         }
         const int n = __shfl_sync(0xffffffffu, kn_l, local - kbase);
-        kept_item(P, t, local, n, sl, lane, flush ? pend_t : -1, pend_n);
-      } else
-        recovery_item(P, t, local - P.k, lane, flush ? pend_t : -1, pend_n);
-      if (flush) pend_n = 0;
-      pend_t = t;
-      ++pend_n;
+        kept_item_cta(P, t, use_s ? (int)(q - cq0) : local, n, sl, lane, wa_s, row_s);
+      } else {
+        recovery_item(P, t, local - P.k, lane, -1, 0);
+        rec_t = t;
+        ++rec_n;
+      }
     }
-    if (ok) publish_item(P, pend_t, pend_n, lane);
-  }
-  }
-  if (lane == 0) TRACE_POINT(14);
-  if (stamp) {
+    if (ok && rec_n) publish_item(P, rec_t, rec_n, lane);
+    if (lane == 0) TRACE_POINT(14);
+    if (threadIdx.x == 0) ctl[1] = 0;
     __syncthreads();
-    if (threadIdx.x == 0) stamp[3] = globaltimer();
+    if (!ok && lane == 0) ctl[1] = 1;   // this warp left its items: the launch is aborting
+    __syncthreads();   // the CTA's kept channels are in
+    if (stamp && threadIdx.x == 0) stamp[3] = globaltimer();
+    if (ctl[1]) return false;   // a list entry may be missing: read no row
+    const int ncb = (d.H + kOutCols - 1) / kOutCols;
+    const int rec = P.k < d.N ? (d.r + kOutBatch - 1) / kOutBatch : 0;
+    const uint32_t total = (uint32_t)(P.k + ncb * rec);   // output contributions per token
+    // the output of the kept rows of each token of the range
+    if (cq0 < cq1) {
+      const int tf = (int)(cq0 / per_tok), tl = (int)((cq1 - 1) / per_tok);
+      for (int t = tf; t <= tl; ++t) {
+        const long long a = max(cq0, (long long)t * per_tok);
+        const long long b = min(cq1, (long long)t * per_tok + P.k);
+        if (a >= b) continue;
+        const TokenSlots tsl = use_s ? TokenSlots{} : load_token_slots(P, t, lane);
+        cta_output(P, t, (int)(a - (long long)t * per_tok), (int)(b - (long long)t * per_tok), wa_s,
+                   row_s, (int)(a - cq0), tsl, warp, lane);
+      }
+      if (P.hnext) {   // a stacked layer: count the rows; each completed token's residual is carried
+        __syncthreads();   // every output add of the CTA precedes the counts
+        if (threadIdx.x == 0)
+          for (int t = tf; t <= tl; ++t) {
+            const long long a = max(cq0, (long long)t * per_tok);
+            const long long b = min(cq1, (long long)t * per_tok + P.k);
+            done_s[t - tf] = a < b && count_output(P, t, (uint32_t)(b - a), total);
+          }
+        __syncthreads();
+        for (int r = warp; r <= tl - tf; r += kWarps)
+          if (done_s[r]) carry_token(P, tf + r, lane);
+      }
+    }
+    // recovery output chunks, dealt from the last warp down so that warps
+    // without kept channels take them first
+    const int nwarps = nctas * kWarps;
+    const int items = P.B * ncb * rec;
+    for (int it = nwarps - 1 - (int)gw; it < items; it += nwarps) {
+      const int t = it / (ncb * rec);
+      if (!uc_item(P, t, (it / rec) % ncb, it % rec, lane)) break;
+      if (P.hnext) {   // a stacked layer: the token's last contribution carries the residual
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = count_output(P, t, 1u, total);
+        if (__shfl_sync(0xffffffffu, last, 0)) carry_token(P, t, lane);
+      }
+    }
   }
-  // phase 3: output warp items (token, 256-column block, row chunk), dealt
-  // from the last warp down so that warps without phase-2 work take them
-  // first; an item loads its rows once the token's top-k is in and weighs
-  // them once the token's phase-2 items are counted
   if (SH) {
+    if (lane == 0) TRACE_POINT(14);
+    if (stamp) {
+      __syncthreads();
+      if (threadIdx.x == 0) stamp[3] = globaltimer();
+    }
+    // phase 3: output warp items, dealt from the last warp down so that warps
+    // without phase-2 work take them first
     // the batch's kept rows in chunks of RCs rows per column block, then each
     // token's recovery chunks
     const int nwarps = nctas * kWarps;
@@ -2365,24 +2321,6 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       } else {
         const int r = it - C * ncb, t = r / (ncb * rec);
         if (!out_chunk<SH>(P, op, t, (r / rec) % ncb, r % rec, lane, per_tok, ow)) break;
-      }
-    }
-  } else {
-    const int nwarps = nctas * kWarps;
-    const OutPlan op = out_plan(P, nwarps);
-    const int items = P.B * op.ncb * op.NR;
-    const int gw = blockIdx.x * kWarps + warp;
-    OutWait ow;
-    for (int it = nwarps - 1 - gw; it < items; it += nwarps) {
-      const int t = it / (op.ncb * op.NR);
-      if (!out_chunk<SH>(P, op, t, (it / op.NR) % op.ncb, it % op.NR, lane, per_tok, ow)) break;
-      if (P.hnext) {   // a layer of a stack: the block's last item carries the residual
-        const int cb = (it / op.NR) % op.ncb;
-        __syncwarp();
-        uint32_t prev = 0;
-        if (lane == 0) prev = atom_add_acq_rel(P.sync + so.cbdone + t * op.ncb + cb, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == (uint32_t)(op.NR - 1)) carry_block(P, t, cb, op.ncb, lane);
       }
     }
   }
@@ -2433,20 +2371,20 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
 }
 
 // The batch-shared selection variant: one kept set for the whole batch.
-// Kernels are specialised on the screen's code words per thread (WPT) and on
-// the small-batch split screen, so that each holds only the code it runs.
+// Kernels are specialised on the screen's code words per thread (WPT), so
+// that each holds only the code it runs.
 template <int WPT>
 __global__ void __launch_bounds__(kThreads, 1) decode_shared_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  decode_layer<true, WPT, false>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<true, WPT>(P, aligned_smem(smem_raw), ctl);
 }
 
-template <int WPT, bool SPLIT>
+template <int WPT>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  decode_layer<false, WPT, SPLIT>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<false, WPT>(P, aligned_smem(smem_raw), ctl);
   if (threadIdx.x == 0) TRACE_POINT(17);
   if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
     // the next layer would wait for inputs that never come
@@ -2457,12 +2395,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
 
 using KernelFn = void (*)(const Params);
 
-// The kernel for a decode: shared selection or not, the shape's code words per
-// thread, and the split screen when the batch is small enough for it.
-KernelFn pick_kernel(bool shared, int wpt, bool split) {
+// The kernel for a decode: shared selection or not, the shape's code words per thread.
+KernelFn pick_kernel(bool shared, int wpt) {
   if (shared) return wpt == 1 ? decode_shared_kernel<1> : wpt == 2 ? decode_shared_kernel<2> : decode_shared_kernel<3>;
-  if (split) return wpt == 1 ? decode_kernel<1, true> : wpt == 2 ? decode_kernel<2, true> : decode_kernel<3, true>;
-  return wpt == 1 ? decode_kernel<1, false> : wpt == 2 ? decode_kernel<2, false> : decode_kernel<3, false>;
+  return wpt == 1 ? decode_kernel<1> : wpt == 2 ? decode_kernel<2> : decode_kernel<3>;
 }
 
 size_t decode_smem_bytes(const Dims& d) {
@@ -2501,8 +2437,8 @@ cudaError_t configure_decode_kernels(const Dims& d) {
   const ScreenPlan sp = screen_plan(d);
   if (sp.bytes == 0) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes(d);
-  for (int v = 0; v < 3; ++v) {   // the shape's kernels: per-token, split, shared
-    const KernelFn fn = pick_kernel(v == 2, sp.wpt, v == 1);
+  for (int v = 0; v < 2; ++v) {   // the shape's kernels: per-token and shared
+    const KernelFn fn = pick_kernel(v == 1, sp.wpt);
     cudaFuncAttributes fa;
     cudaError_t err = cudaFuncGetAttributes(&fa, fn);
     if (err != cudaSuccess) return err;
@@ -2518,7 +2454,7 @@ int decode_grid(const Dims& d) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pick_kernel(false, screen_plan(d).wpt, false),
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pick_kernel(false, screen_plan(d).wpt),
                                                     kThreads, decode_smem_bytes(d)) != cudaSuccess)
     return 0;
   return per_sm >= 1 ? sms : 0;   // one CTA per SM, all co-resident
@@ -2624,8 +2560,7 @@ static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStrea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const bool split = !shared && screen_split_factor(h.d, P.sp, P.B, h.grid) > 1;
-  return cudaLaunchKernelEx(&cfg, pick_kernel(shared, P.sp.wpt, split), P);
+  return cudaLaunchKernelEx(&cfg, pick_kernel(shared, P.sp.wpt), P);
 }
 
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
