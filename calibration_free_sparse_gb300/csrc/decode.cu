@@ -451,6 +451,56 @@ __host__ __device__ inline size_t topk_smem_bytes(int N) {
          + 512;                              // scalars, warp sums, expert ids
 }
 
+// Sum of wsum[0 .. wid) for the calling thread's warp, by a shuffle scan of
+// the kWarps per-warp values (read after the barrier that follows their
+// writes); *total (may be null) receives the sum of all of them.
+__device__ __forceinline__ int warps_before(const int* wsum, int wid, int lane, int* total) {
+  const int v = lane < kWarps ? wsum[lane] : 0;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (total) *total = __shfl_sync(0xffffffffu, incl, 31);
+  return __shfl_sync(0xffffffffu, incl - v, wid);
+}
+
+// The top-k's fallback when more than kCandMax keys share the threshold digit:
+// a full radix select on the keys, ties by the lower global id.  Sets keep[].
+__device__ __noinline__ void topk_radix_fallback(const uint32_t* keys, uint8_t* keep, const int* eid,
+                                                 int N, int k, int I, int* hist, int* sh,
+                                                 int* wsum) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int need2 = 0;
+  const uint32_t T = cta_radix_select(
+      N, k, [&](int n, uint32_t& key) { key = keys[n]; return true; }, hist, sh + 4, &need2);
+  int eq = 0;
+  for (int n = threadIdx.x; n < N; n += kThreads) eq += keys[n] == T;
+  eq = warp_sum_i(eq);
+  if (lane == 0) wsum[wid] = eq;
+  __syncthreads();
+  int eq_total = 0;
+  for (int w = 0; w < kWarps; ++w) eq_total += wsum[w];
+  __syncthreads();
+  uint32_t T2 = 0;
+  if (need2 < eq_total) {
+    int dummy = 0;
+    T2 = cta_radix_select(
+        N, need2,
+        [&](int n, uint32_t& key) {
+          if (keys[n] != T) return false;
+          key = 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I);
+          return true;
+        },
+        hist, sh + 4, &dummy);
+  }
+  for (int n = threadIdx.x; n < N; n += kThreads) {
+    const uint32_t a = keys[n];
+    keep[n] = a > T || (a == T && 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I) >= T2);
+  }
+}
+
 __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   const Dims& d = P.d;
   const int N = d.N, k = P.k, I = d.I;
@@ -466,8 +516,18 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int s = threadIdx.x; s < d.topk; s += kThreads) eid[s] = __ldcg(P.ids_ws + t * d.topk + s);
   if (threadIdx.x == 0) TRACE_POINT(8);
-  for (int n = threadIdx.x; n < N; n += kThreads)
-    keys[n] = __float_as_uint(__ldcg(P.score + (size_t)t * N + n));
+  {   // the token's N scores (N is a multiple of 64: whole float4 groups)
+    const float4* s4 = reinterpret_cast<const float4*>(P.score + (size_t)t * N);
+    uint4* k4 = reinterpret_cast<uint4*>(keys);
+    for (int q = threadIdx.x; q < N / 4; q += kThreads) {
+      const float4 v = __ldcg(s4 + q);
+      k4[q] = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                         __float_as_uint(v.w));
+    }
+  }
+  // the output adds into y[t]: start it from zero while the scores come in
+  for (int h = 4 * threadIdx.x; h < d.H; h += 4 * kThreads)
+    *reinterpret_cast<float4*>(P.y + (size_t)t * d.H + h) = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
   if (threadIdx.x == 0) sh[2] = 0;
   __syncthreads();
@@ -497,8 +557,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     }
     if (lane == 31) wsum[wid] = incl;
     __syncthreads();
-    int before = incl - tot;
-    for (int w = 0; w < wid; ++w) before += wsum[w];
+    const int before = incl - tot + warps_before(wsum, wid, lane, nullptr);
     if (before < k && before + tot >= k) {
       int above = before;
 #pragma unroll
@@ -542,33 +601,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
       }
     } else {
       // degenerate spread (too many keys in one digit): full radix select
-      int need2 = 0;
-      const uint32_t T = cta_radix_select(
-          N, k, [&](int n, uint32_t& key) { key = keys[n]; return true; }, hist, sh + 4, &need2);
-      int eq = 0;
-      for (int n = threadIdx.x; n < N; n += kThreads) eq += keys[n] == T;
-      eq = warp_sum_i(eq);
-      if (lane == 0) wsum[wid] = eq;
-      __syncthreads();
-      int eq_total = 0;
-      for (int w = 0; w < kWarps; ++w) eq_total += wsum[w];
-      __syncthreads();
-      uint32_t T2 = 0;
-      if (need2 < eq_total) {
-        int dummy = 0;
-        T2 = cta_radix_select(
-            N, need2,
-            [&](int n, uint32_t& key) {
-              if (keys[n] != T) return false;
-              key = 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I);
-              return true;
-            },
-            hist, sh + 4, &dummy);
-      }
-      for (int n = threadIdx.x; n < N; n += kThreads) {
-        const uint32_t a = keys[n];
-        keep[n] = a > T || (a == T && 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I) >= T2);
-      }
+      topk_radix_fallback(keys, keep, eid, N, k, I, hist, sh, wsum);
     }
   }
   __syncthreads();
@@ -582,8 +615,7 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   for (int wd = w0; wd < w1; ++wd) mine += __popc(__ballot_sync(0xffffffffu, keep[wd * 32 + lane]));
   if (lane == 0) wsum[wid] = mine;
   __syncthreads();
-  int pos = 0;
-  for (int w = 0; w < wid; ++w) pos += wsum[w];
+  int pos = warps_before(wsum, wid, lane, nullptr);
   const uint32_t below = (1u << lane) - 1u;
   for (int wd = w0; wd < w1; ++wd) {
     const int n = wd * 32 + lane;
@@ -596,8 +628,6 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     pos += __popc(bal);
   }
   if (threadIdx.x == 0) TRACE_POINT(24);
-  // the output phase adds its chunks into y[t]: start it from zero
-  for (int h = threadIdx.x; h < d.H; h += kThreads) P.y[(size_t)t * d.H + h] = 0.f;
   __syncthreads();
   if (threadIdx.x == 0) {
     st_release(&P.sync[sync_offsets(d).flag + t], 1u);
@@ -1396,22 +1426,28 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int t = ts / d.topk, slot = ts % d.topk, I = d.I;
+  // the routing and the first channels' down norms are inputs: requested
+  // before the wait for the slot's screen units
+  int e = P.ids_in[ts];
+  if (e < 0 || e >= d.E) e = 0;
+  const float wv = P.w_in[ts];
+  float dn0[2] = {0.f, 0.f};
+  if (threadIdx.x < I) dn0[0] = __ldg(P.dnorm + (size_t)e * I + threadIdx.x);
+  if (threadIdx.x + kThreads < I) dn0[1] = __ldg(P.dnorm + (size_t)e * I + threadIdx.x + kThreads);
   if (threadIdx.x == 0)
     *flag = wait_at_least(P, P.sync + so.slot + ts, (uint32_t)(d.nb * P.sp.tw + P.stall));
   __syncthreads();
   if (!*flag) return -1;
-  int e = P.ids_in[ts];
   if (threadIdx.x == 0) TRACE_POINT(6);
-  if (e < 0 || e >= d.E) e = 0;
-  const float wv = P.w_in[ts];
   const float* pg0 = P.partial + ((size_t)ts * d.nb) * 2 * I;
   // channels i and i + kThreads together: all their block loads first, then
   // the sums in block order
   for (int i = threadIdx.x; i < I; i += 2 * kThreads) {
     const int i2 = i + kThreads;
     const bool two = i2 < I;
-    const float dn[2] = {__ldg(P.dnorm + (size_t)e * I + i),
-                         two ? __ldg(P.dnorm + (size_t)e * I + i2) : 0.f};
+    const bool first = i < kThreads;
+    const float dn[2] = {first ? dn0[0] : __ldg(P.dnorm + (size_t)e * I + i),
+                         two ? (first ? dn0[1] : __ldg(P.dnorm + (size_t)e * I + i2)) : 0.f};
     float g[2] = {0.f, 0.f}, v[2] = {0.f, 0.f};
     int bb = 0;
     for (; bb + 16 <= d.nb; bb += 16) {
