@@ -1692,37 +1692,20 @@ __device__ void recovery_item(const Params& P, int t, int ch, int lane, int pend
   }
 }
 
-// The warp that completes token t's output in a stacked layer: hnext = hres +
-// y over all H columns (fp32), the fp64 sum of squares, and, when a next layer
-// reads it, that layer's input scale 1 / sqrt(sum / H + 1e-6) and its release.
-__device__ void carry_token(const Params& P, int t, int lane) {
-  const Dims& d = P.d;
-  const size_t row = (size_t)t * d.H;
-  double ss = 0.0;
-  for (int c0 = 4 * lane; c0 < d.H; c0 += 128) {   // H is a multiple of 8
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(P.hres + row + c0));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(P.y + row + c0));
-    const float4 v = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-    *reinterpret_cast<float4*>(P.hnext + row + c0) = v;
-    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
-  }
-  if (!P.xscale_next) return;   // the last layer: h_out only
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  __syncwarp();   // every lane's hnext stores precede the release
-  if (lane == 0) {
-    P.xscale_next[t] = (float)(1.0 / sqrt(ss / d.H + 1e-6));
-    st_release(P.xnext_ready + t, 1u);
-  }
+// Count one output contribution to column block cb of token t in a stacked
+// layer (a CTA's rows, or one recovery chunk of the block); true for the
+// contribution that completes the block (`total` of them), whose warp then
+// carries it.
+__device__ __forceinline__ bool count_block(const Params& P, int t, int cb, int ncb, uint32_t total) {
+  return atom_add_acq_rel(P.sync + sync_offsets(P.d).cbdone + t * ncb + cb, 1u) + 1u == total;
 }
 
-// Count `n` output contributions of token t (kept channels added into y, or
-// one recovery output chunk) in a stacked layer; the contribution that
-// completes the token (k kept channels plus the recovery chunks) carries the
-// residual.  Returns true when the caller's warp must run carry_token.
-__device__ __forceinline__ bool count_output(const Params& P, int t, uint32_t n, uint32_t total) {
-  const uint32_t prev = atom_add_acq_rel(P.sync + sync_offsets(P.d).tokdone + t, n);
-  return prev + n == total;
+// CTAs whose item ranges hold kept channels of token t (items are dealt in
+// runs of ipw per warp, kWarps runs per CTA, token-major, kept items first).
+__device__ __forceinline__ int kept_ctas(long long t, long long per_tok, int k, long long ipw) {
+  if (k <= 0) return 0;
+  const long long span = (long long)kWarps * ipw;
+  return (int)((t * per_tok + k - 1) / span - (t * per_tok) / span + 1);
 }
 
 // ---------------- exact channels and their output, per CTA (per-token) ----------------
@@ -1863,6 +1846,46 @@ __device__ void cta_output(const Params& P, int t, int q0, int q1, const float* 
       float4* yo = reinterpret_cast<float4*>(P.y + (size_t)t * d.H + c0);
       atomicAdd(yo, make_float4(acc[0], acc[1], acc[2], acc[3]));
       atomicAdd(yo + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+  }
+}
+
+// ------------------------------ stack hand-off ------------------------------
+// The warp that completes output block cb of token t: hnext = hres + y on the
+// block's 256 columns (fp32), and, when a next layer reads it, the block's sum
+// of squares (fp64) into the token's sum.  The token's last block sets the
+// next layer's input scale 1 / sqrt(sum / H + 1e-6) and releases the token.
+__device__ void carry_block(const Params& P, int t, int cb, int ncb, int lane) {
+  const Dims& d = P.d;
+  const SyncOff so = sync_offsets(d);
+  const size_t row = (size_t)t * d.H;
+  const int c0 = cb * kOutCols + lane * 8;
+  double ss = 0.0;
+  if (c0 < d.H) {
+    const float4* h4 = reinterpret_cast<const float4*>(P.hres + row + c0);
+    const float4* y4 = reinterpret_cast<const float4*>(P.y + row + c0);
+    const float4 a0 = __ldcg(h4), a1 = __ldcg(h4 + 1), b0 = __ldcg(y4), b1 = __ldcg(y4 + 1);
+    const float4 v0 = make_float4(a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w);
+    const float4 v1 = make_float4(a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w);
+    float4* o4 = reinterpret_cast<float4*>(P.hnext + row + c0);
+    o4[0] = v0;
+    o4[1] = v1;
+    ss = (double)v0.x * v0.x + (double)v0.y * v0.y + (double)v0.z * v0.z + (double)v0.w * v0.w +
+         (double)v1.x * v1.x + (double)v1.y * v1.y + (double)v1.z * v1.z + (double)v1.w * v1.w;
+  }
+  if (!P.xscale_next) return;   // the last layer: h_out only
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  double* sum = reinterpret_cast<double*>(P.sync + so.ssum) + t;
+  __syncwarp();
+  uint32_t prev = 0;
+  if (lane == 0) {
+    atomicAdd(sum, ss);
+    prev = atom_add_acq_rel(P.sync + so.tokdone + t, 1u);
+    if (prev == (uint32_t)(ncb - 1)) {
+      const double tot = __ldcg(sum);
+      P.xscale_next[t] = (float)(1.0 / sqrt(tot / d.H + 1e-6));
+      st_release(P.xnext_ready + t, 1u);
     }
   }
 }
@@ -2235,8 +2258,9 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     const long long cq1 = min(M, cq0 + (long long)kWarps * ipw);
     const int nitems = (int)(cq1 - cq0);
     // the CTA's lists of w a and rows when they fit (else global wa), then a
-    // flag per token of the range
-    const bool use_s = (size_t)nitems * 12 <= (size_t)P.smem_bytes;
+    // flag per (token, column block) of the range
+    const int ncb_s = (d.H + kOutCols - 1) / kOutCols;
+    const bool use_s = (size_t)nitems * 8 + (size_t)(nitems + 1) * ncb_s * 4 <= (size_t)P.smem_bytes;
     float* wa_s = use_s ? reinterpret_cast<float*>(smem) : nullptr;
     int* row_s = use_s ? reinterpret_cast<int*>(smem) + nitems : nullptr;
     int* done_s = reinterpret_cast<int*>(smem) + (use_s ? 2 * nitems : 0);
@@ -2287,7 +2311,6 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     if (ctl[1]) return false;   // a list entry may be missing: read no row
     const int ncb = (d.H + kOutCols - 1) / kOutCols;
     const int rec = P.k < d.N ? (d.r + kOutBatch - 1) / kOutBatch : 0;
-    const uint32_t total = (uint32_t)(P.k + ncb * rec);   // output contributions per token
     // the output of the kept rows of each token of the range
     if (cq0 < cq1) {
       const int tf = (int)(cq0 / per_tok), tl = (int)((cq1 - 1) / per_tok);
@@ -2299,17 +2322,19 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
         cta_output(P, t, (int)(a - (long long)t * per_tok), (int)(b - (long long)t * per_tok), wa_s,
                    row_s, (int)(a - cq0), tsl, warp, lane);
       }
-      if (P.hnext) {   // a stacked layer: count the rows; each completed token's residual is carried
+      if (P.hnext) {   // a stacked layer: each column block the CTA completes is carried
         __syncthreads();   // every output add of the CTA precedes the counts
-        if (threadIdx.x == 0)
-          for (int t = tf; t <= tl; ++t) {
-            const long long a = max(cq0, (long long)t * per_tok);
-            const long long b = min(cq1, (long long)t * per_tok + P.k);
-            done_s[t - tf] = a < b && count_output(P, t, (uint32_t)(b - a), total);
-          }
+        const int nr = (tl - tf + 1) * ncb;
+        for (int r = threadIdx.x; r < nr; r += kThreads) {
+          const int t = tf + r / ncb, cb = r % ncb;
+          const long long a = max(cq0, (long long)t * per_tok);
+          const long long b = min(cq1, (long long)t * per_tok + P.k);
+          const uint32_t total = (uint32_t)(kept_ctas(t, per_tok, P.k, ipw) + rec);
+          done_s[r] = a < b && count_block(P, t, cb, ncb, total);
+        }
         __syncthreads();
-        for (int r = warp; r <= tl - tf; r += kWarps)
-          if (done_s[r]) carry_token(P, tf + r, lane);
+        for (int r = warp; r < nr; r += kWarps)
+          if (done_s[r]) carry_block(P, tf + r / ncb, r % ncb, ncb, lane);
       }
     }
     // recovery output chunks, dealt from the last warp down so that warps
@@ -2318,12 +2343,14 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     const int items = P.B * ncb * rec;
     for (int it = nwarps - 1 - (int)gw; it < items; it += nwarps) {
       const int t = it / (ncb * rec);
-      if (!uc_item(P, t, (it / rec) % ncb, it % rec, lane)) break;
-      if (P.hnext) {   // a stacked layer: the token's last contribution carries the residual
+      const int cb = (it / rec) % ncb;
+      if (!uc_item(P, t, cb, it % rec, lane)) break;
+      if (P.hnext) {   // a stacked layer: the block's last contribution carries it
         __syncwarp();
         int last = 0;
-        if (lane == 0) last = count_output(P, t, 1u, total);
-        if (__shfl_sync(0xffffffffu, last, 0)) carry_token(P, t, lane);
+        if (lane == 0)
+          last = count_block(P, t, cb, ncb, (uint32_t)(kept_ctas(t, per_tok, P.k, ipw) + rec));
+        if (__shfl_sync(0xffffffffu, last, 0)) carry_block(P, t, cb, ncb, lane);
       }
     }
   }
