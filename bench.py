@@ -58,6 +58,8 @@ def parse_args():
                          "batch-shared selection)")
     ap.add_argument("--no-235b", action="store_true",
                     help="skip the Qwen3-235B-A22B-shaped layer at the 12.8%% budget")
+    ap.add_argument("--no-trit5", action="store_true",
+                    help="skip the five-trits-per-byte sketch layout on Qwen3-30B-shaped layers")
     return ap.parse_args()
 
 
@@ -312,8 +314,11 @@ def layer_sweep(torch, dev, stream, args, wl, k, batches, nl, seed0, modes=("per
         del d
     torch.cuda.empty_cache()
     peak, _ = measured_peaks()
+    info = readers[0].info()
     out = {"workload": wl.name, "H": wl.H, "E": wl.E, "topk": wl.topk, "I": wl.I, "k": k,
-           "screen_coords": c, "r": wl.r, "layers": nl, "per_batch": {}}
+           "screen_coords": c, "r": wl.r, "layers": nl, "per_batch": {},
+           "resident_sketch_bytes_per_layer": info["resident_bytes"][0] + info["resident_bytes"][1],
+           "run_stride": info["run_stride"]}
     for B in batches:
         xs, idw = [], []
         for l in range(nl):
@@ -629,6 +634,21 @@ def run_ours(args, wl, world, rank, local):
         large = layer_sweep(torch, dev, stream, args, wl3, wl3.k, (1, 4, 8, 16, 32, 64, 128), 6,
                             300 + 7919 * rank, modes=("per_token", "shared"))
         large["budget"] = 0.178
+    trit5 = None
+    if not args.no_trit5:
+        from calibration_free_sparse_gb300.reader import FLAG_TRIT5
+
+        trit5 = layer_sweep(torch, dev, stream, args, wl, wl.k, batches, 12, 900 + 7919 * rank,
+                            flags=FLAG_TRIT5)
+        trit5["budget"] = 0.178
+        two = readers[0].info()
+        trit5["two_bit_resident_sketch_bytes_per_layer"] = two["resident_bytes"][0] + two["resident_bytes"][1]
+        for B in batches:
+            row = trit5["per_batch"][str(B)]
+            row["vs_two_bit_headline"] = per_batch[str(B)]["us_per_decode"] / row["us_per_decode"]
+            row["two_bit_read_fraction"] = per_batch[str(B)]["read_fraction"]
+        trit5["note"] = ("MOE_READER_FLAG_TRIT5 on 12 Qwen3-30B-shaped layers: the same decode with "
+                         "the sketch stored five trits per byte; vs_two_bit_headline > 1 is faster")
     if not args.no_rho_rank:
         from calibration_free_sparse_gb300.reader import FLAG_RHO_RANK
 
@@ -716,6 +736,7 @@ def run_ours(args, wl, world, rank, local):
             "stack": stack,
             "shared": shared,
             "qwen3_235b": q235,
+            "trit5": trit5,
             "large_batch": large,
             "rho_rank": rho,
             "cpu_baseline": cpu,

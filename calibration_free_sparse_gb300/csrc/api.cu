@@ -22,7 +22,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 int check_config(const moe_reader_config* c) {
   if (!c) return MOE_READER_EINVAL;
-  if (c->flags != 0 && c->flags != MOE_READER_FLAG_RHO_RANK) return MOE_READER_EINVAL;
+  if (c->flags & ~(MOE_READER_FLAG_RHO_RANK | MOE_READER_FLAG_TRIT5)) return MOE_READER_EINVAL;
   if ((c->flags & MOE_READER_FLAG_RHO_RANK) && c->screen_coords != mr::kBlock)
     return MOE_READER_EINVAL;   // the expected-error ranking reads the whole sketch
   if (c->hidden < 8 || c->hidden % 8 != 0 || c->hidden > 65536) return MOE_READER_EINVAL;
@@ -50,9 +50,11 @@ Dims make_dims(const moe_reader_config& c) {
   d.nb = (d.H + mr::kBlock - 1) / mr::kBlock;
   d.Hp = d.nb * mr::kBlock;
   d.N = d.topk * d.I;
-  const int run = (d.I + 3) / 4;
-  d.S = ((run + mr::kSector - 1) / mr::kSector) * mr::kSector;
-  d.runW = d.I / 16;
+  d.trit5 = (c.flags & MOE_READER_FLAG_TRIT5) ? 1 : 0;
+  const int run2 = (d.I + 3) / 4, run5 = (d.I + 4) / 5;
+  d.S2b = ((run2 + mr::kSector - 1) / mr::kSector) * mr::kSector;
+  d.S = d.trit5 ? ((run5 + mr::kSector - 1) / mr::kSector) * mr::kSector : d.S2b;
+  d.runW = d.trit5 ? (run5 + 3) / 4 : d.I / 16;
   d.rho_rank = (c.flags & MOE_READER_FLAG_RHO_RANK) ? 1 : 0;
   return d;
 }
@@ -335,9 +337,24 @@ int moe_reader_prepare(const moe_reader_config* cfg, const void* gate, const voi
     if ((ce = cudaMemcpyAsync(h->p.sigma, sigma, (size_t)d.Hp, cudaMemcpyHostToDevice, s)) !=
         cudaSuccess)
       break;
-    if ((ce = mr::launch_sketch(d, h->G, h->V, h->p.sigma, h->p.codes, h->p.scales, h->p.rho, s)) !=
-        cudaSuccess)
-      break;
+    if (!d.trit5) {
+      if ((ce = mr::launch_sketch(d, h->G, h->V, h->p.sigma, h->p.codes, h->p.scales, h->p.rho,
+                                  s)) != cudaSuccess)
+        break;
+    } else {
+      // 2-bit runs into a scratch array, then five trits per byte into the codes
+      mr::Dims d2 = d;
+      d2.S = d.S2b;
+      void* c2 = nullptr;
+      if ((ce = mr::device_alloc(&c2, (size_t)d.E * d.nb * mr::kBlock * 2 * d.S2b)) != cudaSuccess)
+        break;
+      ce = mr::launch_sketch(d2, h->G, h->V, h->p.sigma, static_cast<uint8_t*>(c2), h->p.scales,
+                             h->p.rho, s);
+      if (ce == cudaSuccess) ce = mr::launch_pack_trit5(d, static_cast<uint8_t*>(c2), h->p.codes, s);
+      if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+      cudaFree(c2);
+      if (ce != cudaSuccess) break;
+    }
     if ((ce = mr::launch_transpose_down(d, static_cast<const __nv_bfloat16*>(down), h->p.Dt, s)) !=
         cudaSuccess)
       break;
@@ -567,7 +584,8 @@ int moe_reader_get_stats(moe_reader_t* h, moe_reader_stats* out) {
   auto up = [](unsigned long long bytes) { return (bytes + 31) / 32; };
   const unsigned long long runs = c[0], kept = c[1], skipped = c[2], experts = c[3], bsec = c[4];
   const int B = h->last_B;
-  out->sectors[MOE_READER_ARR_CODES] = runs * 2 * up((unsigned long long)(d.I + 3) / 4);
+  out->sectors[MOE_READER_ARR_CODES] =
+      runs * 2 * up((unsigned long long)(d.trit5 ? (d.I + 4) / 5 : (d.I + 3) / 4));
   out->sectors[MOE_READER_ARR_SCALES] = experts * d.nb * up(2ULL * d.I * 2);
   out->sectors[MOE_READER_ARR_DNORM] = experts * up(4ULL * d.I);
   out->sectors[MOE_READER_ARR_G] = kept * up(2ULL * d.H);

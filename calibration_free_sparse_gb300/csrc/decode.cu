@@ -44,6 +44,7 @@ struct ScreenPlan {
   int nch;           // chunks per unit
   int stage_bytes;   // one chunk stage: cc + 1 records (the spare slot of an odd count)
   int team_bytes;    // 256-byte flag area, two unit buffers, two chunk stages
+  int e5_off;        // five-trit layout: the byte expansion table after the teams
   size_t bytes;      // shared memory of the screen; 0: the shape does not fit
 };
 
@@ -51,7 +52,7 @@ inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 ScreenPlan screen_plan(const Dims& d) {
   ScreenPlan sp{};
-  const int W4 = d.I / 8;                        // 4-byte words per coordinate record
+  const int W4 = 2 * d.runW;                     // 4-byte words per coordinate record
   double best = 0.0;
   for (int wpt = 1; wpt <= 3; ++wpt) {           // most useful lanes per issue slot
     const int tw = (W4 + 32 * wpt - 1) / (32 * wpt);
@@ -71,7 +72,7 @@ ScreenPlan screen_plan(const Dims& d) {
   sp.coord_off = (int)round_up(64 * (size_t)((d.c + 1) / 2), 256);
   sp.buf_bytes = (int)round_up((size_t)sp.coord_off + 128 + 4 * kBlock, 256);   // + Rx in list order
   const size_t S2 = 2 * (size_t)d.S;
-  const size_t per_team = kSmemBudget / sp.nteams / 256 * 256;
+  const size_t per_team = (kSmemBudget - (d.trit5 ? 1024 : 0)) / sp.nteams / 256 * 256;
   const size_t fixed = 256 + 2 * (size_t)sp.buf_bytes;
   for (int nch = 1; nch <= d.c && !sp.cc; ++nch) {
     int c1 = (d.c + nch - 1) / nch;
@@ -83,6 +84,8 @@ ScreenPlan screen_plan(const Dims& d) {
   sp.stage_bytes = (int)round_up((size_t)(sp.cc + 1) * S2, 256);
   sp.team_bytes = (int)(fixed + 2 * (size_t)sp.stage_bytes);
   sp.bytes = (size_t)sp.nteams * sp.team_bytes;
+  sp.e5_off = (int)sp.bytes;                      // five-trit byte -> 2-bit codes table
+  if (d.trit5) sp.bytes += 1024;
   return sp;
 }
 
@@ -1194,12 +1197,14 @@ __device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane,
 // (16 channels each) and sums them in registers, two coordinates per table
 // read.  A warp publishes a unit once the next one is computed, so the
 // release finds the stores long done.
-template <int WPT>
-__device__ void screen_team(const Params& P, unsigned char* tsm, int team, int tt) {
+template <int WPT, bool T5>
+__device__ void screen_team(const Params& P, unsigned char* tsm, int team, int tt,
+                            uint32_t e5_base) {
   const Dims& d = P.d;
   const ScreenPlan& sp = P.sp;
   const int lane = threadIdx.x & 31, tw_i = tt >> 5;
-  const int TT = 32 * sp.tw, R16 = d.I / 16, W4 = 2 * R16;
+  constexpr int CPW = T5 ? 20 : 16;   // channels of a 4-byte code word
+  const int TT = 32 * sp.tw, R16 = d.runW, W4 = 2 * R16;
   const int units = P.B * d.topk * d.nb, nctas = gridDim.x;
   const uint32_t S2 = 2u * (uint32_t)d.S;
   const int P16 = (int)(S2 / 16);                // 16-byte pieces per record
@@ -1291,8 +1296,8 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   team_sync(team, TT);
   issue(0);
   if (tt == 0 && team == 0) TRACE_POINT(19);
-  float acc[WPT][16];
-  uint4 al[WPT][2];
+  float acc[WPT][CPW];
+  uint4 al[WPT][3];
   int pend = -1;
   for (int j = 0;; ++j) {
     const int n = j / sp.nch, ch = j % sp.nch;
@@ -1321,17 +1326,31 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
     auto load_alpha = [&]() {
 #pragma unroll
       for (int x = 0; x < WPT; ++x) {
-        const uint4* a4 = reinterpret_cast<const uint4*>(
-            P.scales + (((size_t)e * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
-        al[x][0] = has[x] ? ldg_nc4(a4) : make_uint4(0u, 0u, 0u, 0u);
-        al[x][1] = has[x] ? ldg_nc4(a4 + 1) : make_uint4(0u, 0u, 0u, 0u);
+        const __half* a0 = P.scales + (((size_t)e * d.nb + b) * 2 + gv[x]) * d.I + CPW * jw[x];
+        if (!T5) {
+          const uint4* a4 = reinterpret_cast<const uint4*>(a0);
+          al[x][0] = has[x] ? ldg_nc4(a4) : make_uint4(0u, 0u, 0u, 0u);
+          al[x][1] = has[x] ? ldg_nc4(a4 + 1) : make_uint4(0u, 0u, 0u, 0u);
+        } else {   // 20 halves: five 8-byte groups, those past I not read
+          uint32_t h[10];
+#pragma unroll
+          for (int q = 0; q < 5; ++q) {
+            const bool in = has[x] && CPW * jw[x] + 4 * q < d.I;
+            const uint2 v = in ? ldg_stream2(reinterpret_cast<const uint2*>(a0 + 4 * q)) : make_uint2(0u, 0u);
+            h[2 * q] = v.x;
+            h[2 * q + 1] = v.y;
+          }
+          al[x][0] = make_uint4(h[0], h[1], h[2], h[3]);
+          al[x][1] = make_uint4(h[4], h[5], h[6], h[7]);
+          al[x][2] = make_uint4(h[8], h[9], 0u, 0u);
+        }
       }
     };
     if (ch == 0) {
 #pragma unroll
       for (int x = 0; x < WPT; ++x)
 #pragma unroll
-        for (int q = 0; q < 16; ++q) acc[x][q] = 0.f;
+        for (int q = 0; q < CPW; ++q) acc[x][q] = 0.f;
       if (kAlphaEarly) load_alpha();
     }
     const uint32_t stg = smem_addr(stage + (size_t)(j & 1) * sp.stage_bytes);
@@ -1361,6 +1380,27 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
         const uint32_t sub = (uint32_t)(pg & 3) * 0x40404040u;
 #pragma unroll
         for (int x = 0; x < WPT; ++x) {
+          if (T5) {
+            // byte k of each word: five channels; the expansion table gives
+            // their 2-bit codes a nibble apart, so that nibble m of
+            // ea | eb << 2 is channel 5k + m's pair index
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t ba = __byte_perm(wa[v][x], 0u, 0x4440u + k);
+              const uint32_t bb = __byte_perm(wb[v][x], 0u, 0x4440u + k);
+              // (masked: the spare record slot of an odd count holds stale bytes)
+              const uint32_t z = (lds_u32(e5_base + 4u * ba) & 0x33333u) |
+                                 ((lds_u32(e5_base + 4u * bb) << 2) & 0xCCCCCu);
+              const uint32_t we = ((z << 2) & 0x3C3C3C3Cu) | sub;   // channels 5k, 5k + 2, 5k + 4
+              const uint32_t wo = ((z >> 2) & 0x3C3C3C3Cu) | sub;   // channels 5k + 1, 5k + 3
+              acc[x][5 * k] += lds_f32(__byte_perm(we, blk, 0x7650u));
+              acc[x][5 * k + 1] += lds_f32(__byte_perm(wo, blk, 0x7650u));
+              acc[x][5 * k + 2] += lds_f32(__byte_perm(we, blk, 0x7651u));
+              acc[x][5 * k + 3] += lds_f32(__byte_perm(wo, blk, 0x7651u));
+              acc[x][5 * k + 4] += lds_f32(__byte_perm(we, blk, 0x7652u));
+            }
+            continue;
+          }
           // nibble mm: (even-position code) | (odd-position code) << 2 of channel 2mm / 2mm+1
           const uint32_t ze = (wa[v][x] & 0x33333333u) | ((wb[v][x] << 2) & 0xCCCCCCCCu);
           const uint32_t zo = ((wa[v][x] >> 2) & 0x33333333u) | (wb[v][x] & 0xCCCCCCCCu);
@@ -1386,19 +1426,21 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
 #pragma unroll
     for (int x = 0; x < WPT; ++x) {
       if (!has[x]) continue;
-      const uint32_t hw[8] = {al[x][0].x, al[x][0].y, al[x][0].z, al[x][0].w,
-                              al[x][1].x, al[x][1].y, al[x][1].z, al[x][1].w};
+      const uint32_t hw[12] = {al[x][0].x, al[x][0].y, al[x][0].z, al[x][0].w,
+                               al[x][1].x, al[x][1].y, al[x][1].z, al[x][1].w,
+                               al[x][2].x, al[x][2].y, al[x][2].z, al[x][2].w};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < CPW / 2; ++q) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[q]));
         acc[x][2 * q] *= f.x;
         acc[x][2 * q + 1] *= f.y;
       }
       float4* out = reinterpret_cast<float4*>(
-          P.partial + (((size_t)ts * d.nb + b) * 2 + gv[x]) * d.I + 16 * jw[x]);
+          P.partial + (((size_t)ts * d.nb + b) * 2 + gv[x]) * d.I + CPW * jw[x]);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        out[q] = make_float4(acc[x][4 * q], acc[x][4 * q + 1], acc[x][4 * q + 2], acc[x][4 * q + 3]);
+      for (int q = 0; q < CPW / 4; ++q)   // channels past I (the last five-trit word) are not stored
+        if (!T5 || CPW * jw[x] + 4 * q < d.I)
+          out[q] = make_float4(acc[x][4 * q], acc[x][4 * q + 1], acc[x][4 * q + 2], acc[x][4 * q + 3]);
     }
     pend = ts;
   }
@@ -1408,13 +1450,28 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
 }
 
 // Phase 1a of a CTA: its teams' screen units, WPT code words per thread.
-template <int WPT>
+template <int WPT, bool T5>
 __device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
   const ScreenPlan& sp = P.sp;
+  const uint32_t e5_base = smem_addr(smem + sp.e5_off);
+  if (T5) {   // the expansion table of a five-trit byte: its five 2-bit codes a nibble apart
+    for (int v = threadIdx.x; v < 256; v += kThreads) {   // bytes above 242 do not occur: 0
+      uint32_t z = 0;
+      int q = v < 243 ? v : 0;
+#pragma unroll
+      for (int m = 0; m < 5; ++m) {
+        const int dg = q % 3;
+        q /= 3;
+        z |= (dg == 1 ? 1u : (dg == 2 ? 3u : 0u)) << (4 * m);
+      }
+      reinterpret_cast<uint32_t*>(smem + sp.e5_off)[v] = z;
+    }
+    __syncthreads();
+  }
   const int team = warp / sp.tw;
   if (team >= sp.nteams) return;   // warps left over by the team size
   const int tt = (warp % sp.tw) * 32 + (threadIdx.x & 31);
-  screen_team<WPT>(P, smem + (size_t)team * sp.team_bytes, team, tt);
+  screen_team<WPT, T5>(P, smem + (size_t)team * sp.team_bytes, team, tt, e5_base);
 }
 
 // Score the channels of one (token, slot) once all its blocks are in: sum
@@ -2150,7 +2207,7 @@ __device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane) {
 
 // ------------------------------- the kernel --------------------------------
 // One layer's decode by every CTA of the grid.  false: the launch is aborting.
-template <bool SH, int WPT>
+template <bool SH, int WPT, bool T5>
 __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* smem, int* ctl) {
   if (threadIdx.x == 0) ctl[0] = 0;
   const Dims& d = P.d;
@@ -2162,7 +2219,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   if (threadIdx.x == 0) TRACE_POINT(0);
 
   // phase 1a: screen units (rotation, selection and sketch sums), computed by teams of warps
-  screen_compute<WPT>(P, smem, warp);
+  screen_compute<WPT, T5>(P, smem, warp);
   __syncthreads();
   if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(5);
@@ -2436,18 +2493,18 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
 // The batch-shared selection variant: one kept set for the whole batch.
 // Kernels are specialised on the screen's code words per thread (WPT), so
 // that each holds only the code it runs.
-template <int WPT>
+template <int WPT, bool T5>
 __global__ void __launch_bounds__(kThreads, 1) decode_shared_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  decode_layer<true, WPT>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<true, WPT, T5>(P, aligned_smem(smem_raw), ctl);
 }
 
-template <int WPT>
+template <int WPT, bool T5>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[2];
-  decode_layer<false, WPT>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<false, WPT, T5>(P, aligned_smem(smem_raw), ctl);
   if (threadIdx.x == 0) TRACE_POINT(17);
   if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
     // the next layer would wait for inputs that never come
@@ -2458,10 +2515,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
 
 using KernelFn = void (*)(const Params);
 
-// The kernel for a decode: shared selection or not, the shape's code words per thread.
-KernelFn pick_kernel(bool shared, int wpt) {
-  if (shared) return wpt == 1 ? decode_shared_kernel<1> : wpt == 2 ? decode_shared_kernel<2> : decode_shared_kernel<3>;
-  return wpt == 1 ? decode_kernel<1> : wpt == 2 ? decode_kernel<2> : decode_kernel<3>;
+template <bool T5>
+KernelFn pick_kernel_t(bool shared, int wpt) {
+  if (shared)
+    return wpt == 1 ? decode_shared_kernel<1, T5> : wpt == 2 ? decode_shared_kernel<2, T5> : decode_shared_kernel<3, T5>;
+  return wpt == 1 ? decode_kernel<1, T5> : wpt == 2 ? decode_kernel<2, T5> : decode_kernel<3, T5>;
+}
+
+// The kernel for a decode: shared selection or not, the screen's code words
+// per thread and the code layout (2-bit or five trits per byte).
+KernelFn pick_kernel(bool shared, int wpt, bool t5) {
+  return t5 ? pick_kernel_t<true>(shared, wpt) : pick_kernel_t<false>(shared, wpt);
 }
 
 size_t decode_smem_bytes(const Dims& d) {
@@ -2501,7 +2565,7 @@ cudaError_t configure_decode_kernels(const Dims& d) {
   if (sp.bytes == 0) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes(d);
   for (int v = 0; v < 2; ++v) {   // the shape's kernels: per-token and shared
-    const KernelFn fn = pick_kernel(v == 1, sp.wpt);
+    const KernelFn fn = pick_kernel(v == 1, sp.wpt, d.trit5 != 0);
     cudaFuncAttributes fa;
     cudaError_t err = cudaFuncGetAttributes(&fa, fn);
     if (err != cudaSuccess) return err;
@@ -2517,7 +2581,7 @@ int decode_grid(const Dims& d) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pick_kernel(false, screen_plan(d).wpt),
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pick_kernel(false, screen_plan(d).wpt, d.trit5 != 0),
                                                     kThreads, decode_smem_bytes(d)) != cudaSuccess)
     return 0;
   return per_sm >= 1 ? sms : 0;   // one CTA per SM, all co-resident
@@ -2623,7 +2687,7 @@ static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStrea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pick_kernel(shared, P.sp.wpt), P);
+  return cudaLaunchKernelEx(&cfg, pick_kernel(shared, P.sp.wpt, h.d.trit5 != 0), P);
 }
 
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,

@@ -30,9 +30,11 @@ constexpr uint32_t kErrTimeout = MOE_READER_ERR_TIMEOUT;
 struct Dims {
   int H, E, topk, I, c, r, Bmax;
   int Hp, nb, N;
-  int S;            // bytes per coordinate run (multiple of 32)
-  int runW;         // 32-bit words of codes per run actually used: I / 16
+  int S;            // bytes per coordinate run (multiple of 32), in the stored code layout
+  int runW;         // 32-bit words of codes per run actually used (16 channels a word, 20 five-trit)
   int rho_rank;     // 1: full screen ranked by the expected skip error
+  int trit5;        // 1: five trits per byte (else 2-bit codes)
+  int S2b;          // the 2-bit layout's run stride (the sketch is built in it first)
 };
 
 // Decode workspace (device), sized for Bmax tokens.
@@ -131,6 +133,8 @@ bool take_prepare_stall();
 cudaError_t launch_sketch(const Dims& d, const __nv_bfloat16* G, const __nv_bfloat16* V,
                           const int8_t* sigma, uint8_t* codes, __half* scales, __half* rho,
                           cudaStream_t s);
+// Five-trit runs (stride d.S) from 2-bit runs (stride d.S2b), layout [E][nb][128][2][run].
+cudaError_t launch_pack_trit5(const Dims& d, const uint8_t* codes2, uint8_t* codes5, cudaStream_t s);
 cudaError_t launch_transpose_down(const Dims& d, const __nv_bfloat16* D, __nv_bfloat16* Dt,
                                   cudaStream_t s);
 cudaError_t launch_dnorm(const Dims& d, const __nv_bfloat16* Dt, float* dnorm, cudaStream_t s);

@@ -232,7 +232,39 @@ project_b_kernel(Dims d, const __nv_bfloat16* __restrict__ Dt, const __half* __r
   }
 }
 
+// ---------------------------------------------------------------------------
+// Five trits per byte: output byte j of a run holds channels 5j .. 5j+4 as
+// sum_m digit * 3^m (2-bit code 0b00 -> 0, 0b01 (+1) -> 1, 0b11 (-1) -> 2);
+// channels past I and the sector padding are 0.  A thread per output byte.
+// ---------------------------------------------------------------------------
+__global__ void pack_trit5_kernel(Dims d, const uint8_t* __restrict__ codes2,
+                                  uint8_t* __restrict__ codes5, long long runs) {
+  const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= runs * d.S) return;
+  const long long run = q / d.S;
+  const int j = (int)(q - run * d.S);
+  const uint8_t* src = codes2 + run * d.S2b;
+  int v = 0, p3 = 1;
+#pragma unroll
+  for (int m = 0; m < 5; ++m) {
+    const int i = 5 * j + m;
+    if (i < d.I) {
+      const int c = (src[i >> 2] >> (2 * (i & 3))) & 3;
+      v += (c == 1 ? 1 : (c == 3 ? 2 : 0)) * p3;
+    }
+    p3 *= 3;
+  }
+  codes5[q] = (uint8_t)v;
+}
+
 }  // namespace
+
+cudaError_t launch_pack_trit5(const Dims& d, const uint8_t* codes2, uint8_t* codes5, cudaStream_t s) {
+  const long long runs = (long long)d.E * d.nb * kBlock * 2;
+  const long long n = runs * d.S;
+  pack_trit5_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(d, codes2, codes5, runs);
+  return cudaGetLastError();
+}
 
 // Ut[j][h] = U[h][j]: the output phase reads rank components as rows.
 __global__ void transpose_u_kernel(int H, int r, const __half* __restrict__ U,

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(HERE, "libmoe_reader.so")
 
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EDEVICE, ESTATE, ETOOBIG = 0, -1, -2, -3, -4, -5, -6, -7
 FLAG_RHO_RANK = 0x1   # full screen ranked by the expected skip error (screen_coords = 128)
+FLAG_TRIT5 = 0x2      # sketch codes stored five trits per byte
 ERR_EXPERT_RANGE, ERR_EXPERT_DUP, ERR_WEIGHT, ERR_X_NONFINITE, ERR_TIMEOUT = 1, 2, 4, 8, 16
 # one-shot fault injections for tests of failure detection (moe_reader_inject_fault)
 INJECT_DECODE_STALL, INJECT_PREPARE_STALL, INJECT_ALLOC_FAIL = 0x1, 0x2, 0x4

@@ -72,7 +72,7 @@ typedef struct {
   int32_t screen_coords;      /* c: coordinates screened per block, 1..128 (80 = partial screen) */
   int32_t rank;               /* r: recovery rank, 1 <= r <= min(H, 64) */
   int32_t max_batch;          /* B_max: 1..1024 tokens per decode (workspace sizing) */
-  int32_t flags;              /* 0, or MOE_READER_FLAG_RHO_RANK */
+  int32_t flags;              /* 0 or MOE_READER_FLAG_RHO_RANK | MOE_READER_FLAG_TRIT5 */
 } moe_reader_config;
 
 /* Full-screen ranking (Chinese summary page, 方法步骤详情 decode (2): from the
@@ -86,6 +86,16 @@ typedef struct {
  * to first order in the sketch errors; the top-k and everything after it are
  * unchanged. */
 #define MOE_READER_FLAG_RHO_RANK 0x1
+
+/* Five trits per byte (the Chinese summary page's ~30 bytes per 128-coordinate
+ * block, 方法步骤详情 load-time (1) and 核心方法): the sketch codes of a
+ * coordinate run are stored as ceil(I/5) bytes, byte j holding channels
+ * 5j .. 5j+4 as sum_m digit(t_{5j+m}) 3^m with digit(0) = 0, digit(+1) = 1,
+ * digit(-1) = 2, the run padded to 32-byte sectors (S = ceil(ceil(I/5)/32)*32
+ * instead of ceil(ceil(I/4)/32)*32).  Every estimate, score, kept set and
+ * output equals the 2-bit layout's; the screen reads and holds fewer bytes.
+ * Combines with MOE_READER_FLAG_RHO_RANK. */
+#define MOE_READER_FLAG_TRIT5 0x2
 
 /* Read accounting of the last decode, in 32-byte sectors.  Every parameter
  * array starts on a 256-byte boundary; a count is the number of distinct
@@ -113,7 +123,8 @@ typedef struct {
   int32_t hidden_padded;        /* Hp */
   int32_t num_blocks;           /* nb = Hp / 128 */
   int32_t routed_channels;      /* N = topk * I */
-  int32_t run_stride;           /* S: bytes per coordinate run, ceil(ceil(I/4)/32)*32 */
+  int32_t run_stride;           /* S: bytes per coordinate run, ceil(ceil(I/4)/32)*32
+                                   (ceil(ceil(I/5)/32)*32 with MOE_READER_FLAG_TRIT5) */
   uint64_t resident_bytes[9];   /* codes, scales, rho, dnorm, Dt, U (with its transpose), b,
                                    sigma, workspace */
 } moe_reader_info;
@@ -304,7 +315,7 @@ int moe_reader_get_stats(moe_reader_t* h, moe_reader_stats* out);
 int moe_reader_get_kept(moe_reader_t* h, int32_t* kept_host, int64_t capacity);
 
 /* Exportable arrays (moe_reader_export).  Prepared data: */
-#define MOE_READER_EXPORT_CODES    0   /* u8   [E][nb][128][2][S] */
+#define MOE_READER_EXPORT_CODES    0   /* u8   [E][nb][128][2][S] (2-bit or five-trit runs) */
 #define MOE_READER_EXPORT_SCALES   1   /* f16  [E][nb][2][I] */
 #define MOE_READER_EXPORT_RHO      2   /* f16  [E][nb][2][I] */
 #define MOE_READER_EXPORT_DNORM    3   /* f32  [E][I] */

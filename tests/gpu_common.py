@@ -44,6 +44,8 @@ class Pair:
         self.dev = (g, v, d)
         self.reader = MoeReader(H, E, topk, I, g, v, d, self.sigma, screen_coords=c, rank=r,
                                 max_batch=max_batch, flags=flags)
+        from calibration_free_sparse_gb300.reader import FLAG_TRIT5
+        self.codes = "trit5" if flags & FLAG_TRIT5 else "2bit"
         self.layer = R.Layer(self.shape, self.G, self.V, self.D, self.sigma)
 
     def tokens(self, B, seed):
@@ -151,7 +153,7 @@ def assert_read_accounting(pair, ids, gmasks, kept_lists, st=None):
     """The library's sector counts equal the oracle's count of the kernel's
     own screened sets and kept lists (holds whatever the near-ties did)."""
     st = pair.reader.stats() if st is None else st
-    ref = SC.decode_sectors(pair.shape, ids, gmasks, kept_lists)
+    ref = SC.decode_sectors(pair.shape, ids, gmasks, kept_lists, codes=getattr(pair, "codes", "2bit"))
     for name in ref:
         assert st[name] == ref[name], name
     return st
@@ -175,7 +177,7 @@ def check_decode(pair, x, ids, w, k, y, tokens=None, band=KEPT_BAND):
     st = assert_read_accounting(pair, ids, gm, [kept[t] for t in range(B)])
     if ndiff == 0 and len(res) == B:
         ref = SC.decode_sectors(pair.shape, ids, np.stack([res[t].mask for t in range(B)]),
-                                [res[t].kept for t in range(B)])
+                                [res[t].kept for t in range(B)], codes=getattr(pair, "codes", "2bit"))
         for name in ref:
             assert st[name] == ref[name], name
     if rerun:

@@ -38,7 +38,8 @@ def prepare(lib, **over):
 
 
 @pytest.mark.parametrize("over", [
-    dict(flags=2), dict(flags=RD.FLAG_RHO_RANK),            # the ranking needs c = 128
+    dict(flags=4), dict(flags=RD.FLAG_RHO_RANK),            # an unknown bit; the ranking needs c = 128
+    dict(flags=RD.FLAG_RHO_RANK | RD.FLAG_TRIT5),
     dict(hidden=100), dict(hidden=0), dict(num_experts=0),
     dict(experts_per_token=9), dict(experts_per_token=0),
     dict(inter=96), dict(inter=0), dict(inter=16384),
