@@ -390,11 +390,15 @@ def run_ours(args, wl, world, rank, local):
 
     # -- prepared layers (weights drawn on the device, one seed per layer and rank)
     readers, keep = [], []
+    prep_s = []
     for l in range(L):
         seed = 1000 + l + 7919 * rank
         g, v, d = S.weights_device(seed, wl.E, wl.I, wl.H, dev)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         rd = MoeReader(wl.H, wl.E, wl.topk, wl.I, g, v, d, S.signs(seed, wl.Hp),
-                       screen_coords=wl.c, rank=wl.r, max_batch=Bmax)
+                       screen_coords=wl.c, rank=wl.r, max_batch=Bmax)   # synchronizes its stream
+        prep_s.append(time.perf_counter() - t0)
         del d
         readers.append(rd)
         keep.append((g, v))
@@ -741,6 +745,7 @@ def run_ours(args, wl, world, rank, local):
             "rho_rank": rho,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "prepare_ms_per_layer": 1000.0 * statistics.median(prep_s),
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }

@@ -267,30 +267,55 @@ __device__ int sturm_count(int n, const double* dg, const double* e2, double x, 
   return cnt;
 }
 
-// Thread j finds the j-th largest eigenvalue of T = tridiag(e, dg, e).
+// e2[i] = eg[i]^2 (one thread per entry).
+__global__ void square_offdiag_kernel(int n, const double* __restrict__ eg, double* __restrict__ e2) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i + 1 < n) e2[i] = eg[i] * eg[i];
+}
+
+// Warp j finds the j-th largest eigenvalue of T = tridiag(e, dg, e) by
+// multisection: each step its 32 lanes take Sturm counts at 32 points that
+// split [lo, hi] into 33 equal parts, and the part holding the eigenvalue
+// becomes the new interval; it stops when the points no longer fall strictly
+// inside the interval (the interval is down to a few ulps).
 __global__ void bisect_kernel(int n, int r, const double* __restrict__ dg,
-                              const double* __restrict__ eg, double* __restrict__ e2,
+                              const double* __restrict__ eg, const double* __restrict__ e2,
                               double* __restrict__ lam) {
-  // e2 is filled by thread 0 and shared through global memory
-  if (threadIdx.x == 0)
-    for (int i = 0; i + 1 < n; ++i) e2[i] = eg[i] * eg[i];
-  __syncthreads();
-  const int j = threadIdx.x;
+  const int j = blockIdx.x, lane = threadIdx.x;
   if (j >= r) return;
   double lo = DBL_MAX, hi = -DBL_MAX, emax2 = 0.0;
-  for (int i = 0; i < n; ++i) {
+  for (int i = lane; i < n; i += 32) {
     const double a = i > 0 ? fabs(eg[i - 1]) : 0.0;
     const double b = i + 1 < n ? fabs(eg[i]) : 0.0;
     lo = fmin(lo, dg[i] - a - b);
     hi = fmax(hi, dg[i] + a + b);
     if (i + 1 < n) emax2 = fmax(emax2, e2[i]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fmin(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmax(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    emax2 = fmax(emax2, __shfl_xor_sync(0xffffffffu, emax2, o));
+  }
   const double span = fmax(hi - lo, fmax(fabs(lo), fabs(hi)) * DBL_EPSILON);
   lo -= 2.0 * DBL_EPSILON * span + DBL_MIN;
   hi += 2.0 * DBL_EPSILON * span + DBL_MIN;
   const double pivmin = DBL_MIN * fmax(1.0, emax2);
   const int target = n - 1 - j;   // eigenvalues strictly below the wanted one
-  for (int it = 0; it < 256; ++it) {
+  for (int it = 0; it < 64; ++it) {
+    const double x = lo + (hi - lo) * ((double)(lane + 1) / 33.0);
+    const bool inside = x > lo && x < hi;
+    if (!__all_sync(0xffffffffu, inside)) break;
+    const bool above = sturm_count(n, dg, e2, x, pivmin) >= target + 1;   // eigenvalue < x
+    const unsigned bal = __ballot_sync(0xffffffffu, above);
+    const int first = bal ? __ffs(bal) - 1 : 32;   // the first point above the eigenvalue
+    const double xhi = __shfl_sync(0xffffffffu, x, first < 32 ? first : 31);
+    const double xlo = __shfl_sync(0xffffffffu, x, first > 0 ? first - 1 : 0);
+    if (first < 32) hi = xhi;
+    if (first > 0) lo = xlo;
+  }
+  // finish by bisection while a midpoint still falls strictly inside
+  for (int it = 0; it < 128; ++it) {
     const double mid = 0.5 * (lo + hi);
     if (mid <= lo || mid >= hi) break;
     if (sturm_count(n, dg, e2, mid, pivmin) >= target + 1)
@@ -298,7 +323,7 @@ __global__ void bisect_kernel(int n, int r, const double* __restrict__ dg,
     else
       lo = mid;
   }
-  lam[j] = 0.5 * (lo + hi);
+  if (lane == 0) lam[j] = 0.5 * (lo + hi);
 }
 
 // Inverse iteration for eigenvalue lam[j] of T (thread j); scratch holds
@@ -534,7 +559,9 @@ int build_recovery_basis(const Dims& d, const __nv_bfloat16* Dt, __half* U, doub
     if ((ce = cudaLaunchCooperativeKernel((void*)tridiag_kernel, dim3(grid), dim3(512), args, smem,
                                           s)) != cudaSuccess)
       break;
-    bisect_kernel<<<1, 64, 0, s>>>(n, r, dg, eg, e2, lam);
+    square_offdiag_kernel<<<(n + 255) / 256, 256, 0, s>>>(n, eg, e2);
+    if ((ce = cudaGetLastError()) != cudaSuccess) break;
+    bisect_kernel<<<r, 32, 0, s>>>(n, r, dg, eg, e2, lam);
     if ((ce = cudaGetLastError()) != cudaSuccess) break;
     inverse_iter_kernel<<<(r + 31) / 32, 32, 0, s>>>(n, r, dg, eg, lam, scr, piv, Z);
     if ((ce = cudaGetLastError()) != cudaSuccess) break;
