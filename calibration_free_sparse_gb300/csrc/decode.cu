@@ -22,6 +22,8 @@
 //            BF16 rows, fp32 x) and 64-channel recovery chunks
 //            (sum w_j p_j b_j over skipped channels)
 //   phase 3  output slices of 16 columns: y = sum_K w_j a_j Dt_j + U c
+#include <algorithm>
+
 #include "device_util.cuh"
 #include "internal.cuh"
 
@@ -50,14 +52,15 @@ struct ScreenPlan {
 
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-ScreenPlan screen_plan(const Dims& d) {
+// warps: the warps that screen; budget: the shared memory they may use
+ScreenPlan screen_plan(const Dims& d, int warps = kWarps, size_t budget = kSmemBudget) {
   ScreenPlan sp{};
   const int W4 = 2 * d.runW;                     // 4-byte words per coordinate record
   double best = 0.0;
   for (int wpt = 1; wpt <= 3; ++wpt) {           // most useful lanes per issue slot
     const int tw = (W4 + 32 * wpt - 1) / (32 * wpt);
-    if (tw > kWarps) continue;
-    const int nteams = std::min(15, kWarps / tw);
+    if (tw > warps) continue;
+    const int nteams = std::min(15, warps / tw);
     const double score = (double)nteams / wpt;
     if (score > best + 1e-9) {
       best = score;
@@ -72,7 +75,7 @@ ScreenPlan screen_plan(const Dims& d) {
   sp.coord_off = (int)round_up(64 * (size_t)((d.c + 1) / 2), 256);
   sp.buf_bytes = (int)round_up((size_t)sp.coord_off + 128 + 4 * kBlock, 256);   // + Rx in list order
   const size_t S2 = 2 * (size_t)d.S;
-  const size_t per_team = (kSmemBudget - (d.trit5 ? 1024 : 0)) / sp.nteams / 256 * 256;
+  const size_t per_team = (budget - (d.trit5 ? 1024 : 0)) / sp.nteams / 256 * 256;
   const size_t fixed = 256 + 2 * (size_t)sp.buf_bytes;
   for (int nch = 1; nch <= d.c && !sp.cc; ++nch) {
     int c1 = (d.c + nch - 1) / nch;
@@ -244,80 +247,162 @@ __device__ bool wait_at_least(const Params& P, const uint32_t* flag, uint32_t ta
 
 // Offsets (in uint32) of the synchronisation area, fixed per handle.
 // slot .. exact: the decode's own hand-offs; cbdone .. ssum: the residual
-// hand-off of a stacked layer (ssum: fp64 [Bmax], 8-byte aligned).
+// hand-off of a stacked layer (ssum: fp64 [Bmax], 8-byte aligned).  Every
+// group, and each single word below, starts a 128-byte line of its own, so
+// that the words polled by many warps share no line with the counters that
+// the hand-offs add to.
+constexpr int kSyncLine = 32;
+__host__ __device__ inline int sync_line(int w) { return (w + kSyncLine - 1) / kSyncLine * kSyncLine; }
 struct SyncOff {
   int slot, tok, flag, exact, cbdone, tokdone, xready, ssum, ecount, total;
 };
+// the single words: CTAs done, the launch's abort flag, and the shared
+// kernel's batch-wide hand-offs (routed experts scored, the batch's kept set
+// released, shared kept items done)
+constexpr int kSyncDone = 0, kSyncAbort = kSyncLine, kSyncBatch = 2 * kSyncLine,
+              kSyncReady = 3 * kSyncLine, kSyncSdone = 4 * kSyncLine;
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
-  o.slot = 16;
-  o.tok = o.slot + d.Bmax * d.topk;
-  o.flag = o.tok + d.Bmax;
-  o.exact = o.flag + d.Bmax;
-  o.cbdone = o.exact + d.Bmax;
-  o.tokdone = o.cbdone + d.Bmax * ((d.H + 255) / 256);
-  o.xready = o.tokdone + d.Bmax;
-  o.ssum = (o.xready + d.Bmax + 1) & ~1;
-  o.ecount = o.ssum + 2 * d.Bmax;   // the shared kernel: score tasks in, per expert
+  o.slot = 5 * kSyncLine;
+  o.tok = sync_line(o.slot + d.Bmax * d.topk);
+  o.flag = sync_line(o.tok + d.Bmax);
+  o.exact = sync_line(o.flag + d.Bmax);
+  o.cbdone = sync_line(o.exact + d.Bmax);
+  o.tokdone = sync_line(o.cbdone + d.Bmax * ((d.H + 255) / 256));
+  o.xready = sync_line(o.tokdone + d.Bmax);
+  o.ssum = sync_line(o.xready + d.Bmax);
+  o.ecount = sync_line(o.ssum + 2 * d.Bmax);   // the shared kernel: score tasks in, per expert
   o.total = o.ecount + d.E;
   return o;
 }
-constexpr int kSyncDone = 0, kSyncAbort = 2;
 
 __device__ bool wait_at_least(const Params& P, const uint32_t* flag, uint32_t target) {
   if (ld_acquire(flag) >= target) return true;
   uint32_t* abort_flag = P.sync + kSyncAbort;
   const unsigned long long t0 = globaltimer();
-  while (true) {
+  for (uint32_t it = 1;; ++it) {
     // poll without ordering; the acquire load orders what follows once it is met
     if (ld_relaxed(flag) >= target && ld_acquire(flag) >= target) return true;
-    if (ld_relaxed(abort_flag)) return false;
-    if (globaltimer() - t0 > P.wait_ns) {
-      atomicOr(P.err, kErrTimeout);
-      atomicExch(abort_flag, 1u);
-      return false;
+    if ((it & 7u) == 0) {   // the abort flag and the clock every eighth poll
+      if (ld_relaxed(abort_flag)) return false;
+      if (globaltimer() - t0 > P.wait_ns) {
+        atomicOr(P.err, kErrTimeout);
+        atomicExch(abort_flag, 1u);
+        return false;
+      }
     }
     __nanosleep(64);
   }
 }
-// the shared kernel's batch-wide hand-offs: routed experts scored, the
-// batch's kept set released, shared kept items done
-constexpr int kSyncBatch = 5, kSyncReady = 6, kSyncSdone = 7;
+
+// A warp's wait for a flag that several warps of the CTA wait for: the first
+// warp to arrive polls global memory (wait_at_least) and leaves the outcome
+// in shared memory (1 met, 2 given up); the others wait on that word, so the
+// CTA has one poller per flag.  seen / claim: the flag's two shared words,
+// zero before the first caller.  The fence pairs order the poller's acquire
+// before the word and the waiters' later reads after it.
+__device__ bool cta_wait(const Params& P, const uint32_t* flag, uint32_t target, int* seen, int* claim,
+                         int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    volatile int* vs = seen;
+    int v = *vs;
+    if (v == 0) {
+      if (atomicCAS(claim, 0, 1) == 0) {
+        const bool met = wait_at_least(P, flag, target);
+        __threadfence_block();
+        *vs = met ? 1 : 2;
+        v = met ? 1 : 2;
+      } else {
+        // the poller's wait is bounded; this bound only backs it up
+        const unsigned long long t0 = globaltimer();
+        while ((v = *vs) == 0) {
+          if (globaltimer() - t0 > 2 * P.wait_ns) {
+            v = 2;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+    }
+    __threadfence_block();
+    ok = v == 1;
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+// A group of warps of the CTA that works together: thread tid of nt, warp wid
+// of nw, and the named barrier spanning the group (0: the whole CTA).
+struct Grp {
+  int tid, nt, wid, nw, bar;
+  __device__ __forceinline__ void sync() const {
+    if (bar == 0) __syncthreads();
+    else asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nt) : "memory");
+  }
+};
+__device__ __forceinline__ Grp cta_group() {
+  return Grp{(int)threadIdx.x, kThreads, (int)(threadIdx.x >> 5), kWarps, 0};
+}
 
 // ------------------------------- phase 0 -----------------------------------
 // Rotation and screen selection of one (token, 128-block) by one warp: lane
 // l ends with Rx of coordinates l + 32 s (s < 4) in u[s] and with word[s] =
 // the selection bits of coordinates 32 s .. 32 s + 31 (the c largest |Rx|,
-// ties to the lower coordinate).  rotate_load reads sigma x (true: x held a
-// NaN or an infinity); rotate_select_loaded does the rest.
-__device__ __forceinline__ bool rotate_load(const Params& P, int t, int b, int slot, int lane,
-                                            float (&u)[4]) {
+// ties to the lower coordinate).  UnitInput holds a unit's raw loads, issued
+// by unit_issue one unit ahead and used by nothing until unit_finish forms
+// sigma x, so that the loads land while the warp sums; rotate_select_loaded
+// does the rest.
+struct UnitInput {
+  float x[4];       // x (a stacked layer: the residual h) of coordinates lane + 32 s
+  int sg[4];        // their rotation signs
+  float f;          // a stacked layer: the token's input scale
+  int id[2];        // the token's expert ids of slots lane, lane + 32 (inputs)
+  float w[2];       // their routing weights
+};
+
+__device__ __forceinline__ void unit_issue(const Params& P, int t, int b, int lane, UnitInput& in) {
   const Dims& d = P.d;
-  bool bad = false;
   const size_t row = (size_t)t * d.H;
-  if (P.xscale) {   // a stacked layer: x = h / RMS(h), written out once per (token, block)
-    const float f = __ldcg(P.xscale + t);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int col = b * kBlock + lane + 32 * s;
-      const float xv = col < d.H ? __ldcg(P.hres + row + col) * f : 0.f;
-      if (slot == 0 && col < d.H) P.xfill[row + col] = xv;
-      bad |= !isfinite(xv);
-      u[s] = P.sigma[col] < 0 ? -xv : xv;
-    }
-    return bad;
-  }
+  const float* src = P.xscale ? P.hres : P.x;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int col = b * kBlock + lane + 32 * s;
-    const float xv = col < d.H ? __ldcg(P.x + row + col) : 0.f;
+    in.x[s] = col < d.H ? __ldcg(src + row + col) : 0.f;
+    in.sg[s] = P.sigma[col];
+  }
+  in.f = P.xscale ? __ldcg(P.xscale + t) : 1.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int sl = lane + 32 * h;
+    in.id[h] = sl < d.topk ? __ldg(P.ids_in + t * d.topk + sl) : 0;
+    in.w[h] = sl < d.topk ? __ldg(P.w_in + t * d.topk + sl) : 0.f;
+  }
+}
+
+// sigma x into u; true: x held a NaN or an infinity.  A stacked layer's slot-0
+// unit writes x = h * scale out for the rest of the layer.
+__device__ __forceinline__ bool unit_finish(const Params& P, int t, int b, int slot, int lane,
+                                            const UnitInput& in, float (&u)[4]) {
+  const Dims& d = P.d;
+  bool bad = false;
+  const size_t row = (size_t)t * d.H;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int col = b * kBlock + lane + 32 * s;
+    float xv = in.x[s];
+    if (P.xscale) {
+      xv = col < d.H ? xv * in.f : 0.f;
+      if (slot == 0 && col < d.H) P.xfill[row + col] = xv;
+    }
     bad |= !isfinite(xv);
-    u[s] = P.sigma[col] < 0 ? -xv : xv;
+    u[s] = in.sg[s] < 0 ? -xv : xv;
   }
   return bad;
 }
 
-// u[s] = sigma x of coordinate lane + 32 s on entry (from rotate_load), Rx on exit.
+// u[s] = sigma x of coordinate lane + 32 s on entry (from unit_finish), Rx on exit.
 __device__ void rotate_select_loaded(const Params& P, int lane, float (&u)[4], uint32_t (&word)[4]) {
   const Dims& d = P.d;
   // Sylvester butterfly, strides 1, 2, ..., 64; pair (i, i+h) -> (a + b, a - b) in fp32
@@ -348,20 +433,36 @@ __device__ void rotate_select_loaded(const Params& P, int lane, float (&u)[4], u
     return (int)__reduce_add_sync(0xffffffffu, (unsigned)((m[0] >= v) + (m[1] >= v) + (m[2] >= v) +
                                                           (m[3] >= v)));
   };
-  uint32_t T = 0;
-  if (count_ge(1u << 30) >= d.c) T = 1u << 30;
+  // A candidate with exactly c magnitudes at or above it ends the search:
+  // those c are the selection (every magnitude equal to the c-th largest is
+  // among them), the same set as the full search and its tie rule give.
+  const float inv = 0.08838834764831845f;   // 1/sqrt(128) rounded to fp32
+  uint32_t T = 0, Tx = 0xffffffffu;
+  {
+    const int n0 = count_ge(1u << 30);
+    if (n0 == d.c) Tx = 1u << 30;
+    if (n0 >= d.c) T = 1u << 30;
+  }
 #pragma unroll 1
-  for (int bit = 28; bit >= 0; bit -= 2) {
+  for (int bit = 28; bit >= 0 && Tx == 0xffffffffu; bit -= 2) {
     const uint32_t c1 = T | (1u << bit), c2 = T | (2u << bit), c3 = T | (3u << bit);
     const int n1 = count_ge(c1), n2 = count_ge(c2), n3 = count_ge(c3);
+    Tx = n3 == d.c ? c3 : (n2 == d.c ? c2 : (n1 == d.c ? c1 : Tx));
     T = n3 >= d.c ? c3 : (n2 >= d.c ? c2 : (n1 >= d.c ? c1 : T));
+  }
+  if (Tx != 0xffffffffu) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      word[s] = __ballot_sync(0xffffffffu, m[s] >= Tx);
+      u[s] *= inv;
+    }
+    return;
   }
   const int gt = (int)__reduce_add_sync(0xffffffffu, (unsigned)((m[0] > T) + (m[1] > T) + (m[2] > T) +
                                                                 (m[3] > T)));
   const int need = d.c - gt;
   const uint32_t below = (1u << lane) - 1u;
   int before = 0;
-  const float inv = 0.08838834764831845f;   // 1/sqrt(128) rounded to fp32
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const uint32_t eqb = __ballot_sync(0xffffffffu, m[s] == T);
@@ -376,28 +477,28 @@ __device__ void rotate_select_loaded(const Params& P, int lane, float (&u)[4], u
 // ------------------------------- top-k -------------------------------------
 // k-th largest key among the entries keyfn accepts; per-warp histograms.
 template <typename KeyFn>
-__device__ uint32_t cta_radix_select(int N, int kth, KeyFn keyfn, int* hist, int* sh, int* rem) {
+__device__ uint32_t cta_radix_select(const Grp& g, int N, int kth, KeyFn keyfn, int* hist, int* sh,
+                                     int* rem) {
   uint32_t prefix = 0, pmask = 0;
   int remaining = kth;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = g.wid, lane = g.tid & 31;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int n = threadIdx.x; n < N; n += kThreads) {
+    for (int i = g.tid; i < g.nw * 256; i += g.nt) hist[i] = 0;
+    g.sync();
+    for (int n = g.tid; n < N; n += g.nt) {
       uint32_t key;
       if (!keyfn(n, key)) continue;
       if ((key & pmask) == prefix) atomicAdd(&hist[warp * 256 + ((key >> shift) & 255u)], 1);
     }
-    __syncthreads();
-    if (threadIdx.x < 256) {
+    g.sync();
+    for (int i = g.tid; i < 256; i += g.nt) {
       int tot = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) tot += hist[w * 256 + threadIdx.x];
-      hist[kWarps * 256 + threadIdx.x] = tot;
+      for (int w = 0; w < g.nw; ++w) tot += hist[w * 256 + i];
+      hist[g.nw * 256 + i] = tot;
     }
-    __syncthreads();
+    g.sync();
     if (warp == 0) {
-      const int* totals = hist + kWarps * 256;
+      const int* totals = hist + g.nw * 256;
       int local[8];
       int tot = 0;
 #pragma unroll
@@ -429,11 +530,11 @@ __device__ uint32_t cta_radix_select(int N, int kth, KeyFn keyfn, int* hist, int
         sh[1] = fr;
       }
     }
-    __syncthreads();
+    g.sync();
     prefix |= (uint32_t)sh[0] << shift;
     pmask |= 255u << shift;
     remaining = sh[1];
-    __syncthreads();
+    g.sync();
   }
   *rem = remaining;
   return prefix;
@@ -457,8 +558,9 @@ __host__ __device__ inline size_t topk_smem_bytes(int N) {
 // Sum of wsum[0 .. wid) for the calling thread's warp, by a shuffle scan of
 // the kWarps per-warp values (read after the barrier that follows their
 // writes); *total (may be null) receives the sum of all of them.
-__device__ __forceinline__ int warps_before(const int* wsum, int wid, int lane, int* total) {
-  const int v = lane < kWarps ? wsum[lane] : 0;
+__device__ __forceinline__ int warps_before(const int* wsum, int wid, int lane, int* total,
+                                            int nw = kWarps) {
+  const int v = lane < nw ? wsum[lane] : 0;
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -471,26 +573,26 @@ __device__ __forceinline__ int warps_before(const int* wsum, int wid, int lane, 
 
 // The top-k's fallback when more than kCandMax keys share the threshold digit:
 // a full radix select on the keys, ties by the lower global id.  Sets keep[].
-__device__ __noinline__ void topk_radix_fallback(const uint32_t* keys, uint8_t* keep, const int* eid,
-                                                 int N, int k, int I, int* hist, int* sh,
-                                                 int* wsum) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+__device__ __noinline__ void topk_radix_fallback(const Grp& g, const uint32_t* keys, uint8_t* keep,
+                                                 const int* eid, int N, int k, int I, int* hist,
+                                                 int* sh, int* wsum) {
+  const int lane = g.tid & 31, wid = g.wid;
   int need2 = 0;
   const uint32_t T = cta_radix_select(
-      N, k, [&](int n, uint32_t& key) { key = keys[n]; return true; }, hist, sh + 4, &need2);
+      g, N, k, [&](int n, uint32_t& key) { key = keys[n]; return true; }, hist, sh + 4, &need2);
   int eq = 0;
-  for (int n = threadIdx.x; n < N; n += kThreads) eq += keys[n] == T;
+  for (int n = g.tid; n < N; n += g.nt) eq += keys[n] == T;
   eq = warp_sum_i(eq);
   if (lane == 0) wsum[wid] = eq;
-  __syncthreads();
+  g.sync();
   int eq_total = 0;
-  for (int w = 0; w < kWarps; ++w) eq_total += wsum[w];
-  __syncthreads();
+  for (int w = 0; w < g.nw; ++w) eq_total += wsum[w];
+  g.sync();
   uint32_t T2 = 0;
   if (need2 < eq_total) {
     int dummy = 0;
     T2 = cta_radix_select(
-        N, need2,
+        g, N, need2,
         [&](int n, uint32_t& key) {
           if (keys[n] != T) return false;
           key = 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I);
@@ -498,13 +600,15 @@ __device__ __noinline__ void topk_radix_fallback(const uint32_t* keys, uint8_t* 
         },
         hist, sh + 4, &dummy);
   }
-  for (int n = threadIdx.x; n < N; n += kThreads) {
+  for (int n = g.tid; n < N; n += g.nt) {
     const uint32_t a = keys[n];
     keep[n] = a > T || (a == T && 0xffffffffu - (uint32_t)(eid[n / I] * I + n % I) >= T2);
   }
 }
 
-__device__ void topk_token(const Params& P, int t, unsigned char* smem) {
+template <int NT>
+__device__ void topk_token(const Params& P, const Grp& g, int t, unsigned char* smem) {
+  constexpr int NW = NT / 32;
   const Dims& d = P.d;
   const int N = d.N, k = P.k, I = d.I;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                      // [N]
@@ -516,40 +620,42 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
   int* sh = crank + kCandMax;                                               // [8]
   int* wsum = sh + 8;                                                       // [kWarps]
   int* eid = wsum + kWarps;                                                 // [topk]
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int s = threadIdx.x; s < d.topk; s += kThreads) eid[s] = __ldcg(P.ids_ws + t * d.topk + s);
-  if (threadIdx.x == 0) TRACE_POINT(8);
-  {   // the token's N scores (N is a multiple of 64: whole float4 groups)
+  const int lane = g.tid & 31, wid = g.wid;
+  if (g.tid == 0) TRACE_POINT(8);
+  {   // the token's N scores (N is a multiple of 64: whole float4 groups),
+      // then its expert ids from the inputs, sanitised as the screen does
     const float4* s4 = reinterpret_cast<const float4*>(P.score + (size_t)t * N);
     uint4* k4 = reinterpret_cast<uint4*>(keys);
-    for (int q = threadIdx.x; q < N / 4; q += kThreads) {
+    const int e_in = g.tid < d.topk ? __ldg(P.ids_in + t * d.topk + g.tid) : 0;
+    for (int q = g.tid; q < N / 4; q += NT) {
       const float4 v = __ldcg(s4 + q);
       k4[q] = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
                          __float_as_uint(v.w));
     }
+    if (g.tid < d.topk) eid[g.tid] = (e_in < 0 || e_in >= d.E) ? 0 : e_in;
   }
   // the output adds into y[t]: start it from zero while the scores come in
-  for (int h = 4 * threadIdx.x; h < d.H; h += 4 * kThreads)
+  for (int h = 4 * g.tid; h < d.H; h += 4 * NT)
     *reinterpret_cast<float4*>(P.y + (size_t)t * d.H + h) = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = threadIdx.x; i < kBins; i += kThreads) hist[i] = 0;
-  if (threadIdx.x == 0) sh[2] = 0;
-  __syncthreads();
-  if (threadIdx.x == 0) TRACE_POINT(22);
+  for (int i = g.tid; i < kBins; i += NT) hist[i] = 0;
+  if (g.tid == 0) sh[2] = 0;
+  g.sync();
+  if (g.tid == 0) TRACE_POINT(22);
 
   const bool all = k >= N, none = k <= 0;
   if (all || none) {
-    for (int n = threadIdx.x; n < N; n += kThreads) keep[n] = all;
+    for (int n = g.tid; n < N; n += NT) keep[n] = all;
   } else {
     // 1. histogram of the 12-bit digit (keys spread over hundreds of bins)
-    for (int n = threadIdx.x; n < N; n += kThreads) atomicAdd(&hist[key_digit(keys[n])], 1);
-    __syncthreads();
-    if (threadIdx.x == 0) TRACE_POINT(9);
+    for (int n = g.tid; n < N; n += NT) atomicAdd(&hist[key_digit(keys[n])], 1);
+    g.sync();
+    if (g.tid == 0) TRACE_POINT(9);
     // 2. the digit D holding the k-th largest key: 8 digits per thread, from the top
-    constexpr int kPer = kBins / kThreads;
+    constexpr int kPer = kBins / NT;
     int cnt[kPer], tot = 0;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
-      cnt[u] = hist[kBins - 1 - (threadIdx.x * kPer + u)];
+      cnt[u] = hist[kBins - 1 - (g.tid * kPer + u)];
       tot += cnt[u];
     }
     int incl = tot;
@@ -559,14 +665,14 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
       if (lane >= o) incl += v;
     }
     if (lane == 31) wsum[wid] = incl;
-    __syncthreads();
-    const int before = incl - tot + warps_before(wsum, wid, lane, nullptr);
+    g.sync();
+    const int before = incl - tot + warps_before(wsum, wid, lane, nullptr, NW);
     if (before < k && before + tot >= k) {
       int above = before;
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         if (above + cnt[u] >= k) {
-          sh[0] = kBins - 1 - (threadIdx.x * kPer + u);
+          sh[0] = kBins - 1 - (g.tid * kPer + u);
           sh[1] = k - above;       // keys of digit D that are kept
           sh[3] = cnt[u];          // keys of digit D
           break;
@@ -574,12 +680,12 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
         above += cnt[u];
       }
     }
-    __syncthreads();
+    g.sync();
     const int D = sh[0], need = sh[1], m = sh[3];
-    if (threadIdx.x == 0) TRACE_POINT(10);
+    if (g.tid == 0) TRACE_POINT(10);
     if (m <= kCandMax) {
       // 3. the candidates (digit D) ranked exactly: larger key, then lower global id
-      for (int n = threadIdx.x; n < N; n += kThreads) {
+      for (int n = g.tid; n < N; n += NT) {
         const int dg = key_digit(keys[n]);
         keep[n] = dg > D;
         if (dg == D) {
@@ -589,10 +695,10 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
           crank[c] = n;             // the channel for now; the rank below
         }
       }
-      __syncthreads();
-      if (threadIdx.x == 0) TRACE_POINT(23);
+      g.sync();
+      if (g.tid == 0) TRACE_POINT(23);
       // a warp per candidate: its lanes count the candidates ahead of it
-      for (int ci = wid; ci < m; ci += kWarps) {
+      for (int ci = wid; ci < m; ci += NW) {
         const uint32_t ki = ckey[ci], gi = cgid[ci];
         int ahead = 0;
         for (int cj = lane; cj < m; cj += 32) {
@@ -604,21 +710,21 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
       }
     } else {
       // degenerate spread (too many keys in one digit): full radix select
-      topk_radix_fallback(keys, keep, eid, N, k, I, hist, sh, wsum);
+      topk_radix_fallback(g, keys, keep, eid, N, k, I, hist, sh, wsum);
     }
   }
-  __syncthreads();
+  g.sync();
   // 4. compaction in ascending n and the kept bitmap: warp w owns a contiguous
-  if (threadIdx.x == 0) TRACE_POINT(11);
+  if (g.tid == 0) TRACE_POINT(11);
   //    range of whole 32-channel words; one ballot per word
   const int words = N / 32;
-  const int wper = (words + kWarps - 1) / kWarps;
+  const int wper = (words + NW - 1) / NW;
   const int w0 = wid * wper, w1 = min(words, w0 + wper);
   int mine = 0;
   for (int wd = w0; wd < w1; ++wd) mine += __popc(__ballot_sync(0xffffffffu, keep[wd * 32 + lane]));
   if (lane == 0) wsum[wid] = mine;
-  __syncthreads();
-  int pos = warps_before(wsum, wid, lane, nullptr);
+  g.sync();
+  int pos = warps_before(wsum, wid, lane, nullptr, NW);
   const uint32_t below = (1u << lane) - 1u;
   for (int wd = w0; wd < w1; ++wd) {
     const int n = wd * 32 + lane;
@@ -630,9 +736,9 @@ __device__ void topk_token(const Params& P, int t, unsigned char* smem) {
     if (lane == 0) P.keptbits[(size_t)t * words + wd] = bal;
     pos += __popc(bal);
   }
-  if (threadIdx.x == 0) TRACE_POINT(24);
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  if (g.tid == 0) TRACE_POINT(24);
+  g.sync();
+  if (g.tid == 0) {
     st_release(&P.sync[sync_offsets(d).flag + t], 1u);
     TRACE_POINT(12);
   }
@@ -902,7 +1008,8 @@ __device__ void shared_select(const Params& P, unsigned char* smem) {
       };
       int need2 = 0;
       const uint32_t T = cta_radix_select(
-          U, K, [&](int u, uint32_t& key) { key = keyof(u); return true; }, hist, sh + 8, &need2);
+          cta_group(), U, K, [&](int u, uint32_t& key) { key = keyof(u); return true; }, hist, sh + 8,
+          &need2);
       int eq = 0;
       for (int u = threadIdx.x; u < U; u += kThreads) eq += keyof(u) == T;
       eq = warp_sum_i(eq);
@@ -915,7 +1022,7 @@ __device__ void shared_select(const Params& P, unsigned char* smem) {
       if (need2 < eq_total) {
         int dummy = 0;
         T2 = cta_radix_select(
-            U, need2,
+            cta_group(), U, need2,
             [&](int u, uint32_t& key) {
               if (keyof(u) != T) return false;
               key = 0xffffffffu - gidof(u);
@@ -1109,16 +1216,21 @@ __device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) 
 }
 
 // The first warp's part of screen unit uu: rotation and selection of the
-// unit's (token, block) from sigma x (xu, loaded by rotate_load), the side
-// outputs (screened set, input checks, sanitised routing, zeroed recovery
-// vector), and into `buf` the screened coordinate list, their Rx values and
-// the pair tables.  Returns the unit's expert id, clamped into range.
-__device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane, float (&xu)[4],
-                          bool xbad, int e_raw, int team) {
+// unit's (token, block) from its raw loads (in, issued by unit_issue), the
+// side outputs (screened set, input checks, sanitised routing, zeroed
+// recovery vector), and into `buf` the screened coordinate list, their Rx
+// values and the pair tables.  Returns the unit's expert id, clamped into range.
+__device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane, const UnitInput& in,
+                          int team) {
   const Dims& d = P.d;
   uint8_t* cbuf = buf + P.sp.coord_off;
   float* rbuf = reinterpret_cast<float*>(cbuf + 128);
   const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk, slot = ts % d.topk;
+  float xu[4];
+  const bool xbad = unit_finish(P, t, b, slot, lane, in, xu);
+  // the slot's expert id and weight as given (lane-distributed loads)
+  const int e_raw = __shfl_sync(0xffffffffu, slot < 32 ? in.id[0] : in.id[1], slot & 31);
+  const float w_raw = __shfl_sync(0xffffffffu, slot < 32 ? in.w[0] : in.w[1], slot & 31);
   uint32_t word[4];
   rotate_select_loaded(P, lane, xu, word);
   if (lane == 0 && team == 0) TRACE_POINT(2);
@@ -1135,16 +1247,18 @@ __device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane,
     if (lane == s4) P.mask[((size_t)t * d.nb + b) * 4 + s4] = word[s4];
   if (slot == 0 && __any_sync(0xffffffffu, xbad) && lane == 0) atomicOr(P.err, kErrXNonFinite);
   if (b == 0) {
+    // a repeated expert: an earlier slot of the token with the same id
+    const bool dup = __any_sync(0xffffffffu, (lane < slot && in.id[0] == e_raw) ||
+                                                  (lane + 32 < slot && in.id[1] == e_raw));
     if (lane == 0) {
-      int e = P.ids_in[ts];
-      const float wv = P.w_in[ts];
+      int e = e_raw;
+      const float wv = w_raw;
       uint32_t bits = 0;
       if (e < 0 || e >= d.E) {
         bits |= kErrExpertRange;
         e = 0;
       }
-      for (int s2 = 0; s2 < slot; ++s2)
-        if (P.ids_in[t * d.topk + s2] == P.ids_in[ts]) bits |= kErrExpertDup;
+      if (dup) bits |= kErrExpertDup;
       if (!(wv >= 0.f) || !isfinite(wv)) bits |= kErrWeight;
       if (bits) atomicOr(P.err, bits);
       P.ids_ws[ts] = e;
@@ -1227,9 +1341,7 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   // The first warp rotates and screens the unit's (token, block) itself, so
   // the team waits on no other CTA; it keeps the next unit's sigma x (and the
   // expert id) in registers until it writes that unit's buffer.
-  float xu[4] = {0.f, 0.f, 0.f, 0.f};
-  int enext = 0;
-  bool xbad = false;
+  UnitInput uin;
   auto load_list = [&](int uu) {
     const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
     if (P.xwait) {   // a stacked layer: token t's input comes from the layer before
@@ -1238,13 +1350,12 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
       __shfl_sync(0xffffffffu, ok, 0);   // on a timeout the abort flag ends the launch
       __syncwarp();
     }
-    xbad = rotate_load(P, t, b, ts - t * d.topk, lane, xu);
-    enext = P.ids_in[ts];
+    unit_issue(P, t, b, lane, uin);
     if (lane == 0 && team == 0) TRACE_POINT(1);
   };
   auto write_unit = [&](int n) {   // first warp: unit n's tables, coordinates and expert
     unsigned char* buf = ubuf + (size_t)(n & 1) * sp.buf_bytes;
-    const int e = build_unit(P, buf, unit_of(n), lane, xu, xbad, enext, team);
+    const int e = build_unit(P, buf, unit_of(n), lane, uin, team);
     if (lane == 0) flag[2 + (n & 1)] = e;
   };
   // asynchronous copies of chunk j (unit j / nch, chunk j % nch) into stage j % 2
@@ -1450,12 +1561,13 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
 }
 
 // Phase 1a of a CTA: its teams' screen units, WPT code words per thread.
+// fg: the warps that screen (the table is built between its barriers).
 template <int WPT, bool T5>
-__device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
+__device__ void screen_compute(const Params& P, unsigned char* smem, int warp, const Grp& fg) {
   const ScreenPlan& sp = P.sp;
   const uint32_t e5_base = smem_addr(smem + sp.e5_off);
   if (T5) {   // the expansion table of a five-trit byte: its five 2-bit codes a nibble apart
-    for (int v = threadIdx.x; v < 256; v += kThreads) {   // bytes above 242 do not occur: 0
+    for (int v = fg.tid; v < 256; v += fg.nt) {   // bytes above 242 do not occur: 0
       uint32_t z = 0;
       int q = v < 243 ? v : 0;
 #pragma unroll
@@ -1466,7 +1578,7 @@ __device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
       }
       reinterpret_cast<uint32_t*>(smem + sp.e5_off)[v] = z;
     }
-    __syncthreads();
+    fg.sync();
   }
   const int team = warp / sp.tw;
   if (team >= sp.nteams) return;   // warps left over by the team size
@@ -1479,7 +1591,7 @@ __device__ void screen_compute(const Params& P, unsigned char* smem, int warp) {
 // -1 on abort, 1 when this was the token's last slot to be scored (the CTA
 // then runs the token's top-k), else 0.
 template <bool SH>
-__device__ int score_task(const Params& P, int ts, int* flag, unsigned char* smem) {
+__device__ int score_task(const Params& P, const Grp& grp, int ts, int* flag, unsigned char* smem) {
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int t = ts / d.topk, slot = ts % d.topk, I = d.I;
@@ -1489,20 +1601,20 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
   if (e < 0 || e >= d.E) e = 0;
   const float wv = P.w_in[ts];
   float dn0[2] = {0.f, 0.f};
-  if (threadIdx.x < I) dn0[0] = __ldg(P.dnorm + (size_t)e * I + threadIdx.x);
-  if (threadIdx.x + kThreads < I) dn0[1] = __ldg(P.dnorm + (size_t)e * I + threadIdx.x + kThreads);
-  if (threadIdx.x == 0)
+  if (grp.tid < I) dn0[0] = __ldg(P.dnorm + (size_t)e * I + grp.tid);
+  if (grp.tid + grp.nt < I) dn0[1] = __ldg(P.dnorm + (size_t)e * I + grp.tid + grp.nt);
+  if (grp.tid == 0)
     *flag = wait_at_least(P, P.sync + so.slot + ts, (uint32_t)(d.nb * P.sp.tw + P.stall));
-  __syncthreads();
+  grp.sync();
   if (!*flag) return -1;
-  if (threadIdx.x == 0) TRACE_POINT(6);
+  if (grp.tid == 0) TRACE_POINT(6);
   const float* pg0 = P.partial + ((size_t)ts * d.nb) * 2 * I;
-  // channels i and i + kThreads together: all their block loads first, then
+  // channels i and i + grp.nt together: all their block loads first, then
   // the sums in block order
-  for (int i = threadIdx.x; i < I; i += 2 * kThreads) {
-    const int i2 = i + kThreads;
+  for (int i = grp.tid; i < I; i += 2 * grp.nt) {
+    const int i2 = i + grp.nt;
     const bool two = i2 < I;
-    const bool first = i < kThreads;
+    const bool first = i < grp.nt;
     const float dn[2] = {first ? dn0[0] : __ldg(P.dnorm + (size_t)e * I + i),
                          two ? (first ? dn0[1] : __ldg(P.dnorm + (size_t)e * I + i2)) : 0.f};
     float g[2] = {0.f, 0.f}, v[2] = {0.f, 0.f};
@@ -1535,7 +1647,7 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
         v[1] += __ldcg(pb + I + i2);
       }
     }
-    if (threadIdx.x == 0) TRACE_POINT(21);
+    if (grp.tid == 0) TRACE_POINT(21);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (h == 1 && !two) break;
@@ -1567,22 +1679,22 @@ __device__ int score_task(const Params& P, int ts, int* flag, unsigned char* sme
       P.score[o] = sc;
     }
   }
-  __syncthreads();
+  grp.sync();
   if (SH) {
     // every output chunk of the batch adds into y[t]: start it from zero
     // before the batch's set is released
     if (slot == 0)
-      for (int h = threadIdx.x; h < d.H; h += kThreads) P.y[(size_t)t * d.H + h] = 0.f;
+      for (int h = grp.tid; h < d.H; h += grp.nt) P.y[(size_t)t * d.H + h] = 0.f;
     shared_after_score(P, e, smem, flag);
     return 0;
   }
-  if (threadIdx.x == 0) {
+  if (grp.tid == 0) {
     // releases this slot's scores; the last slot in also acquires the others'
     const uint32_t prev = atom_add_acq_rel(P.sync + so.tok + t, 1u);
     *flag = prev == (uint32_t)(d.topk - 1);
     TRACE_POINT(7);
   }
-  __syncthreads();
+  grp.sync();
   return *flag ? 1 : 0;
 }
 
@@ -1615,6 +1727,23 @@ struct TokenSlots {
   int e0, e1;
   float w0, w1;
 };
+
+// Token t's routing, lane-distributed, from the inputs, with the screen's
+// sanitising (an expert id out of range reads as expert 0): independent of
+// the decode's own writes, so it can be requested before any wait.
+__device__ __forceinline__ TokenSlots input_token_slots(const Params& P, int t, int lane) {
+  const Dims& d = P.d;
+  TokenSlots ts;
+  ts.e0 = lane < d.topk ? __ldg(P.ids_in + t * d.topk + lane) : 0;
+  ts.e1 = lane + 32 < d.topk ? __ldg(P.ids_in + t * d.topk + lane + 32) : 0;
+  ts.w0 = lane < d.topk ? __ldg(P.w_in + t * d.topk + lane) : 0.f;
+  ts.w1 = lane + 32 < d.topk ? __ldg(P.w_in + t * d.topk + lane + 32) : 0.f;
+  return ts;
+}
+__device__ __forceinline__ void sanitise_slots(const Dims& d, TokenSlots& ts) {
+  if (ts.e0 < 0 || ts.e0 >= d.E) ts.e0 = 0;
+  if (ts.e1 < 0 || ts.e1 >= d.E) ts.e1 = 0;
+}
 
 __device__ __forceinline__ TokenSlots load_token_slots(const Params& P, int t, int lane) {
   const Dims& d = P.d;
@@ -1783,11 +1912,6 @@ __device__ void kept_item_cta(const Params& P, int t, int qi, int n, const Token
   const uint4* v4 = reinterpret_cast<const uint4*>(P.V + row * d.H);
   const float4* x4 = reinterpret_cast<const float4*>(P.x + (size_t)t * d.H);
   const int n8 = d.H / 8;
-  {
-    const uint4* d4 = reinterpret_cast<const uint4*>(P.Dt + row * d.H);
-    for (int l8 = 8 * lane; l8 < n8; l8 += 256)   // one prefetch per 128-byte line of the down row
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(d4 + l8));
-  }
   float sg = 0.f, sv = 0.f;
   int h8 = lane;
   constexpr int kU = 8;   // 16-byte loads per lane and row issued together
@@ -1858,14 +1982,15 @@ __device__ __forceinline__ void axpy8h(float c, const uint4& v, float* acc) {
 // warp loads its rows' 16-byte down pieces kO at a time, sums them in
 // registers and adds its 8 columns into y once.
 __device__ void cta_output(const Params& P, int t, int q0, int q1, const float* wa_s,
-                           const int* row_s, int s0, const TokenSlots& sl, int warp, int lane) {
+                           const int* row_s, int s0, const TokenSlots& sl, int warp, int lane,
+                           int nw = kWarps) {
   const Dims& d = P.d;
   const int nchunk = (d.H + kOutCols - 1) / kOutCols;
-  const int rsplit = max(1, kWarps / nchunk);          // warps per chunk
+  const int rsplit = max(1, nw / nchunk);              // warps per chunk
   const int nr = q1 - q0, per = (nr + rsplit - 1) / rsplit;
   const uint64_t pol = policy_evict_first();            // the last read of these rows
   constexpr int kO = 12;
-  for (int wi = warp; wi < nchunk * rsplit; wi += kWarps) {
+  for (int wi = warp; wi < nchunk * rsplit; wi += nw) {
     const int ch = wi % nchunk, part = wi / nchunk;
     const int r_lo = q0 + part * per, r_hi = min(q1, r_lo + per);
     if (r_lo >= r_hi) continue;
@@ -2207,9 +2332,59 @@ __device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane) {
 
 // ------------------------------- the kernel --------------------------------
 // One layer's decode by every CTA of the grid.  false: the launch is aborting.
+// The end of a decode by a CTA: the last CTA out resets the synchronisation
+// area for the next call.  Every thread of the CTA calls it.
+template <bool SH>
+__device__ void decode_tail(const Params& P, int* ctl) {
+  const Dims& d = P.d;
+  const SyncOff so = sync_offsets(d);
+  const int nctas = gridDim.x;
+  // the last CTA out resets the synchronisation area for the next call
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    ctl[0] = atomicAdd(P.sync + kSyncDone, 1u) == (uint32_t)(nctas - 1);
+  }
+  __syncthreads();
+  if (ctl[0]) {
+    for (int i = threadIdx.x; i < P.B * d.topk; i += kThreads) P.sync[so.slot + i] = 0u;
+    for (int i = threadIdx.x; i < P.B; i += kThreads) {
+      P.sync[so.tok + i] = 0u;
+      P.sync[so.flag + i] = 0u;
+      P.sync[so.exact + i] = 0u;
+    }
+    if (P.hnext) {
+      const int ncb = (d.H + kOutCols - 1) / kOutCols;
+      for (int i = threadIdx.x; i < P.B * ncb; i += kThreads) P.sync[so.cbdone + i] = 0u;
+      for (int i = threadIdx.x; i < P.B; i += kThreads) {
+        P.sync[so.tokdone + i] = 0u;
+        P.sync[so.xready + i] = 0u;
+        P.sync[so.ssum + 2 * i] = 0u;
+        P.sync[so.ssum + 2 * i + 1] = 0u;
+      }
+    }
+    if (threadIdx.x == 0) {
+      if (SH) {
+        for (int q = 0; q < d.E; ++q) P.sync[so.ecount + q] = 0u;
+        P.sync[kSyncBatch] = 0u;
+        P.sync[kSyncReady] = 0u;
+        P.sync[kSyncSdone] = 0u;
+      }
+      P.sync[kSyncDone] = 0u;
+    }
+  }
+  __syncthreads();   // ctl is reused by the next layer
+}
+
+// Static shared control words of a CTA: [0] the last-CTA test, [1] a
+// broadcast flag, then the shared waits of phase 2 for the first kTokWait
+// tokens of the CTA's item range (seen words, then claim words).
+constexpr int kTokWait = 8, kCtlWords = 2 + 2 * kTokWait;
+
 template <bool SH, int WPT, bool T5>
 __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* smem, int* ctl) {
   if (threadIdx.x == 0) ctl[0] = 0;
+  if (threadIdx.x < 2 * kTokWait) ctl[2 + threadIdx.x] = 0;   // ordered by the barrier after the screen
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -2219,7 +2394,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   if (threadIdx.x == 0) TRACE_POINT(0);
 
   // phase 1a: screen units (rotation, selection and sketch sums), computed by teams of warps
-  screen_compute<WPT, T5>(P, smem, warp);
+  screen_compute<WPT, T5>(P, smem, warp, cta_group());
   __syncthreads();
   if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(5);
@@ -2228,9 +2403,9 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   {
     int* flag = &ctl[1];   // static shared memory: the top-k's working area starts at smem
     for (int ts = blockIdx.x; ts < P.B * d.topk; ts += nctas) {
-      const int r = score_task<SH>(P, ts, flag, smem);
+      const int r = score_task<SH>(P, cta_group(), ts, flag, smem);
       if (r < 0) return false;
-      if (!SH && r > 0) topk_token(P, ts / d.topk, smem);
+      if (!SH && r > 0) topk_token<kThreads>(P, cta_group(), ts / d.topk, smem);
       __syncthreads();
     }
     if (SH) {
@@ -2327,21 +2502,30 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     int kbase = 0, kn_l = 0;   // lane j: kept index at list position kbase + j
     TokenSlots sl{};
     bool ok = true;
+    const int tf_cta = (int)(cq0 / per_tok);   // the first token of the CTA's range
     for (long long q = q0; q < q1; ++q) {
       const int t = (int)(q / per_tok), local = (int)(q % per_tok);
       if (t != cur_t) {
         if (rec_n) publish_item(P, rec_t, rec_n, lane);
         rec_n = 0;
-        int w_ok = 1;
-        if (lane == 0) w_ok = wait_at_least(P, P.sync + so.flag + t, 1u);
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        TokenSlots nsl = input_token_slots(P, t, lane);   // in flight during the wait
+        bool w_ok;
+        const int ti = t - tf_cta;
+        if (ti < kTokWait) {
+          w_ok = cta_wait(P, P.sync + so.flag + t, 1u, &ctl[2 + ti], &ctl[2 + kTokWait + ti], lane);
+        } else {
+          int o = 1;
+          if (lane == 0) o = wait_at_least(P, P.sync + so.flag + t, 1u);
+          w_ok = __shfl_sync(0xffffffffu, o, 0) != 0;
+          __syncwarp();
+        }
         if (!w_ok) {
           ok = false;
           break;
         }
-        __syncwarp();
         cur_t = t;
-        sl = load_token_slots(P, t, lane);
+        sanitise_slots(d, nsl);
+        sl = nsl;
         if (lane == 0 && warp == 0) TRACE_POINT(13);
         kbase = -64;
       }
@@ -2359,6 +2543,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       }
     }
     if (ok && rec_n) publish_item(P, rec_t, rec_n, lane);
+    if (lane == 0 && rec_n) TRACE_POINT(30);
     if (lane == 0) TRACE_POINT(14);
     if (threadIdx.x == 0) ctl[1] = 0;
     __syncthreads();
@@ -2379,6 +2564,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
         cta_output(P, t, (int)(a - (long long)t * per_tok), (int)(b - (long long)t * per_tok), wa_s,
                    row_s, (int)(a - cq0), tsl, warp, lane);
       }
+      if (lane == 0) TRACE_POINT(29);
       if (P.hnext) {   // a stacked layer: each column block the CTA completes is carried
         __syncthreads();   // every output add of the CTA precedes the counts
         const int nr = (tl - tf + 1) * ncb;
@@ -2446,41 +2632,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(16);
-  // the last CTA out resets the synchronisation area for the next call
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    ctl[0] = atomicAdd(P.sync + kSyncDone, 1u) == (uint32_t)(nctas - 1);
-  }
-  __syncthreads();
-  if (ctl[0]) {
-    for (int i = threadIdx.x; i < P.B * d.topk; i += kThreads) P.sync[so.slot + i] = 0u;
-    for (int i = threadIdx.x; i < P.B; i += kThreads) {
-      P.sync[so.tok + i] = 0u;
-      P.sync[so.flag + i] = 0u;
-      P.sync[so.exact + i] = 0u;
-    }
-    if (P.hnext) {
-      const int ncb = (d.H + kOutCols - 1) / kOutCols;
-      for (int i = threadIdx.x; i < P.B * ncb; i += kThreads) P.sync[so.cbdone + i] = 0u;
-      for (int i = threadIdx.x; i < P.B; i += kThreads) {
-        P.sync[so.tokdone + i] = 0u;
-        P.sync[so.xready + i] = 0u;
-        P.sync[so.ssum + 2 * i] = 0u;
-        P.sync[so.ssum + 2 * i + 1] = 0u;
-      }
-    }
-    if (threadIdx.x == 0) {
-      if (SH) {
-        for (int q = 0; q < d.E; ++q) P.sync[so.ecount + q] = 0u;
-        P.sync[kSyncBatch] = 0u;
-        P.sync[kSyncReady] = 0u;
-        P.sync[kSyncSdone] = 0u;
-      }
-      P.sync[kSyncDone] = 0u;
-    }
-  }
-  __syncthreads();   // ctl is reused by the next layer
+  decode_tail<SH>(P, ctl);
   return true;
 }
 
@@ -2496,14 +2648,14 @@ __device__ __forceinline__ unsigned char* aligned_smem(unsigned char* raw) {
 template <int WPT, bool T5>
 __global__ void __launch_bounds__(kThreads, 1) decode_shared_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
-  __shared__ int ctl[2];
+  __shared__ int ctl[kCtlWords];
   decode_layer<true, WPT, T5>(P, aligned_smem(smem_raw), ctl);
 }
 
 template <int WPT, bool T5>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
-  __shared__ int ctl[2];
+  __shared__ int ctl[kCtlWords];
   decode_layer<false, WPT, T5>(P, aligned_smem(smem_raw), ctl);
   if (threadIdx.x == 0) TRACE_POINT(17);
   if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
