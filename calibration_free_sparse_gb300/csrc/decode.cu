@@ -362,17 +362,18 @@ struct UnitInput {
   float w[2];       // their routing weights
 };
 
+template <bool STK>
 __device__ __forceinline__ void unit_issue(const Params& P, int t, int b, int lane, UnitInput& in) {
   const Dims& d = P.d;
   const size_t row = (size_t)t * d.H;
-  const float* src = P.xscale ? P.hres : P.x;
+  const float* src = STK ? P.hres : P.x;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int col = b * kBlock + lane + 32 * s;
     in.x[s] = col < d.H ? __ldcg(src + row + col) : 0.f;
     in.sg[s] = P.sigma[col];
   }
-  in.f = P.xscale ? __ldcg(P.xscale + t) : 1.f;
+  in.f = STK ? __ldcg(P.xscale + t) : 1.f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int sl = lane + 32 * h;
@@ -383,6 +384,7 @@ __device__ __forceinline__ void unit_issue(const Params& P, int t, int b, int la
 
 // sigma x into u; true: x held a NaN or an infinity.  A stacked layer's slot-0
 // unit writes x = h * scale out for the rest of the layer.
+template <bool STK>
 __device__ __forceinline__ bool unit_finish(const Params& P, int t, int b, int slot, int lane,
                                             const UnitInput& in, float (&u)[4]) {
   const Dims& d = P.d;
@@ -392,7 +394,7 @@ __device__ __forceinline__ bool unit_finish(const Params& P, int t, int b, int s
   for (int s = 0; s < 4; ++s) {
     const int col = b * kBlock + lane + 32 * s;
     float xv = in.x[s];
-    if (P.xscale) {
+    if (STK) {
       xv = col < d.H ? xv * in.f : 0.f;
       if (slot == 0 && col < d.H) P.xfill[row + col] = xv;
     }
@@ -1220,6 +1222,7 @@ __device__ __forceinline__ void publish_unit(const Params& P, int ts, int lane) 
 // side outputs (screened set, input checks, sanitised routing, zeroed
 // recovery vector), and into `buf` the screened coordinate list, their Rx
 // values and the pair tables.  Returns the unit's expert id, clamped into range.
+template <bool STK>
 __device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane, const UnitInput& in,
                           int team) {
   const Dims& d = P.d;
@@ -1227,7 +1230,7 @@ __device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane,
   float* rbuf = reinterpret_cast<float*>(cbuf + 128);
   const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk, slot = ts % d.topk;
   float xu[4];
-  const bool xbad = unit_finish(P, t, b, slot, lane, in, xu);
+  const bool xbad = unit_finish<STK>(P, t, b, slot, lane, in, xu);
   // the slot's expert id and weight as given (lane-distributed loads)
   const int e_raw = __shfl_sync(0xffffffffu, slot < 32 ? in.id[0] : in.id[1], slot & 31);
   const float w_raw = __shfl_sync(0xffffffffu, slot < 32 ? in.w[0] : in.w[1], slot & 31);
@@ -1311,7 +1314,7 @@ __device__ int build_unit(const Params& P, unsigned char* buf, int uu, int lane,
 // (16 channels each) and sums them in registers, two coordinates per table
 // read.  A warp publishes a unit once the next one is computed, so the
 // release finds the stores long done.
-template <int WPT, bool T5>
+template <int WPT, bool T5, bool STK>
 __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int tt,
                             uint32_t e5_base) {
   const Dims& d = P.d;
@@ -1344,18 +1347,18 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
   UnitInput uin;
   auto load_list = [&](int uu) {
     const int b = uu % d.nb, ts = uu / d.nb, t = ts / d.topk;
-    if (P.xwait) {   // a stacked layer: token t's input comes from the layer before
+    if (STK) {   // a stacked layer: token t's input comes from the layer before
       int ok = 1;
       if (lane == 0) ok = wait_at_least(P, P.xwait + t, 1u);
       __shfl_sync(0xffffffffu, ok, 0);   // on a timeout the abort flag ends the launch
       __syncwarp();
     }
-    unit_issue(P, t, b, lane, uin);
+    unit_issue<STK>(P, t, b, lane, uin);
     if (lane == 0 && team == 0) TRACE_POINT(1);
   };
   auto write_unit = [&](int n) {   // first warp: unit n's tables, coordinates and expert
     unsigned char* buf = ubuf + (size_t)(n & 1) * sp.buf_bytes;
-    const int e = build_unit(P, buf, unit_of(n), lane, uin, team);
+    const int e = build_unit<STK>(P, buf, unit_of(n), lane, uin, team);
     if (lane == 0) flag[2 + (n & 1)] = e;
   };
   // asynchronous copies of chunk j (unit j / nch, chunk j % nch) into stage j % 2
@@ -1562,7 +1565,7 @@ __device__ void screen_team(const Params& P, unsigned char* tsm, int team, int t
 
 // Phase 1a of a CTA: its teams' screen units, WPT code words per thread.
 // fg: the warps that screen (the table is built between its barriers).
-template <int WPT, bool T5>
+template <int WPT, bool T5, bool STK>
 __device__ void screen_compute(const Params& P, unsigned char* smem, int warp, const Grp& fg) {
   const ScreenPlan& sp = P.sp;
   const uint32_t e5_base = smem_addr(smem + sp.e5_off);
@@ -1583,7 +1586,7 @@ __device__ void screen_compute(const Params& P, unsigned char* smem, int warp, c
   const int team = warp / sp.tw;
   if (team >= sp.nteams) return;   // warps left over by the team size
   const int tt = (warp % sp.tw) * 32 + (threadIdx.x & 31);
-  screen_team<WPT, T5>(P, smem + (size_t)team * sp.team_bytes, team, tt, e5_base);
+  screen_team<WPT, T5, STK>(P, smem + (size_t)team * sp.team_bytes, team, tt, e5_base);
 }
 
 // Score the channels of one (token, slot) once all its blocks are in: sum
@@ -2381,7 +2384,8 @@ __device__ void decode_tail(const Params& P, int* ctl) {
 // tokens of the CTA's item range (seen words, then claim words).
 constexpr int kTokWait = 8, kCtlWords = 2 + 2 * kTokWait;
 
-template <bool SH, int WPT, bool T5>
+// STK: a layer of a stack (its input and residual come from the layer before).
+template <bool SH, int WPT, bool T5, bool STK>
 __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* smem, int* ctl) {
   if (threadIdx.x == 0) ctl[0] = 0;
   if (threadIdx.x < 2 * kTokWait) ctl[2 + threadIdx.x] = 0;   // ordered by the barrier after the screen
@@ -2394,7 +2398,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   if (threadIdx.x == 0) TRACE_POINT(0);
 
   // phase 1a: screen units (rotation, selection and sketch sums), computed by teams of warps
-  screen_compute<WPT, T5>(P, smem, warp, cta_group());
+  screen_compute<WPT, T5, STK>(P, smem, warp, cta_group());
   __syncthreads();
   if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(5);
@@ -2565,7 +2569,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
                    row_s, (int)(a - cq0), tsl, warp, lane);
       }
       if (lane == 0) TRACE_POINT(29);
-      if (P.hnext) {   // a stacked layer: each column block the CTA completes is carried
+      if (STK) {   // a stacked layer: each column block the CTA completes is carried
         __syncthreads();   // every output add of the CTA precedes the counts
         const int nr = (tl - tf + 1) * ncb;
         for (int r = threadIdx.x; r < nr; r += kThreads) {
@@ -2588,7 +2592,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       const int t = it / (ncb * rec);
       const int cb = (it / rec) % ncb;
       if (!uc_item(P, t, cb, it % rec, lane)) break;
-      if (P.hnext) {   // a stacked layer: the block's last contribution carries it
+      if (STK) {   // a stacked layer: the block's last contribution carries it
         __syncwarp();
         int last = 0;
         if (lane == 0)
@@ -2649,16 +2653,16 @@ template <int WPT, bool T5>
 __global__ void __launch_bounds__(kThreads, 1) decode_shared_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[kCtlWords];
-  decode_layer<true, WPT, T5>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<true, WPT, T5, false>(P, aligned_smem(smem_raw), ctl);
 }
 
-template <int WPT, bool T5>
+template <int WPT, bool T5, bool STK>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
   extern __shared__ __align__(256) unsigned char smem_raw[];
   __shared__ int ctl[kCtlWords];
-  decode_layer<false, WPT, T5>(P, aligned_smem(smem_raw), ctl);
+  decode_layer<false, WPT, T5, STK>(P, aligned_smem(smem_raw), ctl);
   if (threadIdx.x == 0) TRACE_POINT(17);
-  if (P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
+  if (STK && P.next_abort && threadIdx.x == 0 && ld_acquire(P.sync + kSyncAbort)) {
     // the next layer would wait for inputs that never come
     atomicOr(P.next_err, kErrTimeout);
     atomicExch(P.next_abort, 1u);
@@ -2668,16 +2672,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const Params P) {
 using KernelFn = void (*)(const Params);
 
 template <bool T5>
-KernelFn pick_kernel_t(bool shared, int wpt) {
+KernelFn pick_kernel_t(bool shared, int wpt, bool stack) {
   if (shared)
     return wpt == 1 ? decode_shared_kernel<1, T5> : wpt == 2 ? decode_shared_kernel<2, T5> : decode_shared_kernel<3, T5>;
-  return wpt == 1 ? decode_kernel<1, T5> : wpt == 2 ? decode_kernel<2, T5> : decode_kernel<3, T5>;
+  if (stack)
+    return wpt == 1 ? decode_kernel<1, T5, true> : wpt == 2 ? decode_kernel<2, T5, true> : decode_kernel<3, T5, true>;
+  return wpt == 1 ? decode_kernel<1, T5, false> : wpt == 2 ? decode_kernel<2, T5, false> : decode_kernel<3, T5, false>;
 }
 
-// The kernel for a decode: shared selection or not, the screen's code words
-// per thread and the code layout (2-bit or five trits per byte).
-KernelFn pick_kernel(bool shared, int wpt, bool t5) {
-  return t5 ? pick_kernel_t<true>(shared, wpt) : pick_kernel_t<false>(shared, wpt);
+// The kernel for a decode: shared selection or not, a stacked layer or not,
+// the screen's code words per thread and the code layout (2-bit or five
+// trits per byte).
+KernelFn pick_kernel(bool shared, int wpt, bool t5, bool stack = false) {
+  return t5 ? pick_kernel_t<true>(shared, wpt, stack) : pick_kernel_t<false>(shared, wpt, stack);
 }
 
 size_t decode_smem_bytes(const Dims& d) {
@@ -2716,8 +2723,8 @@ cudaError_t configure_decode_kernels(const Dims& d) {
   const ScreenPlan sp = screen_plan(d);
   if (sp.bytes == 0) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes(d);
-  for (int v = 0; v < 2; ++v) {   // the shape's kernels: per-token and shared
-    const KernelFn fn = pick_kernel(v == 1, sp.wpt, d.trit5 != 0);
+  for (int v = 0; v < 3; ++v) {   // the shape's kernels: per-token, shared, stacked layer
+    const KernelFn fn = pick_kernel(v == 1, sp.wpt, d.trit5 != 0, v == 2);
     cudaFuncAttributes fa;
     cudaError_t err = cudaFuncGetAttributes(&fa, fn);
     if (err != cudaSuccess) return err;
@@ -2839,7 +2846,7 @@ static cudaError_t launch_params(const moe_reader& h, const Params& P, cudaStrea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pick_kernel(shared, P.sp.wpt, h.d.trit5 != 0), P);
+  return cudaLaunchKernelEx(&cfg, pick_kernel(shared, P.sp.wpt, h.d.trit5 != 0, P.hnext != nullptr), P);
 }
 
 cudaError_t launch_decode(const moe_reader& h, const float* x, int B, const int32_t* ids,
