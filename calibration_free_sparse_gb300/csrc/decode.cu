@@ -256,14 +256,21 @@ __host__ __device__ inline int sync_line(int w) { return (w + kSyncLine - 1) / k
 struct SyncOff {
   int slot, tok, flag, exact, cbdone, tokdone, xready, ssum, ecount, total;
 };
-// the single words: CTAs done, the launch's abort flag, and the shared
-// kernel's batch-wide hand-offs (routed experts scored, the batch's kept set
-// released, shared kept items done)
-constexpr int kSyncDone = 0, kSyncAbort = kSyncLine, kSyncBatch = 2 * kSyncLine,
-              kSyncReady = 3 * kSyncLine, kSyncSdone = 4 * kSyncLine;
+// The single words.  kSyncGen (64-bit, never reset but by the host) counts
+// the CTAs of every launch of the handle; a launch's generation is its value
+// at the launch's start divided by the grid (a CTA reads it with the add that
+// counts it, so at most grid - 1 adds of its own launch precede the read).
+// Token flags are released with generation + 1 and counters are zeroed by
+// their last reader, so a launch leaves nothing to reset; kSyncTail counts
+// the CTAs out for the end-of-launch reset of the words only the shared and
+// stacked kernels use.  Then the launch's abort flag, and the shared kernel's
+// batch-wide hand-offs (routed experts scored, the batch's kept set
+// released, shared kept items done).
+constexpr int kSyncGen = 0, kSyncAbort = kSyncLine, kSyncBatch = 2 * kSyncLine,
+              kSyncReady = 3 * kSyncLine, kSyncSdone = 4 * kSyncLine, kSyncTail = 5 * kSyncLine;
 __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   SyncOff o;
-  o.slot = 5 * kSyncLine;
+  o.slot = 6 * kSyncLine;
   o.tok = sync_line(o.slot + d.Bmax * d.topk);
   o.flag = sync_line(o.tok + d.Bmax);
   o.exact = sync_line(o.flag + d.Bmax);
@@ -276,13 +283,16 @@ __host__ __device__ inline SyncOff sync_offsets(const Dims& d) {
   return o;
 }
 
+__device__ __forceinline__ bool reached(uint32_t v, uint32_t target) {
+  return (int32_t)(v - target) >= 0;   // wrap-safe: flags carry a generation
+}
 __device__ bool wait_at_least(const Params& P, const uint32_t* flag, uint32_t target) {
-  if (ld_acquire(flag) >= target) return true;
+  if (reached(ld_acquire(flag), target)) return true;
   uint32_t* abort_flag = P.sync + kSyncAbort;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     // poll without ordering; the acquire load orders what follows once it is met
-    if (ld_relaxed(flag) >= target && ld_acquire(flag) >= target) return true;
+    if (reached(ld_relaxed(flag), target) && reached(ld_acquire(flag), target)) return true;
     if ((it & 7u) == 0) {   // the abort flag and the clock every eighth poll
       if (ld_relaxed(abort_flag)) return false;
       if (globaltimer() - t0 > P.wait_ns) {
@@ -608,8 +618,9 @@ __device__ __noinline__ void topk_radix_fallback(const Grp& g, const uint32_t* k
   }
 }
 
+// ftag: the launch's flag value (generation + 1).
 template <int NT>
-__device__ void topk_token(const Params& P, const Grp& g, int t, unsigned char* smem) {
+__device__ void topk_token(const Params& P, const Grp& g, int t, unsigned char* smem, uint32_t ftag) {
   constexpr int NW = NT / 32;
   const Dims& d = P.d;
   const int N = d.N, k = P.k, I = d.I;
@@ -739,9 +750,10 @@ __device__ void topk_token(const Params& P, const Grp& g, int t, unsigned char* 
     pos += __popc(bal);
   }
   if (g.tid == 0) TRACE_POINT(24);
+  if (g.tid == 0) P.sync[sync_offsets(d).exact + t] = 0u;   // counted by items after the release
   g.sync();
   if (g.tid == 0) {
-    st_release(&P.sync[sync_offsets(d).flag + t], 1u);
+    st_release(&P.sync[sync_offsets(d).flag + t], ftag);
     TRACE_POINT(12);
   }
 }
@@ -1146,7 +1158,7 @@ __device__ void shared_after_score(const Params& P, int e, unsigned char* smem, 
 
 // Token t's share of the batch's set: its kept bitmap and ascending kept list
 // (n = slot I + i) and their count; y[t] zeroed; then the token is released.
-__device__ void shared_token(const Params& P, int t, unsigned char* smem) {
+__device__ void shared_token(const Params& P, int t, unsigned char* smem, uint32_t ftag) {
   const Dims& d = P.d;
   const int IW = d.I / 32, words = d.N / 32;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -1177,9 +1189,12 @@ __device__ void shared_token(const Params& P, int t, unsigned char* smem) {
     if ((bw >> lane) & 1u) P.kept[(size_t)t * d.N + pos + __popc(bw & below)] = wd * 32 + lane;
     pos += __popc(bw);
   }
-  if (threadIdx.x == 0) P.kcount[t] = total;
+  if (threadIdx.x == 0) {
+    P.kcount[t] = total;
+    P.sync[sync_offsets(d).exact + t] = 0u;   // counted by items after the release
+  }
   __syncthreads();
-  if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], 1u);
+  if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], ftag);
 }
 
 // ------------------------------- phase 1 -----------------------------------
@@ -1606,8 +1621,10 @@ __device__ int score_task(const Params& P, const Grp& grp, int ts, int* flag, un
   float dn0[2] = {0.f, 0.f};
   if (grp.tid < I) dn0[0] = __ldg(P.dnorm + (size_t)e * I + grp.tid);
   if (grp.tid + grp.nt < I) dn0[1] = __ldg(P.dnorm + (size_t)e * I + grp.tid + grp.nt);
-  if (grp.tid == 0)
+  if (grp.tid == 0) {
     *flag = wait_at_least(P, P.sync + so.slot + ts, (uint32_t)(d.nb * P.sp.tw + P.stall));
+    if (*flag) P.sync[so.slot + ts] = 0u;   // every unit is in: the count is not read again
+  }
   grp.sync();
   if (!*flag) return -1;
   if (grp.tid == 0) TRACE_POINT(6);
@@ -1695,6 +1712,7 @@ __device__ int score_task(const Params& P, const Grp& grp, int ts, int* flag, un
     // releases this slot's scores; the last slot in also acquires the others'
     const uint32_t prev = atom_add_acq_rel(P.sync + so.tok + t, 1u);
     *flag = prev == (uint32_t)(d.topk - 1);
+    if (*flag) P.sync[so.tok + t] = 0u;   // the token's last slot: no more adds
     TRACE_POINT(7);
   }
   grp.sync();
@@ -2084,6 +2102,7 @@ __device__ void carry_block(const Params& P, int t, int cb, int ncb, int lane) {
 // (rows known) and the token whose phase-2 items it has seen counted (kept
 // weights and the recovery vector known).
 struct OutWait {
+  uint32_t ftag = 1;   // the launch's flag value
   int flag_t = -1, count_t = -1;
   TokenSlots sl{};
   int kt = 0;          // the shared kernel: kept channels of token flag_t
@@ -2110,6 +2129,8 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
   const float* wa_t = P.wa + (size_t)t * d.N;
   auto counted = [&]() {
     if (ow.count_t == t) return true;
+    // the token's flag first: its count is zeroed before the flag's release
+    if (!out_wait(P, P.sync + so.flag + t, ow.ftag, lane)) return false;
     if (!out_wait(P, P.sync + so.exact + t, (uint32_t)per_tok, lane)) return false;
     if (lane == 0) TRACE_POINT(15);
     if (SH && !ow.shared_in) {
@@ -2130,6 +2151,7 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
       for (int u = 0; u < kOutBatch; ++u)
         v[u] = u < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(j0 + u) * d.H + c0))
                             : make_uint4(0u, 0u, 0u, 0u);
+      if (!out_wait(P, P.sync + so.flag + t, ow.ftag, lane)) return false;
       if (!out_wait(P, P.sync + so.exact + t, (uint32_t)per_tok, lane)) return false;
       const float cj_l = lane < nj ? __ldcg(P.cvec + (size_t)t * d.r + j0 + lane) : 0.f;
 #pragma unroll
@@ -2161,7 +2183,7 @@ __device__ bool out_chunk(const Params& P, const OutPlan& op, int t, int cb, int
     // the rows come from the kept list and the expert ids alone (known at the
     // top-k): their loads go out before the token's phase-2 items are counted
     if (ow.flag_t != t) {
-      if (!out_wait(P, P.sync + so.flag + t, 1u, lane)) return false;
+      if (!out_wait(P, P.sync + so.flag + t, ow.ftag, lane)) return false;
       ow.flag_t = t;
       ow.sl = load_token_slots(P, t, lane);
       if (SH) ow.kt = __ldcg(P.kcount + t);
@@ -2304,7 +2326,7 @@ __device__ bool shared_out_chunk(const Params& P, int c, int cb, int RCs, int K,
 // Recovery output chunk rc of token t on column block cb (the per-token
 // kernel): y += rank components rc*kOutBatch .. of U c, the U^T rows weighted
 // by c, once the token's recovery chunks are counted; the U^T rows load first.
-__device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane) {
+__device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane, uint32_t ftag) {
   const Dims& d = P.d;
   const int c0 = cb * kOutCols + lane * 8;
   const bool on = c0 < d.H;                  // H is a multiple of 8
@@ -2314,6 +2336,8 @@ __device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane) {
   for (int u = 0; u < kOutBatch; ++u)
     v[u] = u < nj && on ? __ldg(reinterpret_cast<const uint4*>(P.Ut + (size_t)(j0 + u) * d.H + c0))
                         : make_uint4(0u, 0u, 0u, 0u);
+  // the token's flag first: its recovery count is zeroed before the flag's release
+  if (!out_wait(P, P.sync + sync_offsets(d).flag + t, ftag, lane)) return false;
   if (!out_wait(P, P.sync + sync_offsets(d).exact + t, (uint32_t)(d.N / 64), lane)) return false;
   if (lane == 0) TRACE_POINT(15);
   const float cj_l = lane < nj ? __ldcg(P.cvec + (size_t)t * d.r + j0 + lane) : 0.f;
@@ -2335,28 +2359,22 @@ __device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane) {
 
 // ------------------------------- the kernel --------------------------------
 // One layer's decode by every CTA of the grid.  false: the launch is aborting.
-// The end of a decode by a CTA: the last CTA out resets the synchronisation
-// area for the next call.  Every thread of the CTA calls it.
-template <bool SH>
+// The end of a shared-selection or stacked-layer decode by a CTA: the last
+// CTA out resets the words only those kernels use (the words every kernel
+// uses need no reset: see kSyncGen).  Every thread of the CTA calls it.
+template <bool SH, bool STK>
 __device__ void decode_tail(const Params& P, int* ctl) {
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
   const int nctas = gridDim.x;
-  // the last CTA out resets the synchronisation area for the next call
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    ctl[0] = atomicAdd(P.sync + kSyncDone, 1u) == (uint32_t)(nctas - 1);
+    ctl[0] = atomicAdd(P.sync + kSyncTail, 1u) == (uint32_t)(nctas - 1);
   }
   __syncthreads();
   if (ctl[0]) {
-    for (int i = threadIdx.x; i < P.B * d.topk; i += kThreads) P.sync[so.slot + i] = 0u;
-    for (int i = threadIdx.x; i < P.B; i += kThreads) {
-      P.sync[so.tok + i] = 0u;
-      P.sync[so.flag + i] = 0u;
-      P.sync[so.exact + i] = 0u;
-    }
-    if (P.hnext) {
+    if (STK) {
       const int ncb = (d.H + kOutCols - 1) / kOutCols;
       for (int i = threadIdx.x; i < P.B * ncb; i += kThreads) P.sync[so.cbdone + i] = 0u;
       for (int i = threadIdx.x; i < P.B; i += kThreads) {
@@ -2373,16 +2391,23 @@ __device__ void decode_tail(const Params& P, int* ctl) {
         P.sync[kSyncReady] = 0u;
         P.sync[kSyncSdone] = 0u;
       }
-      P.sync[kSyncDone] = 0u;
+      P.sync[kSyncTail] = 0u;
     }
   }
-  __syncthreads();   // ctl is reused by the next layer
+  __syncthreads();
 }
 
 // Static shared control words of a CTA: [0] the last-CTA test, [1] a
 // broadcast flag, then the shared waits of phase 2 for the first kTokWait
-// tokens of the CTA's item range (seen words, then claim words).
-constexpr int kTokWait = 8, kCtlWords = 2 + 2 * kTokWait;
+// tokens of the CTA's item range (seen words, then claim words), then the
+// launch's flag value (generation + 1).
+constexpr int kTokWait = 8, kCtlFtag = 2 + 2 * kTokWait, kCtlWords = kCtlFtag + 1;
+
+__device__ __forceinline__ unsigned long long atom_add_u64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
 
 // STK: a layer of a stack (its input and residual come from the layer before).
 template <bool SH, int WPT, bool T5, bool STK>
@@ -2396,10 +2421,15 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   unsigned long long* stamp = P.stamps ? P.stamps + (size_t)blockIdx.x * 5 : nullptr;
   if (stamp && threadIdx.x == 0) stamp[0] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(0);
+  // the launch's generation: requested now, first needed after the screen
+  unsigned long long gen_in = 0;
+  if (threadIdx.x == 0) gen_in = atom_add_u64(reinterpret_cast<unsigned long long*>(P.sync + kSyncGen), 1ull);
 
   // phase 1a: screen units (rotation, selection and sketch sums), computed by teams of warps
   screen_compute<WPT, T5, STK>(P, smem, warp, cta_group());
+  if (threadIdx.x == 0) ctl[kCtlFtag] = (int)(uint32_t)(gen_in / (unsigned long long)nctas + 1ull);
   __syncthreads();
+  const uint32_t ftag = (uint32_t)ctl[kCtlFtag];
   if (stamp && threadIdx.x == 0) stamp[1] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(5);
   // phase 1b: scoring tasks spread over the CTAs; the CTA that scores a
@@ -2409,7 +2439,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     for (int ts = blockIdx.x; ts < P.B * d.topk; ts += nctas) {
       const int r = score_task<SH>(P, cta_group(), ts, flag, smem);
       if (r < 0) return false;
-      if (!SH && r > 0) topk_token<kThreads>(P, cta_group(), ts / d.topk, smem);
+      if (!SH && r > 0) topk_token<kThreads>(P, cta_group(), ts / d.topk, smem, ftag);
       __syncthreads();
     }
     if (SH) {
@@ -2420,7 +2450,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
           *flag = wait_at_least(P, P.sync + kSyncReady, 1u);
         __syncthreads();
         if (!*flag) return false;
-        shared_token(P, t, smem);
+        shared_token(P, t, smem, ftag);
         __syncthreads();
       }
     }
@@ -2461,7 +2491,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
       const int t = (int)(r / per_tok), ch = (int)(r % per_tok);
       if (t != cur_t) {
         int w_ok = 1;
-        if (lane == 0) w_ok = wait_at_least(P, P.sync + so.flag + t, 1u);
+        if (lane == 0) w_ok = wait_at_least(P, P.sync + so.flag + t, ftag);
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) {
           ok = false;
@@ -2516,10 +2546,10 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
         bool w_ok;
         const int ti = t - tf_cta;
         if (ti < kTokWait) {
-          w_ok = cta_wait(P, P.sync + so.flag + t, 1u, &ctl[2 + ti], &ctl[2 + kTokWait + ti], lane);
+          w_ok = cta_wait(P, P.sync + so.flag + t, ftag, &ctl[2 + ti], &ctl[2 + kTokWait + ti], lane);
         } else {
           int o = 1;
-          if (lane == 0) o = wait_at_least(P, P.sync + so.flag + t, 1u);
+          if (lane == 0) o = wait_at_least(P, P.sync + so.flag + t, ftag);
           w_ok = __shfl_sync(0xffffffffu, o, 0) != 0;
           __syncwarp();
         }
@@ -2591,7 +2621,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     for (int it = nwarps - 1 - (int)gw; it < items; it += nwarps) {
       const int t = it / (ncb * rec);
       const int cb = (it / rec) % ncb;
-      if (!uc_item(P, t, cb, it % rec, lane)) break;
+      if (!uc_item(P, t, cb, it % rec, lane, ftag)) break;
       if (STK) {   // a stacked layer: the block's last contribution carries it
         __syncwarp();
         int last = 0;
@@ -2625,6 +2655,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     op.RC = 0;
     op.NR = rec;
     OutWait ow;
+    ow.ftag = ftag;
     for (int it = nwarps - 1 - gw; it < items; it += nwarps) {
       if (it < C * ncb) {
         if (!shared_out_chunk(P, it / ncb, it % ncb, RCs, K, lane, ow)) break;
@@ -2636,7 +2667,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(16);
-  decode_tail<SH>(P, ctl);
+  if (SH || STK) decode_tail<SH, STK>(P, ctl);
   return true;
 }
 
