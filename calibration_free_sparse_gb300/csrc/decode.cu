@@ -262,8 +262,8 @@ struct SyncOff {
 // counts it, so at most grid - 1 adds of its own launch precede the read).
 // Token flags are released with generation + 1 and counters are zeroed by
 // their last reader, so a launch leaves nothing to reset; kSyncTail counts
-// the CTAs out for the end-of-launch reset of the words only the shared and
-// stacked kernels use.  Then the launch's abort flag, and the shared kernel's
+// the CTAs out for the end-of-launch reset of the words only the shared
+// kernel uses.  Then the launch's abort flag, and the shared kernel's
 // batch-wide hand-offs (routed experts scored, the batch's kept set
 // released, shared kept items done).
 constexpr int kSyncGen = 0, kSyncAbort = kSyncLine, kSyncBatch = 2 * kSyncLine,
@@ -1904,7 +1904,10 @@ __device__ void recovery_item(const Params& P, int t, int ch, int lane, int pend
 // contribution that completes the block (`total` of them), whose warp then
 // carries it.
 __device__ __forceinline__ bool count_block(const Params& P, int t, int cb, int ncb, uint32_t total) {
-  return atom_add_acq_rel(P.sync + sync_offsets(P.d).cbdone + t * ncb + cb, 1u) + 1u == total;
+  uint32_t* w = P.sync + sync_offsets(P.d).cbdone + t * ncb + cb;
+  if (atom_add_acq_rel(w, 1u) + 1u != total) return false;
+  *w = 0u;   // the block's last contribution: no more adds this launch
+  return true;
 }
 
 // CTAs whose item ranges hold kept channels of token t (items are dealt in
@@ -2087,6 +2090,9 @@ __device__ void carry_block(const Params& P, int t, int cb, int ncb, int lane) {
     prev = atom_add_acq_rel(P.sync + so.tokdone + t, 1u);
     if (prev == (uint32_t)(ncb - 1)) {
       const double tot = __ldcg(sum);
+      // the token's last block: its count and sum are not read again this launch
+      P.sync[so.tokdone + t] = 0u;
+      *sum = 0.0;
       P.xscale_next[t] = (float)(1.0 / sqrt(tot / d.H + 1e-6));
       st_release(P.xnext_ready + t, 1u);
     }
@@ -2359,10 +2365,10 @@ __device__ bool uc_item(const Params& P, int t, int cb, int rc, int lane, uint32
 
 // ------------------------------- the kernel --------------------------------
 // One layer's decode by every CTA of the grid.  false: the launch is aborting.
-// The end of a shared-selection or stacked-layer decode by a CTA: the last
-// CTA out resets the words only those kernels use (the words every kernel
-// uses need no reset: see kSyncGen).  Every thread of the CTA calls it.
-template <bool SH, bool STK>
+// The end of a shared-selection decode by a CTA: the last CTA out resets the
+// words only that kernel uses (the others need no reset: see kSyncGen; a
+// stacked layer's words are zeroed by their last readers).  Every thread of
+// the CTA calls it.
 __device__ void decode_tail(const Params& P, int* ctl) {
   const Dims& d = P.d;
   const SyncOff so = sync_offsets(d);
@@ -2373,26 +2379,12 @@ __device__ void decode_tail(const Params& P, int* ctl) {
     ctl[0] = atomicAdd(P.sync + kSyncTail, 1u) == (uint32_t)(nctas - 1);
   }
   __syncthreads();
-  if (ctl[0]) {
-    if (STK) {
-      const int ncb = (d.H + kOutCols - 1) / kOutCols;
-      for (int i = threadIdx.x; i < P.B * ncb; i += kThreads) P.sync[so.cbdone + i] = 0u;
-      for (int i = threadIdx.x; i < P.B; i += kThreads) {
-        P.sync[so.tokdone + i] = 0u;
-        P.sync[so.xready + i] = 0u;
-        P.sync[so.ssum + 2 * i] = 0u;
-        P.sync[so.ssum + 2 * i + 1] = 0u;
-      }
-    }
-    if (threadIdx.x == 0) {
-      if (SH) {
-        for (int q = 0; q < d.E; ++q) P.sync[so.ecount + q] = 0u;
-        P.sync[kSyncBatch] = 0u;
-        P.sync[kSyncReady] = 0u;
-        P.sync[kSyncSdone] = 0u;
-      }
-      P.sync[kSyncTail] = 0u;
-    }
+  if (ctl[0] && threadIdx.x == 0) {
+    for (int q = 0; q < d.E; ++q) P.sync[so.ecount + q] = 0u;
+    P.sync[kSyncBatch] = 0u;
+    P.sync[kSyncReady] = 0u;
+    P.sync[kSyncSdone] = 0u;
+    P.sync[kSyncTail] = 0u;
   }
   __syncthreads();
 }
@@ -2439,7 +2431,12 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
     for (int ts = blockIdx.x; ts < P.B * d.topk; ts += nctas) {
       const int r = score_task<SH>(P, cta_group(), ts, flag, smem);
       if (r < 0) return false;
-      if (!SH && r > 0) topk_token<kThreads>(P, cta_group(), ts / d.topk, smem, ftag);
+      if (!SH && r > 0) {
+        topk_token<kThreads>(P, cta_group(), ts / d.topk, smem, ftag);
+        // a stacked layer: every screen unit of the token has passed its
+        // wait for the token's input, which the layer before sets again
+        if (STK && threadIdx.x == 0) P.sync[so.xready + ts / d.topk] = 0u;
+      }
       __syncthreads();
     }
     if (SH) {
@@ -2667,7 +2664,7 @@ __device__ __forceinline__ bool decode_layer(const Params& P, unsigned char* sme
   }
   if (stamp && threadIdx.x == 0) stamp[4] = globaltimer();
   if (threadIdx.x == 0) TRACE_POINT(16);
-  if (SH || STK) decode_tail<SH, STK>(P, ctl);
+  if (SH) decode_tail(P, ctl);
   return true;
 }
 
