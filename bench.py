@@ -276,20 +276,34 @@ PHASE_BYTES = {   # algorithmic parameter arrays each decode kernel reads
 }
 
 
+def kernel_code_digest():
+    """sha256[:16] of the decode kernel's code: decode.cu and the headers it
+    includes, with comments and whitespace removed (a comment edit keeps a
+    recorded capture valid, a code edit does not)."""
+    import hashlib
+    import re
+
+    h = hashlib.sha256()
+    for name in ("decode.cu", "device_util.cuh", "internal.cuh"):
+        path = os.path.join(ROOT, "calibration_free_sparse_gb300", "csrc", name)
+        with open(path, encoding="utf-8") as f:
+            txt = f.read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        txt = re.sub(r"//[^\n]*", "", txt)
+        h.update(re.sub(r"\s+", "", txt).encode())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel, batch):
     """Per-launch DRAM bytes of `kernel` at `batch` from a committed ncu summary,
-    if the summary was taken on the current kernel sources."""
+    if the summary was taken on the current kernel code."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
-    import hashlib
-
     with open(path) as f:
         rec = json.load(f)
-    src = os.path.join(ROOT, "calibration_free_sparse_gb300", "csrc", "decode.cu")
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     ent = rec.get(kernel)
-    if not ent or ent.get("decode_cu_sha256_16") != digest or ent.get("batch") != batch:
+    if not ent or ent.get("code_sha256_16") != kernel_code_digest() or ent.get("batch") != batch:
         return None
     return ent.get("bytes_per_launch")
 

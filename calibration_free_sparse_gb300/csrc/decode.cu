@@ -5,23 +5,27 @@
 //
 // One CTA per SM, all co-resident (cooperative launch).  The phases hand work
 // to each other through counters and flags in global memory instead of
-// kernel boundaries; every wait is bounded (about one second of globaltimer),
-// after which the CTA raises the timeout bit and the abort flag and leaves.
+// kernel boundaries; every wait is bounded (one second of the global timer by
+// default), after which the CTA raises the timeout bit and the abort flag and
+// leaves.
 //
-//   phase 0  rotate x per (token, 128-block): fp32 Sylvester butterfly of
-//            sigma*x, the c largest |Rx| coordinates (ties -> lower index),
-//            routing checks; sets rot_flag[t][b]
-//   phase 1  screen unit per (token, expert slot, block): the 2-bit codes of
-//            the screened coordinates, alpha-scaled block partials of ghat and
-//            vhat.  The last unit of a (token, slot) sums the block partials in
-//            block order and scores the slot's channels,
-//            s = w ||d|| |phi(ghat) vhat|; the last slot of a token runs the
-//            exact top-k over the token's N channels (radix select on the fp32
-//            bits, ties -> lower e*I + i) and sets tok_flag[t]
+//   phase 1a screen units per (token, expert slot, block), dealt to teams of
+//            warps: the team's first warp rotates the unit's (token, block)
+//            (fp32 Sylvester butterfly of sigma x), selects the c largest |Rx|
+//            coordinates (ties -> lower index) and builds pair tables; the
+//            team sums the ternary codes of the screened coordinates into
+//            alpha-scaled block partials of ghat and vhat
+//   phase 1b score task per (token, slot): the block partials summed in block
+//            order, s = w ||d|| |phi(ghat) vhat|
+//   phase 1c the CTA that scores a token's last slot runs the exact top-k
+//            over the token's N channels (12-bit digit histogram, exact
+//            ranking of the threshold digit, ties -> lower e*I + i) and
+//            releases the token's flag
 //   phase 2  warp items: kept channels (a_j = phi(g_j.x)(v_j.x) from native
 //            BF16 rows, fp32 x) and 64-channel recovery chunks
 //            (sum w_j p_j b_j over skipped channels)
-//   phase 3  output slices of 16 columns: y = sum_K w_j a_j Dt_j + U c
+//   phase 3  each CTA adds sum_K w_j a_j Dt_j over the kept rows of its own
+//            items into y; recovery output chunks add U c
 #include <algorithm>
 
 #include "device_util.cuh"
@@ -356,7 +360,7 @@ __device__ __forceinline__ Grp cta_group() {
   return Grp{(int)threadIdx.x, kThreads, (int)(threadIdx.x >> 5), kWarps, 0};
 }
 
-// ------------------------------- phase 0 -----------------------------------
+// ------------------- rotation and screen selection (phase 1a) --------------
 // Rotation and screen selection of one (token, 128-block) by one warp: lane
 // l ends with Rx of coordinates l + 32 s (s < 4) in u[s] and with word[s] =
 // the selection bits of coordinates 32 s .. 32 s + 31 (the c largest |Rx|,
@@ -1197,7 +1201,7 @@ __device__ void shared_token(const Params& P, int t, unsigned char* smem, uint32
   if (threadIdx.x == 0) st_release(&P.sync[sync_offsets(d).flag + t], ftag);
 }
 
-// ------------------------------- phase 1 -----------------------------------
+// ------------------------------- phase 1a ----------------------------------
 // Screen units (token, slot, block) are dealt to the CTAs round-robin; all
 // cost the same.  Inside a CTA the warps form teams that each compute whole
 // units, several units side by side.  Shared memory per team: a flag area and
@@ -1972,7 +1976,7 @@ __device__ void kept_item_cta(const Params& P, int t, int qi, int n, const Token
   }
 }
 
-// ------------------------------- phase 3 -----------------------------------
+// ------------------------------- output ------------------------------------
 __device__ __forceinline__ void axpy8(float c, const uint4& v, float* acc) {
   acc[0] = fmaf(c, bf16_lo(v.x), acc[0]); acc[1] = fmaf(c, bf16_hi(v.x), acc[1]);
   acc[2] = fmaf(c, bf16_lo(v.y), acc[2]); acc[3] = fmaf(c, bf16_hi(v.y), acc[3]);
